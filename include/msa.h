@@ -1,0 +1,224 @@
+/*
+ * msa.h -- C ABI of libmsa: Multi-Segment Attention (MSA) on GB300 (sm_103a).
+ *
+ * MSA is exact attention over a paged KV cache whose live blocks form several
+ * disjoint, physically contiguous segments (AsymCache explainer, "核心方法
+ * 1. Multi-Segment Attention": the live blocks are split by physical
+ * contiguity, each segment is attended with a contiguous kernel and the
+ * per-segment results are combined; MSA paper abstract: lossless KV
+ * management must keep outputs exact, and MSA is the component that makes
+ * non-contiguous context efficient).  Evicted blocks are rebuilt on demand,
+ * so the queried positions can themselves be several disjoint ranges
+ * (recomputed holes plus a new turn).  The result equals dense causal
+ * attention over the full logical sequence:
+ *
+ *   for sequence s (L_s cached tokens), query row at position p, head h,
+ *   kv head g = h / (Hq/Hkv), visible keys j <= min(p, L_s - 1):
+ *     t_j = scale * q.K_s[j,g];  lse = ln sum_j exp(t_j);
+ *     out = sum_j exp(t_j - lse) * V_s[j,g]
+ *
+ * Three calls make up the path:
+ *   msa_plan_create / msa_plan_upload   block table + query ranges -> segment
+ *                                       runs and a work list balanced over
+ *                                       the SMs (host planner, one copy up)
+ *   msa_append_kv                       new / recomputed K,V -> paged pool
+ *   msa_attention                       one persistent launch over all
+ *                                       segments of all sequences, decode
+ *                                       and prefill/recompute rows alike,
+ *                                       with the log-sum-exp merge fused
+ *
+ * Conventions
+ *   - Every function returns MSA_OK (0) or a negative msa_status; no
+ *     exception crosses the ABI.  msa_status_string() names a code.
+ *   - Device pointers are caller-owned (e.g. torch tensors); the library
+ *     never allocates device memory.  The plan is a library-owned host
+ *     object; the workspace it needs is caller-allocated device memory.
+ *   - Device work is asynchronous on the given stream (a cudaStream_t; NULL
+ *     is the legacy default stream).
+ *   - bf16 means IEEE bfloat16 (2 bytes).  Layouts are row-major, C order.
+ *   - Pool layout ("NHD"): K and V pools are bf16 [pool_tokens, Hkv, D];
+ *     pool row = physical_block * block_size + offset_in_block.  A segment of
+ *     n blocks starting at physical block b is pool rows [b*B, (b+n)*B).
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-compatible with cudaStream_t / CUstream without pulling in CUDA headers. */
+typedef struct CUstream_st* msa_stream_t;
+
+typedef enum {
+    MSA_OK = 0,
+    MSA_ERR_INVALID_ARG = -1,       /* null pointer, negative size, bad enum      */
+    MSA_ERR_BAD_BLOCK_ID = -2,      /* block id >= 2^27 or past pool_tokens        */
+    MSA_ERR_MISSING_BLOCK = -3,     /* negative table entry inside [0, L_s)        */
+    MSA_ERR_BAD_Q_RANGE = -4,       /* empty, unsorted, overlapping, p<0 or p>L_s  */
+    MSA_ERR_WORKSPACE_TOO_SMALL = -5,
+    MSA_ERR_UNSUPPORTED_DIMS = -6,  /* D not in {64,128}, B != 16, Hq % Hkv != 0,  */
+                                    /* Hq/Hkv > 16, non-finite or <= 0 scale       */
+    MSA_ERR_CUDA = -7,              /* a CUDA runtime / driver call failed         */
+    MSA_ERR_DEVICE_CHECK = -8,      /* a kernel recorded an error (see below)      */
+    MSA_ERR_NOT_UPLOADED = -9       /* msa_attention before msa_plan_upload        */
+} msa_status;
+
+typedef enum { MSA_OUT_BF16 = 0, MSA_OUT_FP32 = 1 } msa_out_dtype;
+
+/* Attention shape.  block_size must be 16; head_dim 64 or 128;
+ * num_q_heads a multiple of num_kv_heads with at most 16 query heads per kv
+ * head (consecutive query heads share a kv head: g = h / (Hq/Hkv)). */
+typedef struct {
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    float softmax_scale; /* usually 1/sqrt(head_dim) */
+} msa_dims;
+
+typedef struct msa_plan_s* msa_plan_t;
+
+/* Summary of a plan (sizes and the algorithmic work it describes). */
+typedef struct {
+    int32_t num_seqs;
+    int32_t num_q_rows;          /* packed query rows                            */
+    int32_t num_runs;            /* segments over all sequences                  */
+    int32_t num_groups;          /* output groups (merge units)                  */
+    int32_t num_items;           /* work items                                   */
+    int32_t num_decode_items;
+    int32_t num_prefill_items;
+    int32_t num_decode_rows;     /* rows served by the decode (GQA-packed) path  */
+    int32_t num_prefill_rows;    /* rows served by the 128-row tile path         */
+    int32_t grid;                /* CTAs of the persistent launch                */
+    int64_t decode_kv_bytes;     /* K+V bytes the decode rows must read          */
+    int64_t decode_qo_bytes;     /* q in + bf16 out + fp32 lse of decode rows    */
+    double prefill_flops;        /* 4*D*sum over prefill (row, head) of n_vis(p) */
+    int64_t max_pool_row;        /* highest pool row the plan reads, plus one    */
+    double host_plan_us;         /* time msa_plan_create spent                   */
+} msa_plan_info;
+
+/*
+ * Build a plan (host only, no CUDA call except a device-attribute query when
+ * num_sms == 0).
+ *
+ *   dims             attention shape (see msa_dims)
+ *   num_seqs         S >= 0
+ *   max_blocks_per_seq  row stride of block_table; >= ceil(L_s / 16) for all s
+ *   block_table      host int32 [S][max_blocks_per_seq]: physical block of
+ *                    each logical block; entries past ceil(L_s/16) ignored
+ *                    (use -1); a negative entry inside [0, L_s) is
+ *                    MSA_ERR_MISSING_BLOCK (evicted blocks must be recomputed
+ *                    into fresh blocks before attention)
+ *   seq_lens         host int32 [S]: cached tokens L_s (>= 0); only the
+ *                    last logical block of a sequence may be partial
+ *   q_range_indptr   host int32 [S+1]: ranges of sequence s are
+ *                    q_ranges[q_range_indptr[s] .. q_range_indptr[s+1])
+ *   q_ranges         host int32 [n][2]: half-open logical position ranges
+ *                    [start, end), sorted and non-overlapping within a
+ *                    sequence, 0 <= start < end <= L_s + 1.  A row at
+ *                    p < L_s is a prefill/recompute row whose own K/V is
+ *                    already in the pool (it sees keys 0..p); a row at
+ *                    p == L_s is a decode row (it sees all L_s keys).
+ *                    Query rows are packed in (sequence, range, position)
+ *                    order: that is the row order of q, out and lse.
+ *   num_sms          SMs to balance over; 0 = query the current device
+ *   out              receives the plan (NULL on error)
+ *
+ * Segments are maximal runs of logical blocks whose physical ids rise by one
+ * per block (AsymCache explainer, "核心方法 1": split the live blocks into
+ * physically contiguous segments; holes break them).  The block table is
+ * copied: the caller may free or change it afterwards, but a plan is only
+ * valid for the table it was built from.
+ */
+int msa_plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks_per_seq,
+                    const int32_t* block_table, const int32_t* seq_lens,
+                    const int32_t* q_range_indptr, const int32_t* q_ranges, int32_t num_sms,
+                    msa_plan_t* out);
+
+/* Device workspace bytes the plan needs (work list, runs, row positions,
+ * merge counters, partial-result slots).  256-byte aligned. */
+int msa_plan_workspace_bytes(msa_plan_t plan, size_t* bytes);
+
+/* Copy the plan into `workspace` (caller device memory of at least
+ * msa_plan_workspace_bytes(), 256-byte aligned) on `stream` and zero its
+ * counters and error word.  The plan remembers the workspace: it must stay
+ * allocated, and must not be shared with another plan's upload, while
+ * msa_attention calls with this plan may run.  Host memory of the plan may
+ * be reused as soon as the call returns. */
+int msa_plan_upload(msa_plan_t plan, void* workspace, size_t bytes, msa_stream_t stream);
+
+/* Test / tooling introspection of the planner's segments of sequence `seq`:
+ * runs[3*i + 0..2] = (first logical block, first physical block, n_blocks).
+ * With runs == NULL only *n_runs is written. */
+int msa_plan_get_runs(msa_plan_t plan, int32_t seq, int32_t* runs, int32_t* n_runs);
+
+int msa_plan_get_info(msa_plan_t plan, msa_plan_info* info);
+
+/* Host copy of the work list, for tests: items[8*i + 0..7] =
+ * (kind 0=decode 1=prefill, seq, head (kv head for decode, q head for
+ * prefill), first packed row, number of rows, key begin, key end, part).
+ * With items == NULL only *n_items is written. */
+int msa_plan_get_items(msa_plan_t plan, int32_t* items, int32_t* n_items);
+
+int msa_plan_destroy(msa_plan_t plan);
+
+/*
+ * Scatter new or recomputed K/V rows into the paged pools (evicted blocks
+ * are rebuilt on demand: AsymCache explainer, "核心方法 2" and "一句话结论";
+ * MSA paper abstract).  For t in [0, n):
+ *     if slot_mapping[t] >= 0:  k_pool[slot_mapping[t]] = k_new[t]
+ *                               v_pool[slot_mapping[t]] = v_new[t]
+ * A bit copy.  Rows with slot -1 are skipped.
+ *
+ *   k_new, v_new    device bf16 [n, Hkv, D]
+ *   slot_mapping    device int64 [n]: pool row (block*16 + offset) or -1
+ *   k_pool, v_pool  device bf16 [pool_tokens, Hkv, D]
+ * A slot >= pool_tokens is not written; the kernel records
+ * MSA_ERR_BAD_BLOCK_ID in `error_word` (device int32, may be NULL) instead.
+ * Duplicate slots in one call race (one of the rows wins).
+ */
+int msa_append_kv(const void* k_new, const void* v_new, const int64_t* slot_mapping, int32_t n,
+                  void* k_pool, void* v_pool, int64_t pool_tokens, const msa_dims* dims,
+                  int32_t* error_word, msa_stream_t stream);
+
+/*
+ * Attention of every query row of the plan, one persistent launch.
+ *
+ *   q            device bf16 [n_q, Hq, D], rows in the plan's packed order
+ *   k_pool, v_pool  device bf16 [pool_tokens, Hkv, D] (16-byte aligned)
+ *   pool_tokens  rows in each pool; must cover every block the plan reads
+ *   plan         an uploaded plan
+ *   out          device [n_q, Hq, D], bf16 or fp32 per out_dtype
+ *   lse          device fp32 [n_q, Hq] (natural log of the sum of
+ *                exp(scaled scores)), or NULL
+ *   stream       CUDA stream
+ *
+ * Decode rows (a sequence's trailing rows when they number at most 16/G)
+ * are served GQA-packed: one work item reads a K/V chunk of one kv head
+ * once for all G query heads.  Other rows go in tiles of 128 rows per
+ * query head on the tensor cores.  Items whose sequence was split for SM
+ * balance write partial (output, lse) pairs to the workspace; the last item
+ * of a group to finish merges them by log-sum-exp and writes out/lse.
+ * A kernel that hits an internal time limit or a bad index records a code
+ * in the workspace's error word and returns; msa_plan_check_device() reads
+ * it.  Calls with the same plan/workspace must not overlap on the GPU.
+ */
+int msa_attention(const void* q, const void* k_pool, const void* v_pool, int64_t pool_tokens,
+                  msa_plan_t plan, void* out, int32_t out_dtype, float* lse, msa_stream_t stream);
+
+/* Synchronise `stream`, read the workspace's error word and return
+ * MSA_ERR_DEVICE_CHECK if a kernel recorded an error (then clear it), else
+ * MSA_OK.  `detail` (may be NULL) receives the raw error word. */
+int msa_plan_check_device(msa_plan_t plan, msa_stream_t stream, int32_t* detail);
+
+const char* msa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

@@ -1,0 +1,63 @@
+// append.cu -- msa_append_kv: scatter new or recomputed K/V rows into the
+// paged pools.  Evicted blocks are rebuilt on demand and written back into
+// the pool (AsymCache explainer, "核心方法 2": a hit on an evicted block
+// brings it back by recomputation; MSA paper abstract: evicted blocks are
+// reconstructed to keep outputs exact), as are a new turn's tokens.
+//
+// HBM-bound bit copy: one warp per token row (Hkv*D*2 bytes, 128-bit loads
+// and stores, fully coalesced on both sides), a grid of whole waves over the
+// SMs striding through the rows.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "msa_internal.h"
+#include "plan.h"
+
+namespace msa {
+
+__global__ void __launch_bounds__(256) append_kv_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                                                        const int64_t* __restrict__ slot, int32_t n,
+                                                        uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
+                                                        int64_t pool_tokens, int32_t row_chunks,
+                                                        int32_t* error_word) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < n; t += warps) {
+        const int64_t s = slot[t];
+        if (s < 0) continue;
+        if (s >= pool_tokens) {
+            if (lane == 0 && error_word) atomicOr(error_word, kErrAppendSlot);
+            continue;
+        }
+        const uint4* ks = k_new + t * row_chunks;
+        const uint4* vs = v_new + t * row_chunks;
+        uint4* kd = k_pool + s * row_chunks;
+        uint4* vd = v_pool + s * row_chunks;
+        for (int c = lane; c < row_chunks; c += 32) {
+            const uint4 a = __ldcs(ks + c);
+            const uint4 b = __ldcs(vs + c);
+            kd[c] = a;
+            vd[c] = b;
+        }
+    }
+}
+
+int launch_append_kv(const void* k_new, const void* v_new, const int64_t* slot, int32_t n, void* k_pool,
+                     void* v_pool, int64_t pool_tokens, int32_t row_elems, int32_t* error_word,
+                     msa_stream_t stream) {
+    static int sms = 0;
+    if (sms == 0) sms = device_sm_count();
+    if (sms <= 0) return MSA_ERR_CUDA;
+    const int32_t row_chunks = row_elems * 2 / 16;  // 16-byte chunks per token row
+    const int warps_per_block = 8;
+    int64_t blocks = ((int64_t)n + warps_per_block - 1) / warps_per_block;
+    const int64_t cap = (int64_t)sms * 8;  // 8 resident blocks of 256 threads per SM
+    if (blocks > cap) blocks = cap;
+    append_kv_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot, n, static_cast<uint4*>(k_pool),
+        static_cast<uint4*>(v_pool), pool_tokens, row_chunks, error_word);
+    return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+}  // namespace msa

@@ -1,0 +1,312 @@
+// planner.cpp -- host planner of libmsa: validates the block table and the
+// query ranges, splits every sequence's live blocks into physically
+// contiguous segments (runs), forms output groups (GQA-packed decode rows or
+// 128-row prefill tiles per query head), splits long key ranges for SM
+// balance and assigns the work items to the CTAs of one persistent launch.
+//
+// Segment rule (AsymCache explainer, "核心方法 1. Multi-Segment Attention"):
+// live blocks are regrouped by physical contiguity; an eviction hole, or any
+// block that is not the physical successor of the previous logical block,
+// starts a new segment.  Runs are therefore maximal, left to right, and
+// unique.  Two runs that touch physically but not in logical order stay
+// separate, because inside a run the logical->physical map must be a shift.
+//
+// The work list replaces the per-segment kernel launches the pages discuss
+// (MSA summary: one kernel over many disjoint segments removes launch
+// overhead) by one list consumed by a persistent grid.
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <queue>
+#include <vector>
+
+#include "msa_internal.h"
+#include "plan.h"
+
+namespace msa {
+
+static int validate_dims(const msa_dims* d) {
+    if (!d) return MSA_ERR_INVALID_ARG;
+    if (d->block_size != kBlock) return MSA_ERR_UNSUPPORTED_DIMS;
+    if (d->head_dim != 64 && d->head_dim != 128) return MSA_ERR_UNSUPPORTED_DIMS;
+    if (d->num_q_heads <= 0 || d->num_kv_heads <= 0) return MSA_ERR_UNSUPPORTED_DIMS;
+    if (d->num_q_heads % d->num_kv_heads != 0) return MSA_ERR_UNSUPPORTED_DIMS;
+    if (d->num_q_heads / d->num_kv_heads > kDecRows) return MSA_ERR_UNSUPPORTED_DIMS;
+    if (!(d->softmax_scale > 0.0f) || !std::isfinite(d->softmax_scale)) return MSA_ERR_UNSUPPORTED_DIMS;
+    return MSA_OK;
+}
+
+// Number of KV tiles the kernels walk over keys [kb, ke): 128-key windows
+// of the logical key range starting at kb (a window may span segments).
+static int64_t count_tiles(int32_t kb, int32_t ke) {
+    return ke > kb ? (ke - kb + kTileKeys - 1) / kTileKeys : 0;
+}
+
+// Index of the run (within runs[r0..r1)) holding logical key k.
+static int32_t run_of(const Run* runs, int32_t r0, int32_t r1, int32_t k) {
+    int32_t lo = r0, hi = r1 - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) / 2;
+        if (runs[mid].log_start <= k) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
+                const int32_t* table, const int32_t* seq_lens, const int32_t* q_range_indptr,
+                const int32_t* q_ranges, int32_t num_sms, msa_plan_s** out) {
+    auto t0 = std::chrono::steady_clock::now();
+    if (!out) return MSA_ERR_INVALID_ARG;
+    *out = nullptr;
+    int rc = validate_dims(dims);
+    if (rc != MSA_OK) return rc;
+    if (num_seqs < 0 || max_blocks < 0 || num_sms < 0) return MSA_ERR_INVALID_ARG;
+    if (num_seqs > 0 && (!seq_lens || !q_range_indptr)) return MSA_ERR_INVALID_ARG;
+    if (num_seqs > 0 && max_blocks > 0 && !table) return MSA_ERR_INVALID_ARG;
+    if (num_sms == 0) {
+        num_sms = device_sm_count();
+        if (num_sms <= 0) return MSA_ERR_CUDA;
+    }
+
+    msa_plan_s* P = new (std::nothrow) msa_plan_s();
+    if (!P) return MSA_ERR_INVALID_ARG;
+    std::unique_ptr<msa_plan_s> guard(P);
+    P->dims = *dims;
+    P->num_seqs = num_seqs;
+    P->G = dims->num_q_heads / dims->num_kv_heads;
+    P->dec_rows = kDecRows / P->G;
+    const int32_t D = dims->head_dim;
+    const int32_t Hq = dims->num_q_heads, Hkv = dims->num_kv_heads, G = P->G;
+
+    // ---- sequences and segment runs -------------------------------------
+    P->seq_lens.assign(seq_lens, seq_lens + num_seqs);
+    P->run_indptr.assign(1, 0);
+    int64_t max_row = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int32_t L = seq_lens[s];
+        if (L < 0) return MSA_ERR_INVALID_ARG;
+        const int32_t nb = (L + kBlock - 1) / kBlock;
+        if (nb > max_blocks) return MSA_ERR_INVALID_ARG;
+        const int32_t* row = table + (int64_t)s * max_blocks;
+        int32_t b = 0;
+        while (b < nb) {
+            if (row[b] < 0) return MSA_ERR_MISSING_BLOCK;
+            if (row[b] >= (1 << 27)) return MSA_ERR_BAD_BLOCK_ID;
+            int32_t e = b + 1;
+            while (e < nb && row[e] >= 0 && row[e] < (1 << 27) && row[e] == row[e - 1] + 1) ++e;
+            Run r;
+            r.log_start = b * kBlock;
+            r.phys_row = row[b] * kBlock;
+            r.n_tok = std::min(e * kBlock, L) - b * kBlock;
+            r.pad = 0;
+            P->runs.push_back(r);
+            max_row = std::max<int64_t>(max_row, (int64_t)row[e - 1] * kBlock + kBlock);
+            b = e;
+        }
+        P->run_indptr.push_back((int32_t)P->runs.size());
+    }
+    P->max_pool_row = max_row;
+
+    // ---- query rows -------------------------------------------------------
+    if (num_seqs > 0) {
+        if (q_range_indptr[0] != 0) return MSA_ERR_BAD_Q_RANGE;
+        if (q_range_indptr[num_seqs] > 0 && !q_ranges) return MSA_ERR_INVALID_ARG;
+    }
+    P->row_indptr.assign(1, 0);
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int32_t a = q_range_indptr[s], b = q_range_indptr[s + 1];
+        if (b < a) return MSA_ERR_BAD_Q_RANGE;
+        int64_t prev_end = 0;
+        for (int32_t i = a; i < b; ++i) {
+            const int32_t st = q_ranges[2 * i], en = q_ranges[2 * i + 1];
+            if (st < 0 || en <= st || en > seq_lens[s] + 1 || st < prev_end) return MSA_ERR_BAD_Q_RANGE;
+            prev_end = en;
+            if ((int64_t)P->pos.size() + (en - st) > (int64_t)INT32_MAX / 2) return MSA_ERR_INVALID_ARG;
+            for (int32_t p = st; p < en; ++p) P->pos.push_back(p);
+        }
+        P->row_indptr.push_back((int32_t)P->pos.size());
+    }
+    const int32_t n_q = (int32_t)P->pos.size();
+
+    // ---- output groups ----------------------------------------------------
+    // A sequence's trailing rows go to the GQA-packed decode path when they
+    // number at most kDecRows / G; everything else is cut into 128-row tiles.
+    struct Pending { Group g; int32_t ke; int64_t tiles; };
+    std::vector<Pending> pend;
+    double prefill_flops = 0.0;
+    int64_t dec_kv = 0, dec_qo = 0;
+    int32_t dec_rows_total = 0, pre_rows_total = 0;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int32_t r0 = P->row_indptr[s], r1 = P->row_indptr[s + 1];
+        const int32_t n = r1 - r0;
+        if (n == 0) continue;
+        const int32_t L = seq_lens[s];
+        const int32_t ra = P->run_indptr[s], rb = P->run_indptr[s + 1];
+        auto add_groups = [&](int32_t kind, int32_t row0, int32_t nrows) {
+            const int32_t pmax = P->pos[row0 + nrows - 1];  // rows ascend within a sequence
+            const int32_t ke = std::min(pmax + 1, L);
+            const int64_t tiles = count_tiles(0, ke);
+            const int32_t nh = kind == kDecode ? Hkv : Hq;
+            for (int32_t h = 0; h < nh; ++h) {
+                Pending pd;
+                pd.g = Group{kind, s, h, row0, nrows, 1, -1, 0};
+                pd.ke = ke;
+                pd.tiles = tiles;
+                pend.push_back(pd);
+            }
+            if (kind == kDecode) {
+                dec_kv += (int64_t)ke * Hkv * D * 2 * 2;
+                dec_qo += (int64_t)nrows * Hq * (D * 2 + D * 2 + 4);
+                dec_rows_total += nrows;
+            } else {
+                for (int32_t r = row0; r < row0 + nrows; ++r)
+                    prefill_flops += 4.0 * D * Hq * (double)std::min(P->pos[r] + 1, L);
+                pre_rows_total += nrows;
+            }
+        };
+        if (n <= P->dec_rows) {
+            add_groups(kDecode, r0, n);
+        } else {
+            const int32_t full = n / kTileRows, rem = n % kTileRows;
+            for (int32_t t = 0; t < full; ++t) add_groups(kPrefill, r0 + t * kTileRows, kTileRows);
+            if (rem > 0) {
+                if (rem <= P->dec_rows) add_groups(kDecode, r0 + full * kTileRows, rem);
+                else add_groups(kPrefill, r0 + full * kTileRows, rem);
+            }
+        }
+    }
+
+    // ---- split long key ranges, cost model ---------------------------------
+    // Cost of an item ~ its KV tiles (a decode tile moves 2*128*D*2 bytes, a
+    // prefill tile does 4*128*128*D flops; on GB300 both take ~1.3-1.5 us per
+    // SM) plus a fixed per-item cost.
+    const double w_tile[2] = {1.1, 1.0};
+    const double w_item[2] = {0.5, 2.0};
+    double total = 0.0;
+    for (auto& pd : pend) total += pd.tiles * w_tile[pd.g.kind] + w_item[pd.g.kind];
+    P->grid = std::max(1, num_sms);
+    const double per_cta = total / P->grid;
+    const int64_t min_tiles[2] = {4, 8};
+
+    std::vector<double> cost;
+    for (size_t gi = 0; gi < pend.size(); ++gi) {
+        Pending& pd = pend[gi];
+        const int32_t kind = pd.g.kind;
+        int64_t chunk = std::max<int64_t>(min_tiles[kind], (int64_t)std::ceil(per_cta / 16.0 / w_tile[kind]));
+        int32_t parts = (int32_t)std::max<int64_t>(1, (pd.tiles + chunk - 1) / chunk);
+        const int32_t s = pd.g.seq;
+        const int32_t ra = P->run_indptr[s], rb = P->run_indptr[s + 1];
+        Group g = pd.g;
+        g.n_parts = parts;
+        const int32_t gid = (int32_t)P->groups.size();
+        if (parts > 1) {
+            if (kind == kDecode) { g.slot = P->n_dec_slots; P->n_dec_slots += parts; }
+            else { g.slot = P->n_pre_slots; P->n_pre_slots += parts; }
+        }
+        P->groups.push_back(g);
+        // cut the key range into `parts` runs of whole tiles
+        if (pd.ke <= 0 || ra == rb) {
+            Item it{gid, 0, 0, ra, 0, kind, s, 0};
+            P->items.push_back(it);
+            cost.push_back(w_item[kind]);
+            continue;
+        }
+        const int64_t per = (pd.tiles + parts - 1) / parts;
+        int32_t part = 0;
+        for (int64_t t = 0; t < pd.tiles; t += per) {
+            const int32_t kb = (int32_t)(t * kTileKeys);
+            const int32_t ke = (int32_t)std::min<int64_t>((t + per) * kTileKeys, pd.ke);
+            Item it{gid, kb, ke, run_of(P->runs.data(), ra, rb, kb), part, kind, s, 0};
+            P->items.push_back(it);
+            cost.push_back(std::min<int64_t>(per, pd.tiles - t) * w_tile[kind] + w_item[kind]);
+            ++part;
+        }
+        P->groups[gid].n_parts = part;
+        if (part == 1) P->groups[gid].slot = -1;
+    }
+
+    // KV tiles of every item (the kernels walk exactly these)
+    for (auto& it : P->items) it.pad = (int32_t)count_tiles(it.kb, it.ke);
+
+    // ---- LPT assignment of items to CTAs ------------------------------------
+    const int32_t n_items = (int32_t)P->items.size();
+    std::vector<int32_t> order(n_items);
+    for (int32_t i = 0; i < n_items; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
+    typedef std::pair<double, int32_t> Load;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int32_t c = 0; c < P->grid; ++c) heap.push(Load(0.0, c));
+    std::vector<std::vector<int32_t>> per(P->grid);
+    for (int32_t i : order) {
+        Load l = heap.top();
+        heap.pop();
+        per[l.second].push_back(i);
+        l.first += cost[i];
+        heap.push(l);
+    }
+    P->cta_indptr.assign(1, 0);
+    for (int32_t c = 0; c < P->grid; ++c) {
+        for (int32_t i : per[c]) P->cta_items.push_back(i);
+        P->cta_indptr.push_back((int32_t)P->cta_items.size());
+    }
+
+    // ---- info ---------------------------------------------------------------
+    msa_plan_info& I = P->info;
+    std::memset(&I, 0, sizeof I);
+    I.num_seqs = num_seqs;
+    I.num_q_rows = n_q;
+    I.num_runs = (int32_t)P->runs.size();
+    I.num_groups = (int32_t)P->groups.size();
+    I.num_items = n_items;
+    for (auto& it : P->items) (it.kind == kDecode ? I.num_decode_items : I.num_prefill_items)++;
+    I.num_decode_rows = dec_rows_total;
+    I.num_prefill_rows = pre_rows_total;
+    I.grid = P->grid;
+    I.decode_kv_bytes = dec_kv;
+    I.decode_qo_bytes = dec_qo;
+    I.prefill_flops = prefill_flops;
+    I.max_pool_row = P->max_pool_row;
+
+    build_image(P);
+    I.host_plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
+    *out = guard.release();
+    return MSA_OK;
+}
+
+// Lay out the workspace and serialise the int sections into the host image.
+void build_image(msa_plan_s* P) {
+    WsLayout& W = P->lay;
+    const size_t D = (size_t)P->dims.head_dim;
+    size_t o = 0;
+    auto sec = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+    W.error = sec(64 * sizeof(int32_t));
+    W.items = sec(P->items.size() * sizeof(Item));
+    W.groups = sec(P->groups.size() * sizeof(Group));
+    W.runs = sec(P->runs.size() * sizeof(Run));
+    W.pos = sec(P->pos.size() * sizeof(int32_t));
+    W.cta_indptr = sec(P->cta_indptr.size() * sizeof(int32_t));
+    W.cta_items = sec(P->cta_items.size() * sizeof(int32_t));
+    W.image_end = o;
+    W.counters = sec(P->groups.size() * sizeof(int32_t));
+    W.counters_end = o;
+    W.dec_part = sec((size_t)P->n_dec_slots * kDecRows * D * sizeof(float));
+    W.dec_lse = sec((size_t)P->n_dec_slots * kDecRows * sizeof(float));
+    W.pre_part = sec((size_t)P->n_pre_slots * kTileRows * D * sizeof(float));
+    W.pre_lse = sec((size_t)P->n_pre_slots * kTileRows * sizeof(float));
+    W.total = align_up(o, 256);
+
+    P->image.assign(W.image_end, 0);
+    auto put = [&](size_t at, const void* src, size_t bytes) {
+        if (bytes) std::memcpy(P->image.data() + at, src, bytes);
+    };
+    put(W.items, P->items.data(), P->items.size() * sizeof(Item));
+    put(W.groups, P->groups.data(), P->groups.size() * sizeof(Group));
+    put(W.runs, P->runs.data(), P->runs.size() * sizeof(Run));
+    put(W.pos, P->pos.data(), P->pos.size() * sizeof(int32_t));
+    put(W.cta_indptr, P->cta_indptr.data(), P->cta_indptr.size() * sizeof(int32_t));
+    put(W.cta_items, P->cta_items.data(), P->cta_items.size() * sizeof(int32_t));
+}
+
+}  // namespace msa

@@ -1,0 +1,62 @@
+"""Convenience wrapper over the C ABI for callers holding torch tensors.
+
+`MsaSession` builds a plan from host arrays, allocates its device workspace
+(a torch uint8 tensor), uploads it, and forwards attention calls.  It only
+marshals arguments; all work runs in libmsa.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import msa
+
+
+class MsaSession:
+    def __init__(self, num_q_heads, num_kv_heads, head_dim, block_table, seq_lens, q_range_indptr, q_ranges,
+                 device="cuda", num_sms=0, softmax_scale=None, stream=None):
+        import torch
+        self.dims = msa.make_dims(num_q_heads, num_kv_heads, head_dim, 16, softmax_scale)
+        self.plan = msa.msa_plan_create(self.dims, block_table, seq_lens, q_range_indptr, q_ranges, num_sms)
+        self.info = msa.msa_plan_get_info(self.plan)
+        self.ws_bytes = msa.msa_plan_workspace_bytes(self.plan)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
+        self.stream = stream
+        msa.msa_plan_upload(self.plan, self.workspace, self.ws_bytes, self._stream())
+
+    @classmethod
+    def from_workload(cls, wl, device="cuda", num_sms=0, stream=None):
+        return cls(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_table, wl.seq_lens, wl.q_range_indptr,
+                   wl.q_ranges_flat, device=device, num_sms=num_sms, softmax_scale=wl.scale, stream=stream)
+
+    def _stream(self):
+        import torch
+        return self.stream if self.stream is not None else torch.cuda.current_stream()
+
+    def attention(self, q, k_pool, v_pool, out=None, lse=None, out_fp32=False):
+        import torch
+        n_q, hq, d = q.shape
+        if out is None:
+            out = torch.empty((n_q, hq, d), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=q.device)
+        out_dtype = msa.MSA_OUT_FP32 if out.dtype == torch.float32 else msa.MSA_OUT_BF16
+        msa.msa_attention(q, k_pool, v_pool, k_pool.shape[0], self.plan, out, out_dtype, lse, self._stream())
+        return out
+
+    def check_device(self):
+        return msa.msa_plan_check_device(self.plan, self._stream())
+
+    def close(self):
+        if self.plan:
+            msa.msa_plan_destroy(self.plan)
+            self.plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def append_kv(k_new, v_new, slot_mapping, k_pool, v_pool, dims, error_word=None, stream=None):
+    import torch
+    msa.msa_append_kv(k_new, v_new, slot_mapping, k_new.shape[0], k_pool, v_pool, k_pool.shape[0], dims,
+                      error_word, stream if stream is not None else torch.cuda.current_stream())

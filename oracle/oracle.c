@@ -108,7 +108,10 @@ static void* dense_worker(void* arg) {
     double* qv = (double*)malloc(sizeof(double) * (size_t)d);
     if (!t || !qv) { free(t); free(qv); jb->status = ORACLE_ERR_NOMEM; return NULL; }
 
-    for (int64_t i = jb->begin; i < jb->end; ++i) {
+    /* work units are (output row, head) pairs: unit u = i * hq + h */
+    for (int64_t u = jb->begin; u < jb->end; ++u) {
+        const int64_t i = u / hq;
+        const int32_t h = (int32_t)(u % hq);
         const int64_t r = jb->rows ? jb->rows[i] : i;
         const int32_t s = seq_of_row(jb->q_indptr, jb->num_seqs, r);
         const int64_t kv0 = jb->kv_indptr[s];
@@ -116,7 +119,7 @@ static void* dense_worker(void* arg) {
         const int64_t p = jb->q_pos[r];
         int64_t n_vis = p + 1 < len ? p + 1 : len; /* keys j <= p and j < L_s */
         if (n_vis < 0) n_vis = 0;
-        for (int32_t h = 0; h < hq; ++h) {
+        {
             const int32_t g = h / group;
             double* o = jb->out + (i * hq + h) * (int64_t)d;
             for (int32_t c = 0; c < d; ++c) o[c] = 0.0;
@@ -186,8 +189,9 @@ int oracle_dense_attention(int32_t num_seqs, int32_t hq, int32_t hkv, int32_t d,
     if (!kv_indptr || !q_indptr || !q_pos || !out || !lse) return ORACLE_ERR_ARG;
     const int64_t n_out = rows ? n_rows : q_indptr[num_seqs];
     if (n_out <= 0) return ORACLE_OK;
+    const int64_t n_units = n_out * hq;
     if (num_threads < 1) num_threads = 1;
-    if (num_threads > n_out) num_threads = (int32_t)n_out;
+    if (num_threads > n_units) num_threads = (int32_t)n_units;
     dense_job* jobs = (dense_job*)calloc((size_t)num_threads, sizeof(dense_job));
     if (!jobs) return ORACLE_ERR_NOMEM;
     for (int32_t i = 0; i < num_threads; ++i) {
@@ -196,8 +200,8 @@ int oracle_dense_attention(int32_t num_seqs, int32_t hq, int32_t hkv, int32_t d,
         jb->kv_indptr = kv_indptr; jb->k = k; jb->v = v;
         jb->q_indptr = q_indptr; jb->q_pos = q_pos; jb->q = q;
         jb->rows = rows; jb->n_rows = n_rows; jb->out = out; jb->lse = lse;
-        jb->begin = n_out * i / num_threads;
-        jb->end = n_out * (i + 1) / num_threads;
+        jb->begin = n_units * i / num_threads;
+        jb->end = n_units * (i + 1) / num_threads;
     }
     int rc = run_jobs(dense_worker, jobs, sizeof(dense_job), num_threads);
     for (int32_t i = 0; rc == ORACLE_OK && i < num_threads; ++i) rc = jobs[i].status;

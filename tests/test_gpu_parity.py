@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Tolerance (bf16 in, fp32 accumulate): every out element within
+2e-3 + 1e-2*|ref|, lse within 1e-4 absolute; pool scatter bit-exact."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_harness import compare, oracle_ref, run_gpu
+from kv_cache_segment_gb300 import msa, workloads as W
+from kv_cache_segment_gb300.runner import MsaSession, append_kv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    msa.load()
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# ------------------------------------------------------------------ append --
+
+@pytest.mark.parametrize("hkv,d", [(8, 128), (4, 64), (1, 128)])
+def test_append_kv_bit_exact(hkv, d):
+    g = torch.Generator().manual_seed(5)
+    pool_tokens, n = 4096, 700
+    kp = torch.randn((pool_tokens, hkv, d), generator=g).to(torch.bfloat16).cuda()
+    vp = torch.randn((pool_tokens, hkv, d), generator=g).to(torch.bfloat16).cuda()
+    kn = torch.randn((n, hkv, d), generator=g).to(torch.bfloat16).cuda()
+    vn = torch.randn((n, hkv, d), generator=g).to(torch.bfloat16).cuda()
+    slot = torch.randperm(pool_tokens, generator=g)[:n].to(torch.int64)
+    slot[::7] = -1
+    want_k = oracle.scatter_rows(_bits(kn), slot.numpy(), _bits(kp).copy())
+    want_v = oracle.scatter_rows(_bits(vn), slot.numpy(), _bits(vp).copy())
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dims = msa.make_dims(hkv, hkv, d)
+    append_kv(kn, vn, slot.cuda(), kp, vp, dims, error_word=err)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(kp), want_k)
+    assert np.array_equal(_bits(vp), want_v)
+    assert int(err.item()) == 0
+    # and against torch's own index_copy_
+    keep = slot >= 0
+    ref = torch.zeros_like(kp).copy_(kp)
+    ref.index_copy_(0, slot[keep].cuda(), kn[keep.cuda()])
+    assert torch.equal(ref.view(torch.int16), kp.view(torch.int16))
+
+
+def test_append_kv_slot_past_pool_is_reported_not_written():
+    kp = torch.zeros((64, 2, 64), dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    kn = torch.ones((3, 2, 64), dtype=torch.bfloat16, device="cuda")
+    slot = torch.tensor([1, 64, 5], dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    append_kv(kn, kn, slot, kp, vp, msa.make_dims(2, 2, 64), error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) != 0
+    assert kp[1].float().sum().item() == 128 and kp[5].float().sum().item() == 128
+    assert kp.float().sum().item() == 256
+
+
+# ------------------------------------------------------- attention, small --
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
+def test_small_configs_match_oracle(idx):
+    wl = W.small_config(idx)
+    k, v, q = W.make_values(wl)
+    out, lse, info = run_gpu(wl, k, v, q)
+    ro, rl = oracle_ref(wl, k, v, q)
+    compare(out, lse, ro, rl, wl.name)
+
+
+@pytest.mark.parametrize("idx", [2, 3, 5])
+def test_split_groups_merge(idx):
+    """Many CTAs -> long groups split into parts merged by log-sum-exp."""
+    wl = W.small_config(idx)
+    k, v, q = W.make_values(wl)
+    out, lse, info = run_gpu(wl, k, v, q, num_sms=1500)
+    assert info["num_items"] > info["num_groups"]
+    ro, rl = oracle_ref(wl, k, v, q)
+    compare(out, lse, ro, rl, wl.name + "/split")
+
+
+def test_fp32_output():
+    wl = W.small_config(3)
+    k, v, q = W.make_values(wl)
+    out, lse, _ = run_gpu(wl, k, v, q, out_fp32=True)
+    assert out.dtype == torch.float32
+    ro, rl = oracle_ref(wl, k, v, q)
+    compare(out, lse, ro, rl, "fp32 out")
+
+
+def test_segmented_equals_contiguous_layout():
+    """Losslessness: the same logical K/V laid out as one segment or as many
+    gives the same result (both within tolerance of the oracle and of each
+    other)."""
+    lens = [1000, 777]
+    many = [[5, 9, 3, 20, 12, 14], [7, 7, 7, 7, 7, 7, 7]]
+    one = [[63], [49]]
+    ranges = [[(100, 260), (1000, 1001)], [(0, 40), (500, 777)]]
+    wl_a = W.custom(lens, many, ranges, hq=8, hkv=2, seed=3)
+    wl_b = W.custom(lens, one, ranges, hq=8, hkv=2, seed=4)
+    k, v, q = W.make_values(wl_a)
+    oa, la, _ = run_gpu(wl_a, k, v, q)
+    ob, lb, _ = run_gpu(wl_b, k, v, q)
+    ro, rl = oracle_ref(wl_a, k, v, q)
+    compare(oa, la, ro, rl, "segmented")
+    compare(ob, lb, ro, rl, "contiguous")
+    assert (oa.float() - ob.float()).abs().max().item() <= 4e-3
+
+
+# ------------------------------------------------------------- edge cases --
+
+@pytest.mark.parametrize("case", ["empty_seq", "mid_decode", "ragged", "gqa16", "d64_prefill", "one_key",
+                                  "far_ranges", "single_block_runs"])
+def test_edge_cases(case):
+    if case == "empty_seq":       # L = 0 queried at p = 0 (no key visible) next to a normal one
+        wl = W.custom([0, 50], [[], [4]], [[(0, 1)], [(50, 51)]], hq=4, hkv=2)
+    elif case == "mid_decode":    # decode-path rows at p < L (they see keys <= p only)
+        wl = W.custom([300], [[3, 5, 11]], [[(33, 35)]], hq=8, hkv=4)
+    elif case == "ragged":        # partial last blocks, NaN past L, prefill tile + decode tail
+        wl = W.custom([129, 1], [[2, 3, 4], [1]], [[(0, 129), (129, 130)], [(0, 2)]], hq=4, hkv=1)
+    elif case == "gqa16":
+        wl = W.custom([600, 90], [[10, 28], [6]], [[(600, 601)], [(20, 91)]], hq=16, hkv=1)
+    elif case == "d64_prefill":
+        wl = W.custom([700], [[4, 30, 10]], [[(0, 300), (650, 701)]], hq=8, hkv=2, d=64)
+    elif case == "one_key":       # L = 1
+        wl = W.custom([1, 1], [[1], [1]], [[(0, 2)], [(1, 2)]], hq=4, hkv=2)
+    elif case == "far_ranges":    # one 128-row tile spanning distant ranges
+        wl = W.custom([3000], [[40, 60, 88]], [[(10, 70), (1500, 1540), (2990, 3001)]], hq=4, hkv=2)
+    else:                         # every block its own segment
+        wl = W.custom([400], [[1] * 25], [[(0, 400), (400, 401)]], hq=8, hkv=2)
+    k, v, q = W.make_values(wl)
+    out, lse, _ = run_gpu(wl, k, v, q)
+    ro, rl = oracle_ref(wl, k, v, q)
+    compare(out, lse, ro, rl, case)
+    if case == "empty_seq":
+        assert torch.all(out[0].float() == 0) and torch.all(torch.isneginf(lse[0]))
+
+
+def test_repeat_calls_are_identical():
+    """Merge counters reset themselves: back-to-back calls give the same bits."""
+    wl = W.small_config(2)
+    k, v, q = W.make_values(wl)
+    dev = torch.device("cuda")
+    kp, vp = W.make_pool(wl, k.to(dev), v.to(dev))
+    sess = MsaSession.from_workload(wl, num_sms=1000)
+    qd = q.to(dev)
+    outs = [sess.attention(qd, kp, vp).clone() for _ in range(3)]
+    assert sess.check_device()[0] == 0
+    assert all(torch.equal(outs[0].view(torch.int16), o.view(torch.int16)) for o in outs[1:])
+    sess.close()
+
+
+# ---------------------------------------------------------- full size --
+
+def _sample_rows(wl, rng, per_seq=2):
+    rows = []
+    for s in range(wl.num_seqs):
+        a, b = int(wl.q_indptr[s]), int(wl.q_indptr[s + 1])
+        if b - a <= per_seq:
+            rows += list(range(a, b))
+        else:
+            rows += [a, b - 1] + list(rng.choice(np.arange(a + 1, b - 1), size=per_seq - 2 if per_seq > 2 else 0,
+                                                 replace=False))
+    return np.unique(np.asarray(rows, np.int64))
+
+
+@pytest.mark.parametrize("idx", [2, 3, 4, 5])
+def test_full_size_configs_sampled(idx):
+    """The full workloads in the bench's launch configuration, checked on
+    sampled rows (first/last row of every sequence plus random ones)."""
+    wl = W.config(idx)
+    dev = torch.device("cuda")
+    k, v, q = W.make_values(wl, device=dev)
+    out, lse, _ = run_gpu(wl, k, v, q)
+    rng = np.random.default_rng(idx)
+    rows = _sample_rows(wl, rng, per_seq=4 if idx != 4 else 6)
+    if idx == 3:
+        rows = rows[rng.permutation(len(rows))[:48]]
+        rows.sort()
+    ro, rl = oracle_ref(wl, k.cpu(), v.cpu(), q.cpu(), rows=rows)
+    compare(out[torch.as_tensor(rows, device=dev)], lse[torch.as_tensor(rows, device=dev)], ro, rl, wl.name)
