@@ -210,6 +210,34 @@ int msa_append_kv(const void* k_new, const void* v_new, const int64_t* slot_mapp
 int msa_attention(const void* q, const void* k_pool, const void* v_pool, int64_t pool_tokens,
                   msa_plan_t plan, void* out, int32_t out_dtype, float* lse, msa_stream_t stream);
 
+/*
+ * msa_attention for callers that cannot allocate device memory.  The paper
+ * has no counterpart; this is a deployment convenience.  Some callers may not
+ * call cudaMalloc or an allocator at all: code that runs inside a
+ * pre-planned memory budget (a serving engine whose device memory is fully
+ * carved up at start-up), a host thread that must not synchronise with the
+ * device the way a first allocation can, or a plug-in that has no handle on
+ * the host framework's allocator.  This entry point needs no workspace from
+ * them.
+ *
+ * Same arguments, results and error codes as msa_attention, except that the
+ * plan does not have to be uploaded: each call copies the plan's work list
+ * into a library-owned device array of 32 MiB (held by every GPU that loads
+ * the library, until the process exits) and zeroes its counters there, in
+ * stream order, then launches the same kernel.  A plan whose workspace
+ * (msa_plan_workspace_bytes) exceeds 32 MiB is rejected with
+ * MSA_ERR_WORKSPACE_TOO_SMALL.  No device memory is allocated or freed.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array: calls that overlap on the GPU
+ * (other streams, other host threads) race and corrupt each other's results;
+ * serialise them.  msa_plan_check_device does not see this array's error
+ * word.
+ */
+int msa_attention_no_alloc(const void* q, const void* k_pool, const void* v_pool, int64_t pool_tokens,
+                           msa_plan_t plan, void* out, int32_t out_dtype, float* lse, msa_stream_t stream);
+
 /* Synchronise `stream`, read the workspace's error word and return
  * MSA_ERR_DEVICE_CHECK if a kernel recorded an error (then clear it), else
  * MSA_OK.  `detail` (may be NULL) receives the raw error word. */

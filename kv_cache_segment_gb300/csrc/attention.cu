@@ -978,6 +978,12 @@ static int launch_d(const msa_plan_s* P, const AttnParams& prm, const CUtensorMa
 
 int launch_attention(const msa_plan_s* P, const void* q, const void* k_pool, const void* v_pool,
                      int64_t pool_tokens, void* out, int32_t out_dtype, float* lse, msa_stream_t stream) {
+    return launch_attention_ws(P, P->workspace, q, k_pool, v_pool, pool_tokens, out, out_dtype, lse, stream);
+}
+
+int launch_attention_ws(const msa_plan_s* P, void* workspace, const void* q, const void* k_pool,
+                        const void* v_pool, int64_t pool_tokens, void* out, int32_t out_dtype, float* lse,
+                        msa_stream_t stream) {
     const int D = P->dims.head_dim, Hq = P->dims.num_q_heads, Hkv = P->dims.num_kv_heads;
     CUtensorMap maps[5];
     const int64_t nq = P->info.num_q_rows;
@@ -987,7 +993,7 @@ int launch_attention(const msa_plan_s* P, const void* q, const void* k_pool, con
         !make_map(&maps[3], v_pool, pool_tokens, Hkv, D, kBlock) ||
         !make_map(&maps[4], q, nq, Hq, D, kTileRows))
         return MSA_ERR_CUDA;
-    uint8_t* ws = static_cast<uint8_t*>(P->workspace);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
     const WsLayout& W = P->lay;
     AttnParams prm;
     prm.items = reinterpret_cast<const Item*>(ws + W.items);

@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH):
         "msa_plan_destroy": ([vp], ctypes.c_int),
         "msa_append_kv": ([vp, vp, vp, i32, vp, vp, i64, ctypes.POINTER(msa_dims), vp, vp], ctypes.c_int),
         "msa_attention": ([vp, vp, vp, i64, vp, vp, i32, vp, vp], ctypes.c_int),
+        "msa_attention_no_alloc": ([vp, vp, vp, i64, vp, vp, i32, vp, vp], ctypes.c_int),
         "msa_plan_check_device": ([vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
         "msa_status_string": ([ctypes.c_int], ctypes.c_char_p),
     }
@@ -193,6 +194,14 @@ def msa_attention(q, k_pool, v_pool, pool_tokens: int, plan, out, out_dtype: int
                   stream=None):
     _check(load().msa_attention(_p(q), _p(k_pool), _p(v_pool), int(pool_tokens), plan, _p(out), int(out_dtype),
                                 _p(lse), _stream(stream)), "msa_attention")
+
+
+def msa_attention_no_alloc(q, k_pool, v_pool, pool_tokens: int, plan, out, out_dtype: int = MSA_OUT_BF16,
+                           lse=None, stream=None):
+    """msa_attention without a caller workspace (library-owned 32 MiB device
+    array; see include/msa.h for who needs it and its limits)."""
+    _check(load().msa_attention_no_alloc(_p(q), _p(k_pool), _p(v_pool), int(pool_tokens), plan, _p(out),
+                                         int(out_dtype), _p(lse), _stream(stream)), "msa_attention_no_alloc")
 
 
 def msa_plan_check_device(plan, stream=None):
