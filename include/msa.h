@@ -158,10 +158,11 @@ int msa_plan_get_runs(msa_plan_t plan, int32_t seq, int32_t* runs, int32_t* n_ru
 
 int msa_plan_get_info(msa_plan_t plan, msa_plan_info* info);
 
-/* Host copy of the work list, for tests: items[8*i + 0..7] =
- * (kind 0=decode 1=prefill, seq, head (kv head for decode, q head for
- * prefill), first packed row, number of rows, key begin, key end, part).
- * With items == NULL only *n_items is written. */
+/* Host copy of the work list, for tests: items[9*i + 0..8] =
+ * (kind 0=decode 1=prefill, seq, head (kv head for decode, first query
+ * head for prefill), query heads covered (G for decode, 1 or 2 consecutive
+ * heads for prefill), first packed row, number of rows, key begin, key end,
+ * part).  With items == NULL only *n_items is written. */
 int msa_plan_get_items(msa_plan_t plan, int32_t* items, int32_t* n_items);
 
 int msa_plan_destroy(msa_plan_t plan);

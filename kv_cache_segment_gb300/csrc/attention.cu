@@ -3,24 +3,31 @@
 // One launch serves every work item of a plan: decode groups (a sequence's
 // few trailing query rows, all G query heads of one kv head packed as the
 // rows of a warp-level MMA) and prefill / hole-recompute tiles (128 query
-// rows of one query head, tcgen05 tensor cores with TMEM accumulators).
-// Each item walks its key range segment by segment: KV tiles never cross a
-// segment, so every tile is one rectangle of the paged pool fetched by TMA
-// (AsymCache explainer, "核心方法 1. Multi-Segment Attention": attend to the
+// rows of one or two query heads that share a kv head, on the tcgen05 tensor
+// cores with TMEM accumulators).  KV tiles are 128-key windows of an item's
+// logical key range; the producer fetches each window from the physically
+// contiguous segments it overlaps, one TMA rectangle per piece (AsymCache
+// explainer, "核心方法 1. Multi-Segment Attention": attention over the
 // physically contiguous segments of the live KV; MSA summary: one kernel over
-// many disjoint segments instead of a launch per segment).  Segments of one
-// item are combined by the online-softmax running (max, sum, output) state,
-// which is the pairwise form of the log-sum-exp merge; items of a group that
-// was split for SM balance write (output, lse) partials and the last one to
-// finish merges them by log-sum-exp.
+// many disjoint segments instead of a launch per segment).  Inside an item
+// the online-softmax running (max, sum, output) state carries across
+// segments, which is the pairwise form of the log-sum-exp merge; items of a
+// group that was split for SM balance write (output, lse) partials and the
+// last one to finish merges them by log-sum-exp.
 //
-// CTA = 6 warps:
-//   warp 0      TMA producer: Q tile (prefill) and K/V tiles into a ring of
-//               shared-memory stages, one mbarrier pair per stage.
-//   warp 1      owns TMEM; one lane issues tcgen05.mma: S = Q K^T into one
-//               of two TMEM S buffers, then O += P V into the TMEM O buffer.
-//   warps 2..5  compute: prefill softmax / epilogue (thread = tile row =
-//               TMEM lane), or the decode math (mma.sync on 32 keys each).
+// CTA roles (10 warps; 6 when the launch has decode items only):
+//   warp 0      TMA producer: the Q tiles of a prefill item and the K/V
+//               tiles into a ring of shared-memory stages.
+//   warp 1      owns TMEM; one lane issues tcgen05.mma.  Per KV tile j, in
+//               this order: PV0(j-1), S0(j), PV1(j-1), S1(j), where
+//               Sk = Qk K^T lands in TMEM buffer k and PVk accumulates
+//               O_k += P_k V with P_k read from TMEM (it overwrites S_k; the
+//               tensor core runs one thread's MMAs in issue order).
+//   warps 2..5  warpgroup 0: softmax of Q tile 0 (thread = row = TMEM lane),
+//               and the decode math (mma.sync, 32 keys per warp per tile).
+//   warps 6..9  warpgroup 1: softmax of Q tile 1.
+// Each softmax warpgroup has the other's PV + S (about 1024 tensor cycles) to
+// produce its P before the tensor core needs it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -41,7 +48,7 @@ struct AttnParams {
     const int32_t* pos;
     const int32_t* cta_indptr;
     const int32_t* cta_items;
-    int32_t* counters;
+    int32_t* counters;   // two per group: [2*group + head slot]
     int32_t* error_word;
     float* dec_part;
     float* dec_lse;
@@ -60,42 +67,41 @@ struct AttnParams {
 };
 
 // Shared-memory plan of a CTA.  DEC = the launch has decode items only: no
-// Q tile and no P buffer, so those bytes become extra K/V stages (more bytes
-// in flight for the HBM-bound path); the decode merge scratch then has its
-// own region.
+// Q tiles, so those bytes become a third K/V stage (more bytes in flight for
+// the HBM-bound path).  The decode merge scratch has its own region.
 template <int D, bool DEC>
 struct Cfg {
+    static constexpr int kWarps = DEC ? 6 : 10;
+    static constexpr int kThreads = kWarps * 32;
     static constexpr int kPanels = D / 64;            // 64-element (128-byte) column panels
     static constexpr int kPanelBytes = 128 * 128;     // one panel of a 128-row tile
     static constexpr int kTileBytes = kPanels * kPanelBytes;  // 128 rows x D bf16
     static constexpr int kStages = DEC ? (D == 128 ? 3 : 6) : (D == 128 ? 2 : 4);
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = DEC ? 0 : kTileBytes;
+    static constexpr int kOffQ = 0;                   // Q tiles 0 and 1 (prefill)
+    static constexpr int kOffK = DEC ? 0 : 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
-    static constexpr int kOffP = kOffV + kStages * kTileBytes;  // P buffer, or the decode scratch
-    static constexpr int kScratchBytes = 4 * kDecRows * D * 4;
-    static constexpr int kPBytes = DEC ? kScratchBytes : 2 * kPanelBytes;  // P: 128 rows x 128 keys bf16
-    static constexpr int kOffCtl = kOffP + kPBytes;
+    static constexpr int kOffScr = kOffV + kStages * kTileBytes;  // decode merge scratch [4][16][D] fp32
+    static constexpr int kScrBytes = 4 * kDecRows * D * 4;
+    static constexpr int kOffCtl = kOffScr + kScrBytes;
     static constexpr int kCtlBytes = 1536;
     static constexpr int kSmem = kOffCtl + kCtlBytes + 1024;  // + slack to align the base to 1024
-    static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kTmemO = 256;           // S buffers at columns 0 and 128
-    static_assert(kScratchBytes <= kPBytes, "decode merge scratch must fit");
+    static constexpr uint32_t kTmemCols = 512;        // S0 [0,128) S1 [128,256) O0, O1 from 256
+    static constexpr uint32_t kTmemO = 256;
     static_assert(kSmem + 64 <= 232448, "shared memory over the per-CTA limit");
+    static_assert(kTmemO + 2 * D <= kTmemCols, "TMEM budget");
 };
 
 struct Ctl {
     uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
     uint64_t q_full, q_empty;
-    uint64_t s_full[2], s_empty[2];
-    uint64_t p_full, p_empty, o_full, o_empty;
+    uint64_t s_full[2], p_full[2], p_empty[2], o_empty[2];
+    uint64_t o_full;
     uint64_t drain;
-    uint64_t csync;  // bounded barrier of the 128 compute threads
-    int4 meta[8];  // per stage: first logical key, valid keys, item, unused
+    uint64_t csync[2];  // bounded barriers of warpgroup 0 / 1 (128 threads each)
+    int4 meta[8];       // per stage: first logical key, valid keys, item, unused
     uint32_t tmem_base;
     int abort;
-    int flag_last;
-    int pad;
+    int flag_last[2];
     float dec_m[4][kDecRows];
     float dec_l[4][kDecRows];
     float dec_lr[4][kDecRows];
@@ -103,7 +109,6 @@ struct Ctl {
 
 static_assert(sizeof(Ctl) <= Cfg<128, false>::kCtlBytes, "control block too large");
 
-constexpr int kThreads = 192;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 __device__ __forceinline__ void fail(const AttnParams& p, Ctl* ctl, int code) {
@@ -122,12 +127,12 @@ __device__ __forceinline__ float bf16x2_sum(uint32_t w) {
     return __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
 }
 
-// Barrier of the 128 compute threads built on an mbarrier, so that a wait
-// that can never complete (a warp gave up on a timeout) runs out instead of
-// hanging.  `cnt` counts this thread's passes.
-__device__ __forceinline__ bool compute_sync(const AttnParams& p, Ctl* ctl, uint32_t& cnt) {
-    ptx::mbar_arrive(&ctl->csync);
-    const bool ok = wait_bar(p, ctl, &ctl->csync, cnt & 1, kErrTimeoutCompute);
+// Barrier of one warpgroup (128 threads) built on an mbarrier, so that a
+// wait that can never complete (a warp gave up on a timeout) runs out
+// instead of hanging.  `cnt` counts this thread's passes.
+__device__ __forceinline__ bool compute_sync(const AttnParams& p, Ctl* ctl, int wg, uint32_t& cnt) {
+    ptx::mbar_arrive(&ctl->csync[wg]);
+    const bool ok = wait_bar(p, ctl, &ctl->csync[wg], cnt & 1, kErrTimeoutCompute);
     ++cnt;
     return ok;
 }
@@ -153,67 +158,72 @@ __device__ void producer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int i0, i
         const Item it = p.items[p.cta_items[ii]];
         const Group g = p.groups[it.group];
         int kvh = g.head;
-        if (it.kind == kPrefill) {
+        if (!DEC && it.kind == kPrefill) {
             kvh = g.head / p.G;
+            const int nh = g.pad;  // query heads of the item: 1 or 2 (consecutive, same kv head)
             if (!wait_bar(p, ctl, &ctl->q_empty, (q_cnt & 1) ^ 1, kErrTimeoutProducer)) goto drain;
-            ptx::mbar_arrive_expect_tx(&ctl->q_full, C::kTileBytes);
-            for (int pn = 0; pn < C::kPanels; ++pn)
-                ptx::tma_load_3d(smem + C::kOffQ + pn * C::kPanelBytes, tmQ, pn * 64, g.head, g.row0, &ctl->q_full);
+            ptx::mbar_arrive_expect_tx(&ctl->q_full, nh * C::kTileBytes);
+            for (int k = 0; k < nh; ++k)
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    ptx::tma_load_3d(smem + C::kOffQ + k * C::kTileBytes + pn * C::kPanelBytes, tmQ, pn * 64,
+                                     g.head + k, g.row0, &ctl->q_full);
             ++q_cnt;
         }
-        // KV tiles are 128-key windows of the item's logical key range.  A
-        // window that lies inside one segment is one TMA rectangle; where it
-        // spans segments, each piece is fetched from its own segment, one
-        // 16-row box per block (segments are whole blocks, so every piece is).
-        int r = it.first_run;
-        int tiles = 0;
-        for (int t0 = it.kb; t0 < it.ke; t0 += kTileKeys) {
-            if (tiles >= it.pad) {  // plan inconsistent: never run past the item
-                fail(p, ctl, kErrBadIndex);
-                goto drain;
-            }
-            ++tiles;
-            const int t1 = min(t0 + kTileKeys, it.ke);
-            const int n = t1 - t0;
-            const int st = kv_cnt % C::kStages;
-            const uint32_t ph = (kv_cnt / C::kStages) & 1;
-            if (!wait_bar(p, ctl, &ctl->k_empty[st], ph ^ 1, kErrTimeoutProducer)) goto drain;
-            if (!wait_bar(p, ctl, &ctl->v_empty[st], ph ^ 1, kErrTimeoutProducer)) goto drain;
-            ctl->meta[st] = make_int4(t0, n, ii, 0);
-            uint8_t* ks = smem + C::kOffK + st * C::kTileBytes;
-            uint8_t* vs = smem + C::kOffV + st * C::kTileBytes;
-            const uint32_t bytes = (uint32_t)(((n + kBlock - 1) & ~(kBlock - 1)) * D * 2);
-            ptx::mbar_arrive_expect_tx(&ctl->k_full[st], bytes);
-            ptx::mbar_arrive_expect_tx(&ctl->v_full[st], bytes);
-            int cur = t0;
-            while (cur < t1) {
-                if (r < 0 || r >= p.n_runs) {
+        {
+            // KV tiles are 128-key windows of the item's logical key range.  A
+            // window that lies inside one segment is one TMA rectangle; where it
+            // spans segments, each piece is fetched from its own segment, one
+            // 16-row box per block (segments are whole blocks, so every piece is).
+            int r = it.first_run;
+            int tiles = 0;
+            for (int t0 = it.kb; t0 < it.ke; t0 += kTileKeys) {
+                if (tiles >= it.pad) {  // plan inconsistent: never run past the item
                     fail(p, ctl, kErrBadIndex);
                     goto drain;
                 }
-                const Run R = p.runs[r];
-                const int rend = R.log_start + R.n_tok;
-                if (cur >= rend) { ++r; continue; }
-                const int pend = min(t1, rend);
-                const int phys = R.phys_row + (cur - R.log_start);
-                const int off = cur - t0;
-                if (off == 0 && pend - cur == kTileKeys) {
-                    for (int pn = 0; pn < C::kPanels; ++pn) {
-                        ptx::tma_load_3d(ks + pn * C::kPanelBytes, tmK, pn * 64, kvh, phys, &ctl->k_full[st]);
-                        ptx::tma_load_3d(vs + pn * C::kPanelBytes, tmV, pn * 64, kvh, phys, &ctl->v_full[st]);
+                ++tiles;
+                const int t1 = min(t0 + kTileKeys, it.ke);
+                const int n = t1 - t0;
+                const int st = kv_cnt % C::kStages;
+                const uint32_t ph = (kv_cnt / C::kStages) & 1;
+                if (!wait_bar(p, ctl, &ctl->k_empty[st], ph ^ 1, kErrTimeoutProducer)) goto drain;
+                if (!wait_bar(p, ctl, &ctl->v_empty[st], ph ^ 1, kErrTimeoutProducer)) goto drain;
+                ctl->meta[st] = make_int4(t0, n, ii, 0);
+                uint8_t* ks = smem + C::kOffK + st * C::kTileBytes;
+                uint8_t* vs = smem + C::kOffV + st * C::kTileBytes;
+                const uint32_t bytes = (uint32_t)(((n + kBlock - 1) & ~(kBlock - 1)) * D * 2);
+                ptx::mbar_arrive_expect_tx(&ctl->k_full[st], bytes);
+                ptx::mbar_arrive_expect_tx(&ctl->v_full[st], bytes);
+                int cur = t0;
+                while (cur < t1) {
+                    if (r < 0 || r >= p.n_runs) {
+                        fail(p, ctl, kErrBadIndex);
+                        goto drain;
                     }
-                } else {
-                    const int nb = (pend - cur + kBlock - 1) / kBlock;
-                    for (int b = 0; b < nb; ++b)
+                    const Run R = p.runs[r];
+                    const int rend = R.log_start + R.n_tok;
+                    if (cur >= rend) { ++r; continue; }
+                    const int pend = min(t1, rend);
+                    const int phys = R.phys_row + (cur - R.log_start);
+                    const int off = cur - t0;
+                    if (off == 0 && pend - cur == kTileKeys) {
                         for (int pn = 0; pn < C::kPanels; ++pn) {
-                            const int so = pn * C::kPanelBytes + (off + b * kBlock) * 128;
-                            ptx::tma_load_3d(ks + so, tmK16, pn * 64, kvh, phys + b * kBlock, &ctl->k_full[st]);
-                            ptx::tma_load_3d(vs + so, tmV16, pn * 64, kvh, phys + b * kBlock, &ctl->v_full[st]);
+                            ptx::tma_load_3d(ks + pn * C::kPanelBytes, tmK, pn * 64, kvh, phys, &ctl->k_full[st]);
+                            ptx::tma_load_3d(vs + pn * C::kPanelBytes, tmV, pn * 64, kvh, phys, &ctl->v_full[st]);
                         }
+                    } else {
+                        const int nb = (pend - cur + kBlock - 1) / kBlock;
+                        for (int b = 0; b < nb; ++b)
+                            for (int pn = 0; pn < C::kPanels; ++pn) {
+                                const int so = pn * C::kPanelBytes + (off + b * kBlock) * 128;
+                                ptx::tma_load_3d(ks + so, tmK16, pn * 64, kvh, phys + b * kBlock, &ctl->k_full[st]);
+                                ptx::tma_load_3d(vs + so, tmV16, pn * 64, kvh, phys + b * kBlock, &ctl->v_full[st]);
+                            }
+                    }
+                    cur = pend;
                 }
-                cur = pend;
+                ++kv_cnt;
             }
-            ++kv_cnt;
         }
     }
 drain:
@@ -239,82 +249,83 @@ template <int D, bool DEC>
 __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int i0, int i1) {
     using C = Cfg<D, DEC>;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, 128, 0, 0);  // Q K-major, K K-major
-    constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, 0, 1);   // P K-major, V MN-major
+    constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, 0, 1);   // P (TMEM), V MN-major
     const uint32_t tbase = ctl->tmem_base;
     const uint32_t sQ = ptx::smem_u32(smem + C::kOffQ);
     const uint32_t sK = ptx::smem_u32(smem + C::kOffK);
     const uint32_t sV = ptx::smem_u32(smem + C::kOffV);
-    const uint32_t sP = ptx::smem_u32(smem + C::kOffP);
-    uint32_t kv_cnt = 0, q_cnt = 0, s_cnt = 0, pv_cnt = 0, o_cnt = 0;
+    uint32_t kv_cnt = 0, q_cnt = 0, pf[2] = {0u, 0u}, oc[2] = {0u, 0u};
+
     for (int ii = i0; ii < i1; ++ii) {
         const Item it = p.items[p.cta_items[ii]];
         const int T = it.pad;  // KV tiles of this item
         if (it.kind != kPrefill) { kv_cnt += T; continue; }
-        const int pmin = p.pos[p.groups[it.group].row0];  // rows ascend: the tile's smallest position
-        if (!wait_bar(p, ctl, &ctl->q_full, q_cnt & 1, kErrTimeoutMma)) goto drain;
+        const Group g = p.groups[it.group];
+        const int nh = g.pad;
+        const int pmin = p.pos[g.row0];  // rows ascend: the tile's smallest position
+        if (!wait_bar(p, ctl, &ctl->q_full, q_cnt & 1, kErrTimeoutMma)) return;
         ++q_cnt;
         for (int j = 0; j <= T; ++j) {
-            if (j < T) {
-                const uint32_t k = kv_cnt + j;
-                const int st = k % C::kStages;
-                const uint32_t ph = (k / C::kStages) & 1;
-                if (!wait_bar(p, ctl, &ctl->k_full[st], ph, kErrTimeoutMma)) goto drain;
-                const int sb = s_cnt & 1;
-                if (!wait_bar(p, ctl, &ctl->s_empty[sb], ((s_cnt >> 1) & 1) ^ 1, kErrTimeoutMma)) goto drain;
-                ptx::tc_fence_after();
-                const uint32_t kbase = sK + st * C::kTileBytes;
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * C::kPanelBytes + (ks & 3) * 32;
-                    const uint64_t ad = ptx::smem_desc(sQ + off, 16, 1024, 2);
-                    const uint64_t bd = ptx::smem_desc(kbase + off, 16, 1024, 2);
-                    ptx::tc_mma_ss(tbase + sb * 128, ad, bd, kIdescS, ks > 0);
+            const int jj = j - 1;
+            const uint32_t kj = kv_cnt + j, kp = kv_cnt + jj;
+            const int st = kj % C::kStages, stp = kp % C::kStages;
+            bool precise = false;
+            int nk = 0;
+            for (int k = 0; k < nh; ++k) {
+                // O_k += P_k V for tile j-1: P_k read from TMEM columns of S_k;
+                // rows that see fewer than 128 keys add a second pass with the
+                // bf16 residual of P, stored 64 columns further
+                if (j >= 1) {
+                    if (!wait_bar(p, ctl, &ctl->p_full[k], pf[k] & 1, kErrTimeoutMma)) return;
+                    ++pf[k];
+                    if (k == 0 && !wait_bar(p, ctl, &ctl->v_full[stp], (kp / C::kStages) & 1, kErrTimeoutMma))
+                        return;
+                    if (jj == 0 && !wait_bar(p, ctl, &ctl->o_empty[k], (oc[k] & 1) ^ 1, kErrTimeoutMma)) return;
+                    ptx::tc_fence_after();
+                    if (k == 0) {
+                        const int4 mt = ctl->meta[stp];
+                        precise = mt.x < kTileKeys && pmin < kTileKeys;
+                        nk = (mt.y + 15) >> 4;
+                    }
+                    const uint32_t vbase = sV + stp * C::kTileBytes;
+                    for (int pass = 0; pass < (precise ? 2 : 1); ++pass)
+                        for (int ks = 0; ks < nk; ++ks) {
+                            const uint64_t bd = ptx::smem_desc(vbase + ks * 16 * 128, C::kPanelBytes, 1024, 2);
+                            ptx::tc_mma_ts(tbase + C::kTmemO + k * D, tbase + k * 128 + pass * 64 + ks * 8, bd,
+                                           kIdescPV, (jj > 0 || ks > 0 || pass > 0) ? 1u : 0u);
+                        }
+                    ptx::tc_commit(&ctl->p_empty[k]);
                 }
-                ptx::tc_commit(&ctl->k_empty[st]);
-                ptx::tc_commit(&ctl->s_full[sb]);
-                ++s_cnt;
-                if (j == T - 1) ptx::tc_commit(&ctl->q_empty);
+                // S_k = Q_k K^T for tile j
+                if (j < T) {
+                    if (k == 0 && !wait_bar(p, ctl, &ctl->k_full[st], (kj / C::kStages) & 1, kErrTimeoutMma))
+                        return;
+                    ptx::tc_fence_after();
+                    const uint32_t kbase = sK + st * C::kTileBytes;
+                    const uint32_t qbase = sQ + k * C::kTileBytes;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t off = (ks >> 2) * C::kPanelBytes + (ks & 3) * 32;
+                        ptx::tc_mma_ss(tbase + k * 128, ptx::smem_desc(qbase + off, 16, 1024, 2),
+                                       ptx::smem_desc(kbase + off, 16, 1024, 2), kIdescS, ks > 0);
+                    }
+                    ptx::tc_commit(&ctl->s_full[k]);
+                }
             }
             if (j >= 1) {
-                const int jj = j - 1;
-                const uint32_t k = kv_cnt + jj;
-                const int st = k % C::kStages;
-                const uint32_t ph = (k / C::kStages) & 1;
-                if (!wait_bar(p, ctl, &ctl->p_full, pv_cnt & 1, kErrTimeoutMma)) goto drain;
-                if (!wait_bar(p, ctl, &ctl->v_full[st], ph, kErrTimeoutMma)) goto drain;
-                if (jj == 0 && !wait_bar(p, ctl, &ctl->o_empty, (o_cnt & 1) ^ 1, kErrTimeoutMma)) goto drain;
-                ptx::tc_fence_after();
-                const int4 mt = ctl->meta[st];
-                const int nk = (mt.y + 15) >> 4;
-                const uint32_t vbase = sV + st * C::kTileBytes;
-                // rows that see fewer than 128 keys get a second pass with the
-                // bf16 residual of P (see prefill_item)
-                const bool precise = mt.x < kTileKeys && pmin < kTileKeys;
-                for (int pass = 0; pass < (precise ? 2 : 1); ++pass) {
-                    if (pass == 1) {
-                        if (!wait_bar(p, ctl, &ctl->p_full, pv_cnt & 1, kErrTimeoutMma)) goto drain;
-                        ptx::tc_fence_after();
-                    }
-                    for (int ks = 0; ks < nk; ++ks) {
-                        const uint64_t ad =
-                            ptx::smem_desc(sP + (ks >> 2) * C::kPanelBytes + (ks & 3) * 32, 16, 1024, 2);
-                        const uint64_t bd = ptx::smem_desc(vbase + ks * 16 * 128, C::kPanelBytes, 1024, 2);
-                        ptx::tc_mma_ss(tbase + C::kTmemO, ad, bd, kIdescPV, (jj > 0 || ks > 0 || pass > 0) ? 1u : 0u);
-                    }
-                    ptx::tc_commit(&ctl->p_empty);
-                    ++pv_cnt;
-                }
-                ptx::tc_commit(&ctl->v_empty[st]);
+                ptx::tc_commit(&ctl->v_empty[stp]);
                 if (jj == T - 1) {
                     ptx::tc_commit(&ctl->o_full);
-                    ++o_cnt;
+                    for (int k = 0; k < nh; ++k) ++oc[k];
                 }
+            }
+            if (j < T) {
+                ptx::tc_commit(&ctl->k_empty[st]);
+                if (j == T - 1) ptx::tc_commit(&ctl->q_empty);
             }
         }
         kv_cnt += T;
     }
-drain:
-    return;
 }
 
 // ----------------------------------------------------- output helpers --
@@ -330,7 +341,6 @@ template <int D, bool DEC>
 __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const Item& it, const Group& g,
                             uint32_t& kv_cnt, uint32_t& cs, int cw, int lane) {
     using C = Cfg<D, DEC>;
-    constexpr int KS = D / 16;  // k-steps over the head dimension
     constexpr int NT = D / 8;   // 8-column output tiles
     const int G = p.G;
     const int M = g.nrows * G;
@@ -340,24 +350,28 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
     const int prow0 = gr < M ? p.pos[g.row0 + gr / G] : -1;
     const int prow1 = gr + 8 < M ? p.pos[g.row0 + (gr + 8) / G] : -1;
 
-    // Q fragments (rows = query row x head, zero past M)
-    uint32_t qa[KS][4];
+    // Q (rows = query row x head, zero past M) staged in shared memory as
+    // [16][D] bf16 with 16-byte chunks XOR-swizzled by row, read back as MMA
+    // A fragments with ldmatrix (the merge scratch is free until the tiles
+    // are done)
+    uint8_t* qs = smem + C::kOffScr;
     {
-        const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
-        auto qword = [&](int m, int dim) -> uint32_t {
-            if (m >= M) return 0u;
-            const int64_t row = g.row0 + m / G;
-            const int64_t h = (int64_t)kvh * G + m % G;
-            return qw[((row * p.Hq + h) * D + dim) >> 1];
-        };
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            qa[ks][0] = qword(gr, ks * 16 + 2 * tq);
-            qa[ks][1] = qword(gr + 8, ks * 16 + 2 * tq);
-            qa[ks][2] = qword(gr, ks * 16 + 8 + 2 * tq);
-            qa[ks][3] = qword(gr + 8, ks * 16 + 8 + 2 * tq);
+        const int tid = cw * 32 + lane;
+        const uint4* qg = reinterpret_cast<const uint4*>(p.q);
+        for (int e = tid; e < kDecRows * (D / 8); e += 128) {
+            const int m = e / (D / 8), c = e % (D / 8);
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (m < M) {
+                const int64_t row = g.row0 + m / G;
+                const int64_t h = (int64_t)kvh * G + m % G;
+                v = qg[((row * p.Hq + h) * D) / 8 + c];
+            }
+            *reinterpret_cast<uint4*>(qs + m * (D * 2) + ((c ^ (m & 7)) << 4)) = v;
         }
+        if (!compute_sync(p, ctl, 0, cs)) return false;
     }
+    const uint32_t qsa = ptx::smem_u32(qs);
+    const int qrow = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row this lane addresses
 
     float o[NT][4];
 #pragma unroll
@@ -381,15 +395,23 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
             const uint32_t vb = ptx::smem_u32(smem + C::kOffV + st * C::kTileBytes);
             float s[4][4];
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-                const int key = key0 + nt * 8 + (lane & 7);
+            for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
-                for (int kk = 0; kk < D / 32; ++kk) {
+            for (int kk = 0; kk < D / 32; ++kk) {
+                uint32_t qa0[4], qa1[4];
+                {
+                    const int c0 = 4 * kk + (lane >> 4);  // chunk of k-step 2kk
+                    ptx::ldmatrix_x4(qsa + qrow * (D * 2) + ((c0 ^ (qrow & 7)) << 4), qa0[0], qa0[1], qa0[2], qa0[3]);
+                    const int c1 = c0 + 2;                 // k-step 2kk+1
+                    ptx::ldmatrix_x4(qsa + qrow * (D * 2) + ((c1 ^ (qrow & 7)) << 4), qa1[0], qa1[1], qa1[2], qa1[3]);
+                }
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int key = key0 + nt * 8 + (lane & 7);
                     uint32_t b0, b1, b2, b3;
                     ptx::ldmatrix_x4(kb + sw128_off<D>(key, kk * 4 + (lane >> 3)), b0, b1, b2, b3);
-                    ptx::mma_bf16_16816(s[nt], qa[2 * kk], b0, b1);
-                    ptx::mma_bf16_16816(s[nt], qa[2 * kk + 1], b2, b3);
+                    ptx::mma_bf16_16816(s[nt], qa0, b0, b1);
+                    ptx::mma_bf16_16816(s[nt], qa1, b2, b3);
                 }
             }
             // mask (key inside the tile, causal key <= row position), scale to log2 units
@@ -486,7 +508,7 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
                 }
             }
         }
-        if (!compute_sync(p, ctl, cs)) return false;
+        if (!compute_sync(p, ctl, 0, cs)) return false;
         if (cw == 0 && lane == 0) {
             ptx::mbar_arrive(&ctl->k_empty[st]);
             ptx::mbar_arrive(&ctl->v_empty[st]);
@@ -503,7 +525,7 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
     rrun0 += __shfl_xor_sync(0xffffffffu, rrun0, 2);
     rrun1 += __shfl_xor_sync(0xffffffffu, rrun1, 1);
     rrun1 += __shfl_xor_sync(0xffffffffu, rrun1, 2);
-    float* scr = reinterpret_cast<float*>(smem + C::kOffP);  // [4][16][D]
+    float* scr = reinterpret_cast<float*>(smem + C::kOffScr);  // [4][16][D]
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
         const int c = i * 8 + 2 * tq;
@@ -518,7 +540,7 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
         ctl->dec_lr[cw][gr] = rrun0;
         ctl->dec_lr[cw][gr + 8] = rrun1;
     }
-    if (!compute_sync(p, ctl, cs)) return false;
+    if (!compute_sync(p, ctl, 0, cs)) return false;
     const int tid = cw * 32 + lane;
     const bool split = g.n_parts > 1;
     float* part = split ? p.dec_part + (int64_t)(g.slot + it.part) * kDecRows * D : nullptr;
@@ -553,13 +575,13 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
     }
     if (split) {
         __threadfence();
-        if (!compute_sync(p, ctl, cs)) return false;
+        if (!compute_sync(p, ctl, 0, cs)) return false;
         if (tid == 0) {
-            const int old = atomicAdd(&p.counters[it.group], 1);
-            ctl->flag_last = (old == g.n_parts - 1);
+            const int old = atomicAdd(&p.counters[2 * it.group], 1);
+            ctl->flag_last[0] = (old == g.n_parts - 1);
         }
-        if (!compute_sync(p, ctl, cs)) return false;
-        if (ctl->flag_last) {
+        if (!compute_sync(p, ctl, 0, cs)) return false;
+        if (ctl->flag_last[0]) {
             __threadfence();
             const float* base = p.dec_part + (int64_t)g.slot * kDecRows * D;
             const float* lbase = p.dec_lse + (int64_t)g.slot * kDecRows;
@@ -583,282 +605,311 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
                 store_out(p, (row * p.Hq + h) * D + d, val);
                 if (d == 0 && p.lse) p.lse[row * p.Hq + h] = lse2 * kLn2;
             }
-            if (tid == 0) p.counters[it.group] = 0;  // ready for the next launch
+            if (tid == 0) p.counters[2 * it.group] = 0;  // ready for the next launch
         }
     }
-    return compute_sync(p, ctl, cs);  // scratch and flag free for the next item
+    return compute_sync(p, ctl, 0, cs);  // scratch and flag free for the next item
 }
 
 // ----------------------------------------------------- prefill (compute) --
 
+// Probabilities of one S row for rows that see fewer than 128 keys: P as
+// bf16 pairs into columns 0..63 of the S buffer and the bf16 residual
+// p - bf16(p) into columns 64..127, for a second PV pass (one rounding of a
+// few large probabilities would otherwise not average away).  Half 0's
+// residual is held in registers until half 1's scores have been read.
+// Returns (sum of p, sum of what the two PV passes consume).  Kept out of
+// line: it is rare, and its registers must not crowd the common path.
+__device__ __noinline__ float2 precise_probs(uint32_t tS, int lim, float m, float sl) {
+    float sum = 0.f, sumr = 0.f;
+    uint32_t lo0[32];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float s[64];
+        ptx::tmem_ld64(tS + 64 * h, s);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+            s[c] = 64 * h + c < lim ? ptx::ex2(fmaf(s[c], sl, -m)) : 0.f;
+            sum += s[c];
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            pk[i] = ptx::pack_bf16x2(s[2 * i], s[2 * i + 1]);
+            sumr += bf16x2_sum(pk[i]);
+        }
+        ptx::tmem_st32(tS + 32 * h, reinterpret_cast<const float*>(pk));
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float a = s[2 * i], b = s[2 * i + 1];
+            const uint32_t hi = pk[i];
+            const uint32_t lo = ptx::pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
+            sumr += bf16x2_sum(lo);
+            if (h == 0) lo0[i] = lo; else pk[i] = lo;
+        }
+        if (h == 1) {
+            ptx::tmem_st32(tS + 64, reinterpret_cast<const float*>(lo0));
+            ptx::tmem_st32(tS + 96, reinterpret_cast<const float*>(pk));
+        }
+    }
+    ptx::tmem_wait_st();
+    return make_float2(sum, sumr);
+}
+
+// Softmax and epilogue of Q tile `k` (warpgroup k) of a prefill item.
+// Thread = tile row = TMEM lane.
 template <int D, bool DEC>
 __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const Item& it, const Group& g,
-                             uint32_t& kv_cnt, uint32_t& s_cnt, uint32_t& pvb, uint32_t& o_cnt, uint32_t& cs,
-                             int cw, int warp, int lane) {
+                             uint32_t& kv_cnt, uint32_t& sk, uint32_t& pvk, uint32_t& ok_cnt, uint32_t& cs, int k,
+                             int warp, int lane) {
     using C = Cfg<D, DEC>;
     const int quarter = warp & 3;
     const int ri = quarter * 32 + lane;  // tile row = TMEM lane
     const bool valid = ri < g.nrows;
     const int prow = valid ? p.pos[g.row0 + ri] : -1;
     const int pmin = p.pos[g.row0];
+    const int head = g.head + k;
     const uint32_t tlane = ctl->tmem_base + ((uint32_t)(quarter * 32) << 16);
-    uint8_t* pbuf = smem + C::kOffP;
+    const uint32_t tS = tlane + k * 128;             // S_k, later P_k (cols 0..63) and its residual (64..127)
+    const uint32_t tO = tlane + C::kTmemO + k * D;  // O_k
     const int T = it.pad;
-    // l: sum of the fp32 probabilities (gives lse); lr: sum of the same
-    // values rounded to bf16, exactly as the PV MMA consumes them (the
-    // normaliser of the output, so that out is a true weighted mean of V
-    // rows even when one key dominates)
+    const float sl = p.scale_log2;
+    // l: sum of the fp32 probabilities (gives lse); lr: sum of the values the
+    // PV MMA actually consumes (bf16-rounded, plus the residual pass where
+    // there is one), the normaliser of the output
     float m = -INFINITY, l = 0.f, lr = 0.f;
 
     for (int j = 0; j < T; ++j) {
-        const uint32_t k = kv_cnt + j;
-        const int st = k % C::kStages;
-        const uint32_t ph = (k / C::kStages) & 1;
-        const int sb = s_cnt & 1;
-        if (!wait_bar(p, ctl, &ctl->s_full[sb], (s_cnt >> 1) & 1, kErrTimeoutCompute)) return false;
-        if (!wait_bar(p, ctl, &ctl->k_full[st], ph, kErrTimeoutCompute)) return false;
+        const uint32_t kj = kv_cnt + j;
+        const int st = kj % C::kStages;
+        const uint32_t ph = (kj / C::kStages) & 1;
+        if (!wait_bar(p, ctl, &ctl->s_full[k], sk & 1, kErrTimeoutCompute)) return false;
+        ++sk;
+        if (!wait_bar(p, ctl, &ctl->k_full[st], ph, kErrTimeoutCompute)) return false;  // tile metadata
         ptx::tc_fence_after();
         const int4 mt = ctl->meta[st];
         const int kt0 = mt.x, n = mt.y;
-        // rows that see fewer than 128 keys in total get a second PV pass
-        // with the bf16 residual of P (see below); those tiles keep their S
-        // buffer until the second pass has re-read it
+        // rows that see fewer than 128 keys in total: a bf16 rounding of one
+        // probability is not averaged away, so the PV MMA gets a second pass
+        // with the residual p - bf16(p)
         const bool precise = kt0 < kTileKeys && pmin < kTileKeys;
-        float s[128];
-        ptx::tmem_ld128(tlane + sb * 128, s);
-        if (!precise) {
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&ctl->s_empty[sb]);
-        }
-        ++s_cnt;
-
         const int lim = max(0, min(n, prow - kt0 + 1));  // visible columns of this row
+        // row max, over two 64-column halves of S (eight independent chains)
         float mx;
         {
-            // eight independent chains, then a tree: no 128-long dependency
             float m8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], c < lim ? s[c] : -INFINITY);
+            for (int h = 0; h < 2; ++h) {
+                float s[64];
+                ptx::tmem_ld64(tS + 64 * h, s);
+#pragma unroll
+                for (int c = 0; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], 64 * h + c < lim ? s[c] : -INFINITY);
+            }
             mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                        fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         }
         float alpha = 1.f;
         bool resc = false;
         if (lim > 0) {
-            const float ms = mx * p.scale_log2;
+            const float ms = mx * sl;
             // keep the running max unless the new one is larger by more than
-            // 8 (log2 units): values stay <= 256, rescales become rare
+            // 8 (log2 units): values stay <= 256, rescales of O become rare
             if (ms > m + 8.f) {
                 alpha = ptx::ex2(m - ms);
                 resc = j > 0;
                 m = ms;
             }
         }
-        // previous PV batches done: the P buffer is free and O is current
-        if (j > 0 && !wait_bar(p, ctl, &ctl->p_empty, (pvb - 1) & 1, kErrTimeoutCompute)) return false;
         if (__any_sync(0xffffffffu, resc)) {
+            // O_k must hold PV_k(j-1) before it is scaled
+            if (!wait_bar(p, ctl, &ctl->p_empty[k], (pvk - 1) & 1, kErrTimeoutCompute)) return false;
             ptx::tc_fence_after();
             const float f = resc ? alpha : 1.f;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 float ov[32];
-                ptx::tmem_ld32(tlane + C::kTmemO + c * 32, ov);
+                ptx::tmem_ld32(tO + c * 32, ov);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) ov[i] *= f;
-                ptx::tmem_st32(tlane + C::kTmemO + c * 32, ov);
+                ptx::tmem_st32(tO + c * 32, ov);
             }
             ptx::tmem_wait_st();
         }
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f}, sr4[4] = {0.f, 0.f, 0.f, 0.f};
-        const float sl = p.scale_log2;
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        float sr4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (!precise) {
+            // probabilities of each half, packed as bf16 pairs into the first
+            // 64 columns of S_k (half h's P overwrites columns already read)
 #pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8) {
-            float pv[8];
+            for (int h = 0; h < 2; ++h) {
+                float s[64];
+                ptx::tmem_ld64(tS + 64 * h, s);
+                uint32_t pk[32];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = c8 * 8 + e;
-                pv[e] = c < lim ? ptx::ex2(fmaf(s[c], sl, -m)) : 0.f;
-                sum4[e & 3] += pv[e];
+                for (int i = 0; i < 32; ++i) {
+                    const int c = 64 * h + 2 * i;
+                    const float a = c < lim ? ptx::ex2(fmaf(s[2 * i], sl, -m)) : 0.f;
+                    const float b = c + 1 < lim ? ptx::ex2(fmaf(s[2 * i + 1], sl, -m)) : 0.f;
+                    sum4[(2 * i) & 3] += a;
+                    sum4[(2 * i + 1) & 3] += b;
+                    pk[i] = ptx::pack_bf16x2(a, b);
+                    sr4[i & 3] += bf16x2_sum(pk[i]);
+                }
+                ptx::tmem_st32(tS + 32 * h, reinterpret_cast<const float*>(pk));
             }
-            uint4 w;
-            w.x = ptx::pack_bf16x2(pv[0], pv[1]);
-            w.y = ptx::pack_bf16x2(pv[2], pv[3]);
-            w.z = ptx::pack_bf16x2(pv[4], pv[5]);
-            w.w = ptx::pack_bf16x2(pv[6], pv[7]);
-            sr4[c8 & 3] += (bf16x2_sum(w.x) + bf16x2_sum(w.y)) + (bf16x2_sum(w.z) + bf16x2_sum(w.w));
-            const int panel = c8 >> 3, cc = c8 & 7;
-            *reinterpret_cast<uint4*>(pbuf + panel * C::kPanelBytes + ri * 128 + ((cc ^ (ri & 7)) << 4)) = w;
+        } else {
+            const float2 r = precise_probs(tS, lim, m, sl);
+            sum4[0] += r.x;
+            sr4[0] += r.y;
         }
         const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-        float sumr = (sr4[0] + sr4[1]) + (sr4[2] + sr4[3]);
+        const float sumr = (sr4[0] + sr4[1]) + (sr4[2] + sr4[3]);
         l = l * alpha + sum;
-        lr = lr * alpha;
-        if (n & (kBlock - 1)) {
-            // The tile ends inside the sequence's last, partial block: rows
-            // [n, ceil16(n)) of the V stage are pool rows past L_s and may
-            // hold anything.  The PV MMA covers whole 16-row steps, so zero
-            // them (P is already 0 there).
+        lr = lr * alpha + sumr;
+        if (k == 0 && (n & (kBlock - 1))) {
+            // The tile ends inside a block: rows [n, ceil16(n)) of the V stage
+            // may be pool rows past L_s holding anything.  The PV MMA covers
+            // whole 16-row steps, so zero them (P is 0 there).  Warpgroup 0's
+            // PV comes first, so this also covers warpgroup 1.
             if (!wait_bar(p, ctl, &ctl->v_full[st], ph, kErrTimeoutCompute)) return false;
             const int nz = ((n + 15) & ~15) - n;
             uint8_t* vs = smem + C::kOffV + st * C::kTileBytes;
             const int chunks = nz * (D / 8);
-            for (int c = cw * 32 + lane; c < chunks; c += 128) {
+            for (int c = ri; c < chunks; c += 128) {
                 const int r = n + c / (D / 8), cc = c % (D / 8);
                 *reinterpret_cast<uint4*>(vs + (cc >> 3) * C::kPanelBytes + r * 128 + (cc & 7) * 16) =
                     make_uint4(0, 0, 0, 0);
             }
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(&ctl->p_full);
-        ++pvb;
-        if (precise) {
-            // Rows of this tile see fewer than 128 keys in total, so a bf16
-            // rounding of one probability is not averaged away (the output
-            // error would be ~2^-9 * |V|).  Second pass: the bf16 residual
-            // p - bf16(p), accumulated by a second PV MMA once the first
-            // one has released the P buffer.  p is recomputed from S.
-            if (!wait_bar(p, ctl, &ctl->p_empty, (pvb - 1) & 1, kErrTimeoutCompute)) return false;
-            float s2[128];
-            ptx::tmem_ld128(tlane + sb * 128, s2);
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&ctl->s_empty[sb]);
-            float sumlo = 0.f;
-#pragma unroll
-            for (int c8 = 0; c8 < 16; ++c8) {
-                uint32_t wv[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = c8 * 8 + 2 * e;
-                    const float a = c < lim ? ptx::ex2(fmaf(s2[c], sl, -m)) : 0.f;
-                    const float b = c + 1 < lim ? ptx::ex2(fmaf(s2[c + 1], sl, -m)) : 0.f;
-                    const uint32_t hi = ptx::pack_bf16x2(a, b);
-                    wv[e] = ptx::pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
-                    sumlo += bf16x2_sum(wv[e]);
-                }
-                const int panel = c8 >> 3, cc = c8 & 7;
-                *reinterpret_cast<uint4*>(pbuf + panel * C::kPanelBytes + ri * 128 + ((cc ^ (ri & 7)) << 4)) =
-                    make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            }
-            sumr += sumlo;
             ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(&ctl->p_full);
-            ++pvb;
         }
-        lr += sumr;
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(&ctl->p_full[k]);
+        ++pvk;
     }
     kv_cnt += T;
 
-    // epilogue
-    if (!wait_bar(p, ctl, &ctl->o_full, o_cnt & 1, kErrTimeoutCompute)) return false;
-    ++o_cnt;
+    // epilogue: O_k row in 32-column chunks
+    if (!wait_bar(p, ctl, &ctl->o_full, ok_cnt & 1, kErrTimeoutCompute)) return false;
+    ++ok_cnt;
     ptx::tc_fence_after();
-    float ov[D];
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tlane + C::kTmemO + c * 32, ov + c * 32);
-    ptx::tc_fence_before();
-    ptx::mbar_arrive(&ctl->o_empty);
-
     const float inv = lr > 0.f ? 1.f / lr : 0.f;
     const float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
-    const int tid = cw * 32 + lane;
-    if (g.n_parts == 1) {
-        if (valid) {
-            const int64_t base = ((int64_t)(g.row0 + ri) * p.Hq + g.head) * D;
+    const bool split = g.n_parts > 1;
+    const int64_t slot0 = split ? ((int64_t)(g.slot + it.part) * 2 + k) * kTileRows : 0;
+    const int64_t obase = ((int64_t)(g.row0 + ri) * p.Hq + head) * D;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+        float ov[32];
+        ptx::tmem_ld32(tO + c * 32, ov);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ov[i] *= inv;
+        if (split) {
+            float4* dst = reinterpret_cast<float4*>(p.pre_part + (slot0 + ri) * D + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
+        } else if (valid) {
             if (p.out_fp32) {
-                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + base);
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + c * 32);
 #pragma unroll
-                for (int c = 0; c < D / 4; ++c)
-                    dst[c] = make_float4(ov[4 * c] * inv, ov[4 * c + 1] * inv, ov[4 * c + 2] * inv, ov[4 * c + 3] * inv);
+                for (int i = 0; i < 8; ++i) dst[i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
             } else {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + base);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + c * 32);
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c) {
+                for (int i = 0; i < 4; ++i) {
                     uint4 w;
-                    w.x = ptx::pack_bf16x2(ov[8 * c] * inv, ov[8 * c + 1] * inv);
-                    w.y = ptx::pack_bf16x2(ov[8 * c + 2] * inv, ov[8 * c + 3] * inv);
-                    w.z = ptx::pack_bf16x2(ov[8 * c + 4] * inv, ov[8 * c + 5] * inv);
-                    w.w = ptx::pack_bf16x2(ov[8 * c + 6] * inv, ov[8 * c + 7] * inv);
-                    dst[c] = w;
+                    w.x = ptx::pack_bf16x2(ov[8 * i], ov[8 * i + 1]);
+                    w.y = ptx::pack_bf16x2(ov[8 * i + 2], ov[8 * i + 3]);
+                    w.z = ptx::pack_bf16x2(ov[8 * i + 4], ov[8 * i + 5]);
+                    w.w = ptx::pack_bf16x2(ov[8 * i + 6], ov[8 * i + 7]);
+                    dst[i] = w;
                 }
             }
-            if (p.lse) p.lse[(int64_t)(g.row0 + ri) * p.Hq + g.head] = lse2 * kLn2;
         }
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(&ctl->o_empty[k]);
+    if (!split) {
+        if (valid && p.lse) p.lse[(int64_t)(g.row0 + ri) * p.Hq + head] = lse2 * kLn2;
         return true;
     }
-    // split group: write this part, the last part to arrive merges
-    {
-        float* part = p.pre_part + ((int64_t)(g.slot + it.part) * kTileRows + ri) * D;
-        float4* dst = reinterpret_cast<float4*>(part);
-#pragma unroll
-        for (int c = 0; c < D / 4; ++c)
-            dst[c] = make_float4(ov[4 * c] * inv, ov[4 * c + 1] * inv, ov[4 * c + 2] * inv, ov[4 * c + 3] * inv);
-        p.pre_lse[(int64_t)(g.slot + it.part) * kTileRows + ri] = lse2;
-    }
+    // split group: this part is written; the last part to arrive merges
+    p.pre_lse[slot0 + ri] = lse2;
     __threadfence();
-    if (!compute_sync(p, ctl, cs)) return false;
-    if (tid == 0) {
-        const int old = atomicAdd(&p.counters[it.group], 1);
-        ctl->flag_last = (old == g.n_parts - 1);
+    if (!compute_sync(p, ctl, k, cs)) return false;
+    if (ri == 0) {
+        const int old = atomicAdd(&p.counters[2 * it.group + k], 1);
+        ctl->flag_last[k] = (old == g.n_parts - 1);
     }
-    if (!compute_sync(p, ctl, cs)) return false;
-    if (ctl->flag_last) {
+    if (!compute_sync(p, ctl, k, cs)) return false;
+    if (ctl->flag_last[k]) {
         __threadfence();
         if (valid) {
             float mm = -INFINITY;
             for (int q = 0; q < g.n_parts; ++q)
-                mm = fmaxf(mm, __ldcg(p.pre_lse + (int64_t)(g.slot + q) * kTileRows + ri));
+                mm = fmaxf(mm, __ldcg(p.pre_lse + ((int64_t)(g.slot + q) * 2 + k) * kTileRows + ri));
             float L = 0.f;
-            float acc[D];
+            if (mm != -INFINITY)
+                for (int q = 0; q < g.n_parts; ++q)
+                    L += ptx::ex2(__ldcg(p.pre_lse + ((int64_t)(g.slot + q) * 2 + k) * kTileRows + ri) - mm);
+            const float invL = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                float acc[32];
 #pragma unroll
-            for (int d = 0; d < D; ++d) acc[d] = 0.f;
-            if (mm != -INFINITY) {
-                for (int q = 0; q < g.n_parts; ++q) {
-                    const float f = ptx::ex2(__ldcg(p.pre_lse + (int64_t)(g.slot + q) * kTileRows + ri) - mm);
-                    L += f;
-                    const float4* src =
-                        reinterpret_cast<const float4*>(p.pre_part + ((int64_t)(g.slot + q) * kTileRows + ri) * D);
+                for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+                if (mm != -INFINITY) {
+                    for (int q = 0; q < g.n_parts; ++q) {
+                        const int64_t sq = ((int64_t)(g.slot + q) * 2 + k) * kTileRows + ri;
+                        const float f = ptx::ex2(__ldcg(p.pre_lse + sq) - mm) * invL;
+                        const float4* src = reinterpret_cast<const float4*>(p.pre_part + sq * D + c * 32);
 #pragma unroll
-                    for (int c = 0; c < D / 4; ++c) {
-                        const float4 v = __ldcg(src + c);
-                        acc[4 * c] += f * v.x; acc[4 * c + 1] += f * v.y;
-                        acc[4 * c + 2] += f * v.z; acc[4 * c + 3] += f * v.w;
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 v = __ldcg(src + i);
+                            acc[4 * i] += f * v.x; acc[4 * i + 1] += f * v.y;
+                            acc[4 * i + 2] += f * v.z; acc[4 * i + 3] += f * v.w;
+                        }
                     }
                 }
-            }
-            const float invL = L > 0.f ? 1.f / L : 0.f;
-            const int64_t base = ((int64_t)(g.row0 + ri) * p.Hq + g.head) * D;
 #pragma unroll
-            for (int d = 0; d < D; ++d) store_out(p, base + d, acc[d] * invL);
-            if (p.lse) p.lse[(int64_t)(g.row0 + ri) * p.Hq + g.head] = L > 0.f ? (mm + log2f(L)) * kLn2 : -INFINITY;
+                for (int i = 0; i < 32; ++i) store_out(p, obase + c * 32 + i, acc[i]);
+            }
+            if (p.lse) p.lse[(int64_t)(g.row0 + ri) * p.Hq + head] = L > 0.f ? (mm + log2f(L)) * kLn2 : -INFINITY;
         }
-        if (tid == 0) p.counters[it.group] = 0;
+        if (ri == 0) p.counters[2 * it.group + k] = 0;  // ready for the next launch
     }
-    return compute_sync(p, ctl, cs);
+    return compute_sync(p, ctl, k, cs);
 }
 
 template <int D, bool DEC>
 __device__ void compute(const AttnParams& p, uint8_t* smem, Ctl* ctl, int i0, int i1, int warp, int lane) {
-    const int cw = warp - 2;
-    uint32_t kv_cnt = 0, s_cnt = 0, pvb = 0, o_cnt = 0, cs = 0;
+    const int wg = (warp - 2) >> 2;  // warpgroup 0 or 1
+    const int cw = (warp - 2) & 3;
+    uint32_t kv_cnt = 0, sk = 0, pvk = 0, ok_cnt = 0, cs = 0;
     for (int ii = i0; ii < i1; ++ii) {
         const Item it = p.items[p.cta_items[ii]];
         const Group g = p.groups[it.group];
-        bool ok;
-        if constexpr (DEC) {
-            ok = decode_item<D, DEC>(p, smem, ctl, it, g, kv_cnt, cs, cw, lane);
-        } else {
-            ok = it.kind == kDecode ? decode_item<D, DEC>(p, smem, ctl, it, g, kv_cnt, cs, cw, lane)
-                                    : prefill_item<D, DEC>(p, smem, ctl, it, g, kv_cnt, s_cnt, pvb, o_cnt, cs, cw,
-                                                           warp, lane);
+        bool ok = true;
+        if (DEC || it.kind == kDecode) {
+            // decode items run on warpgroup 0; warpgroup 1 only keeps count
+            if (wg == 0) ok = decode_item<D, DEC>(p, smem, ctl, it, g, kv_cnt, cs, cw, lane);
+            else kv_cnt += it.pad;
+        } else if constexpr (!DEC) {
+            if (wg < g.pad) {
+                ok = prefill_item<D, DEC>(p, smem, ctl, it, g, kv_cnt, sk, pvk, ok_cnt, cs, wg, warp, lane);
+            } else {  // a one-head item: only the o_full phase and the ring position move on
+                kv_cnt += it.pad;
+                ++ok_cnt;
+            }
         }
         if (!ok) return;
     }
 }
 
 template <int D, bool DEC>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
     msa_attention_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmK16, const __grid_constant__ CUtensorMap tmV,
                          const __grid_constant__ CUtensorMap tmV16, const __grid_constant__ CUtensorMap tmQ) {
@@ -877,18 +928,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::mbar_init(&ctl->q_full, 1);
         ptx::mbar_init(&ctl->q_empty, 1);
-        for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(&ctl->s_full[s], 1);
-            ptx::mbar_init(&ctl->s_empty[s], 128);
+        for (int k = 0; k < 2; ++k) {
+            ptx::mbar_init(&ctl->s_full[k], 1);
+            ptx::mbar_init(&ctl->p_full[k], 128);
+            ptx::mbar_init(&ctl->p_empty[k], 1);
+            ptx::mbar_init(&ctl->o_empty[k], 128);
+            ptx::mbar_init(&ctl->csync[k], 128);
         }
-        ptx::mbar_init(&ctl->p_full, 128);
-        ptx::mbar_init(&ctl->p_empty, 1);
         ptx::mbar_init(&ctl->o_full, 1);
-        ptx::mbar_init(&ctl->o_empty, 128);
         ptx::mbar_init(&ctl->drain, 1);
-        ptx::mbar_init(&ctl->csync, 128);
         ctl->abort = 0;
-        ctl->flag_last = 0;
+        ctl->flag_last[0] = ctl->flag_last[1] = 0;
         ptx::fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -896,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tmap(&tmK16);
         ptx::prefetch_tmap(&tmV);
         ptx::prefetch_tmap(&tmV16);
-        ptx::prefetch_tmap(&tmQ);
+        if (!DEC) ptx::prefetch_tmap(&tmQ);
     }
     if (!DEC && warp == 1 && p.has_prefill) {
         ptx::tmem_alloc(&ctl->tmem_base, C::kTmemCols);
@@ -912,10 +962,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if constexpr (!DEC) {
             if (lane == 0 && p.has_prefill) {
-            mma_issuer<D, DEC>(p, smem, ctl, i0, i1);
-            // every MMA issued must have completed before TMEM is released
-            ptx::tc_commit(&ctl->drain);
-            ptx::mbar_wait(&ctl->drain, 0, &ctl->abort, p.limit_ns);
+                mma_issuer<D, DEC>(p, smem, ctl, i0, i1);
+                // every MMA issued must have completed before TMEM is released
+                ptx::tc_commit(&ctl->drain);
+                static __shared__ int never;
+                never = 0;
+                ptx::mbar_wait(&ctl->drain, 0, &never, 100000000ull);
             }
         }
     } else {
@@ -972,7 +1024,7 @@ static int launch_d(const msa_plan_s* P, const AttnParams& prm, const CUtensorMa
         configured = true;
     }
     msa_attention_kernel<D, DEC>
-        <<<P->grid, kThreads, C::kSmem, st>>>(prm, maps[0], maps[1], maps[2], maps[3], maps[4]);
+        <<<P->grid, C::kThreads, C::kSmem, st>>>(prm, maps[0], maps[1], maps[2], maps[3], maps[4]);
     return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 

@@ -87,9 +87,9 @@ int msa_plan_get_items(msa_plan_t plan, int32_t* items, int32_t* n_items) {
         for (size_t i = 0; i < plan->items.size(); ++i) {
             const msa::Item& it = plan->items[i];
             const msa::Group& g = plan->groups[it.group];
-            int32_t* o = items + 8 * i;
-            o[0] = g.kind; o[1] = g.seq; o[2] = g.head; o[3] = g.row0;
-            o[4] = g.nrows; o[5] = it.kb; o[6] = it.ke; o[7] = it.part;
+            int32_t* o = items + 9 * i;
+            o[0] = g.kind; o[1] = g.seq; o[2] = g.head; o[3] = g.pad; o[4] = g.row0;
+            o[5] = g.nrows; o[6] = it.kb; o[7] = it.ke; o[8] = it.part;
         }
     }
     return MSA_OK;

@@ -27,9 +27,11 @@ struct Run {
 
 // An output group: the rows and heads one merge produces.
 //   decode : rows [row0, row0+nrows) x query heads [head*G, head*G+G), kv head = head
-//   prefill: rows [row0, row0+nrows) x query head `head`
+//   prefill: rows [row0, row0+nrows) x query heads [head, head+pad) (pad =
+//            1 or 2 consecutive heads of one kv head)
 // n_parts > 1 means the key range was split; parts write partials to slots
-// [slot, slot + n_parts) and the last to finish merges them.
+// [slot, slot + n_parts) (two head slots each for prefill) and the last to
+// finish merges them.
 struct Group {
     int32_t kind;
     int32_t seq;
@@ -38,7 +40,7 @@ struct Group {
     int32_t nrows;
     int32_t n_parts;
     int32_t slot;
-    int32_t pad;
+    int32_t pad;  // query heads per group (G for decode, 1 or 2 for prefill)
 };
 
 // A work item: one group's keys [kb, ke), starting in run `first_run`
@@ -64,12 +66,12 @@ struct WsLayout {
     size_t cta_indptr;  // int32[grid + 1]
     size_t cta_items;   // int32[n_items]: item ids per CTA, in processing order
     size_t image_end;   // end of the part copied from the host image
-    size_t counters;    // int32[n_groups]: merge arrival counters (zeroed)
+    size_t counters;    // int32[2 * n_groups]: merge arrival counters per head slot (zeroed)
     size_t counters_end;
     size_t dec_part;    // float[n_dec_slots][kDecRows][D]
     size_t dec_lse;     // float[n_dec_slots][kDecRows]
-    size_t pre_part;    // float[n_pre_slots][kTileRows][D]
-    size_t pre_lse;     // float[n_pre_slots][kTileRows]
+    size_t pre_part;    // float[n_pre_slots][2][kTileRows][D]
+    size_t pre_lse;     // float[n_pre_slots][2][kTileRows]
     size_t total;
 };
 

@@ -148,10 +148,14 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
             const int32_t pmax = P->pos[row0 + nrows - 1];  // rows ascend within a sequence
             const int32_t ke = std::min(pmax + 1, L);
             const int64_t tiles = count_tiles(0, ke);
-            const int32_t nh = kind == kDecode ? Hkv : Hq;
-            for (int32_t h = 0; h < nh; ++h) {
+            // decode: one group per kv head (all G query heads packed);
+            // prefill: one group per pair of query heads sharing a kv head
+            // (G even), else per query head; Group.pad = query heads per group
+            const int32_t hpg = kind == kDecode ? G : (G % 2 == 0 ? 2 : 1);
+            const int32_t ngr = kind == kDecode ? Hkv : Hq / hpg;
+            for (int32_t h = 0; h < ngr; ++h) {
                 Pending pd;
-                pd.g = Group{kind, s, h, row0, nrows, 1, -1, 0};
+                pd.g = Group{kind, s, kind == kDecode ? h : h * hpg, row0, nrows, 1, -1, hpg};
                 pd.ke = ke;
                 pd.tiles = tiles;
                 pend.push_back(pd);
@@ -289,12 +293,12 @@ void build_image(msa_plan_s* P) {
     W.cta_indptr = sec(P->cta_indptr.size() * sizeof(int32_t));
     W.cta_items = sec(P->cta_items.size() * sizeof(int32_t));
     W.image_end = o;
-    W.counters = sec(P->groups.size() * sizeof(int32_t));
+    W.counters = sec(2 * P->groups.size() * sizeof(int32_t));
     W.counters_end = o;
     W.dec_part = sec((size_t)P->n_dec_slots * kDecRows * D * sizeof(float));
     W.dec_lse = sec((size_t)P->n_dec_slots * kDecRows * sizeof(float));
-    W.pre_part = sec((size_t)P->n_pre_slots * kTileRows * D * sizeof(float));
-    W.pre_lse = sec((size_t)P->n_pre_slots * kTileRows * sizeof(float));
+    W.pre_part = sec((size_t)P->n_pre_slots * 2 * kTileRows * D * sizeof(float));
+    W.pre_lse = sec((size_t)P->n_pre_slots * 2 * kTileRows * sizeof(float));
     W.total = align_up(o, 256);
 
     P->image.assign(W.image_end, 0);

@@ -173,7 +173,7 @@ def msa_plan_get_items(plan) -> np.ndarray:
     lib = load()
     n = ctypes.c_int32(0)
     _check(lib.msa_plan_get_items(plan, None, ctypes.byref(n)), "msa_plan_get_items")
-    out = np.zeros((max(n.value, 1), 8), np.int32)
+    out = np.zeros((max(n.value, 1), 9), np.int32)
     _check(lib.msa_plan_get_items(plan, out.ctypes.data, ctypes.byref(n)), "msa_plan_get_items")
     return out[: n.value]
 

@@ -83,11 +83,16 @@ def _check_coverage(wl, plan, enumerate_keys=True):
     q_indptr = wl.q_indptr
     owner = np.zeros((wl.num_q_rows, wl.num_q_heads), np.int32)
     groups = {}
-    for kind, seq, head, row0, nrows, kb, ke, part in items:
-        groups.setdefault((kind, seq, head, row0, nrows), []).append((part, kb, ke))
-    for (kind, seq, head, row0, nrows), parts in groups.items():
+    for kind, seq, head, nh, row0, nrows, kb, ke, part in items:
+        groups.setdefault((kind, seq, head, nh, row0, nrows), []).append((part, kb, ke))
+    for (kind, seq, head, nh, row0, nrows), parts in groups.items():
         assert q_indptr[seq] <= row0 and row0 + nrows <= q_indptr[seq + 1]
-        heads = range(head * G, head * G + G) if kind == 0 else [head]
+        if kind == 0:
+            assert nh == G
+            heads = range(head * G, head * G + G)
+        else:
+            assert nh in (1, 2) and (nh == 1 or head // G == (head + 1) // G)
+            heads = range(head, head + nh)
         for h in heads:
             owner[row0:row0 + nrows, h] += 1
         parts.sort()
@@ -104,7 +109,7 @@ def _check_coverage(wl, plan, enumerate_keys=True):
     assert np.all(owner == 1)
     if enumerate_keys:
         # every visible key of every row is inside exactly one part's range
-        for (kind, seq, head, row0, nrows), parts in groups.items():
+        for (kind, seq, head, nh, row0, nrows), parts in groups.items():
             L = int(wl.seq_lens[seq])
             for r in range(row0, row0 + nrows):
                 vis = min(int(q_pos[r]) + 1, L)
@@ -190,8 +195,8 @@ def test_empty_sequence_and_split_groups():
     try:
         items = msa.msa_plan_get_items(plan)
         empty = items[items[:, 1] == 0]
-        assert len(empty) == 2 and np.all(empty[:, 5] == 0) and np.all(empty[:, 6] == 0)
+        assert len(empty) == 2 and np.all(empty[:, 6] == 0) and np.all(empty[:, 7] == 0)
         long = items[items[:, 1] == 1]
-        assert long[:, 7].max() > 0  # split into several parts
+        assert long[:, 8].max() > 0  # split into several parts
     finally:
         msa.msa_plan_destroy(plan)
