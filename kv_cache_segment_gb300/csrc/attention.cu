@@ -46,8 +46,9 @@ struct AttnParams {
     const Group* groups;
     const Run* runs;
     const int32_t* pos;
-    const int32_t* cta_indptr;
-    const int32_t* cta_items;
+    const int32_t* order;  // item ids, longest first (the dynamic queue)
+    int32_t* sched;        // [0] queue head, [1] CTAs finished
+    int32_t n_items;
     int32_t* counters;   // two per group: [2*group + head slot]
     int32_t* error_word;
     float* dec_part;
@@ -71,8 +72,19 @@ struct AttnParams {
 // the HBM-bound path).  The decode merge scratch has its own region.
 template <int D, bool DEC>
 struct Cfg {
-    static constexpr int kWarps = DEC ? 6 : 10;
+    // mixed launch: 3 warpgroups (producer/MMA, softmax 0, softmax 1) with
+    // a register split; decode-only: producer + 4 compute warps
+    static constexpr int kWarps = DEC ? 6 : 12;
     static constexpr int kThreads = kWarps * 32;
+    static constexpr int kFirstCompute = DEC ? 2 : 4;  // first compute warp
+    // Register split of the mixed launch (setmaxnreg): 384 threads launch with
+    // 168 registers each (3 warps share an SM sub-partition's 16K registers);
+    // warpgroup 0 gives back down to kRegsLow, the two softmax warpgroups grow
+    // to kRegsHigh.  128*72 + 256*216 = 384*168 exactly.
+    static constexpr int kRegsLaunch = 168;
+    static constexpr int kRegsLow = 72;
+    static constexpr int kRegsHigh = 216;
+    static_assert(DEC || 128 * kRegsLow + 256 * kRegsHigh == kThreads * kRegsLaunch, "register split must balance");
     static constexpr int kPanels = D / 64;            // 64-element (128-byte) column panels
     static constexpr int kPanelBytes = 128 * 128;     // one panel of a 128-row tile
     static constexpr int kTileBytes = kPanels * kPanelBytes;  // 128 rows x D bf16
@@ -98,10 +110,12 @@ struct Ctl {
     uint64_t o_full;
     uint64_t drain;
     uint64_t csync[2];  // bounded barriers of warpgroup 0 / 1 (128 threads each)
+    uint64_t item_full[4], item_empty[4];  // ring of item ids from the producer to the other roles
     int4 meta[8];       // per stage: first logical key, valid keys, item, unused
     uint32_t tmem_base;
     int abort;
     int flag_last[2];
+    int ring[4];
     float dec_m[4][kDecRows];
     float dec_l[4][kDecRows];
     float dec_lr[4][kDecRows];
@@ -137,6 +151,30 @@ __device__ __forceinline__ bool compute_sync(const AttnParams& p, Ctl* ctl, int 
     return ok;
 }
 
+// Dynamic work queue.  The producer takes the next item id from a global
+// counter over the longest-first order and passes it to the other roles of
+// its CTA through a 4-deep shared ring (id -1 = no more work); every role
+// therefore walks the same item sequence.
+__device__ __forceinline__ int publish_item(const AttnParams& p, Ctl* ctl, uint32_t& n) {
+    const int slot = n & 3;
+    if (!wait_bar(p, ctl, &ctl->item_empty[slot], ((n >> 2) & 1) ^ 1, kErrTimeoutProducer)) return -2;
+    const int q = atomicAdd(&p.sched[0], 1);
+    const int id = q < p.n_items ? p.order[q] : -1;
+    ctl->ring[slot] = id;
+    ptx::mbar_arrive(&ctl->item_full[slot]);
+    ++n;
+    return id;
+}
+
+__device__ __forceinline__ int take_item(const AttnParams& p, Ctl* ctl, uint32_t& n, int code) {
+    const int slot = n & 3;
+    if (!wait_bar(p, ctl, &ctl->item_full[slot], (n >> 2) & 1, code)) return -2;
+    const int id = ctl->ring[slot];
+    ptx::mbar_arrive(&ctl->item_empty[slot]);
+    ++n;
+    return id;
+}
+
 // Byte offset of 16-byte chunk `c16` (0..D/8-1) of row `r` in a 128-row
 // tile stored as 128-byte-swizzled 64-column panels (the TMA SWIZZLE_128B
 // layout, which is also the tcgen05 canonical K-major layout).
@@ -149,13 +187,15 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c16) {
 // ------------------------------------------------------------ producer --
 
 template <int D, bool DEC>
-__device__ void producer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int i0, int i1, const CUtensorMap* tmK,
+__device__ void producer(const AttnParams& p, uint8_t* smem, Ctl* ctl, const CUtensorMap* tmK,
                          const CUtensorMap* tmK16, const CUtensorMap* tmV, const CUtensorMap* tmV16,
                          const CUtensorMap* tmQ) {
     using C = Cfg<D, DEC>;
-    uint32_t kv_cnt = 0, q_cnt = 0;
-    for (int ii = i0; ii < i1; ++ii) {
-        const Item it = p.items[p.cta_items[ii]];
+    uint32_t kv_cnt = 0, q_cnt = 0, n_taken = 0;
+    for (;;) {
+        const int ii = publish_item(p, ctl, n_taken);
+        if (ii < 0) break;
+        const Item it = p.items[ii];
         const Group g = p.groups[it.group];
         int kvh = g.head;
         if (!DEC && it.kind == kPrefill) {
@@ -246,7 +286,7 @@ drain:
 // ------------------------------------------------------------ MMA warp --
 
 template <int D, bool DEC>
-__device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int i0, int i1) {
+__device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
     using C = Cfg<D, DEC>;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, 128, 0, 0);  // Q K-major, K K-major
     constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, 0, 1);   // P (TMEM), V MN-major
@@ -254,10 +294,12 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int i0,
     const uint32_t sQ = ptx::smem_u32(smem + C::kOffQ);
     const uint32_t sK = ptx::smem_u32(smem + C::kOffK);
     const uint32_t sV = ptx::smem_u32(smem + C::kOffV);
-    uint32_t kv_cnt = 0, q_cnt = 0, pf[2] = {0u, 0u}, oc[2] = {0u, 0u};
+    uint32_t kv_cnt = 0, q_cnt = 0, pf[2] = {0u, 0u}, oc[2] = {0u, 0u}, n_taken = 0;
 
-    for (int ii = i0; ii < i1; ++ii) {
-        const Item it = p.items[p.cta_items[ii]];
+    for (;;) {
+        const int ii = take_item(p, ctl, n_taken, kErrTimeoutMma);
+        if (ii < 0) return;
+        const Item it = p.items[ii];
         const int T = it.pad;  // KV tiles of this item
         if (it.kind != kPrefill) { kv_cnt += T; continue; }
         const Group g = p.groups[it.group];
@@ -274,7 +316,7 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int i0,
             for (int k = 0; k < nh; ++k) {
                 // O_k += P_k V for tile j-1: P_k read from TMEM columns of S_k;
                 // rows that see fewer than 128 keys add a second pass with the
-                // bf16 residual of P, stored 64 columns further
+                // bf16 residual of P (interleaved per 16-key step)
                 if (j >= 1) {
                     if (!wait_bar(p, ctl, &ctl->p_full[k], pf[k] & 1, kErrTimeoutMma)) return;
                     ++pf[k];
@@ -291,8 +333,9 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int i0,
                     for (int pass = 0; pass < (precise ? 2 : 1); ++pass)
                         for (int ks = 0; ks < nk; ++ks) {
                             const uint64_t bd = ptx::smem_desc(vbase + ks * 16 * 128, C::kPanelBytes, 1024, 2);
-                            ptx::tc_mma_ts(tbase + C::kTmemO + k * D, tbase + k * 128 + pass * 64 + ks * 8, bd,
-                                           kIdescPV, (jj > 0 || ks > 0 || pass > 0) ? 1u : 0u);
+                            const uint32_t pcol = precise ? ks * 16 + pass * 8 : ks * 8;  // see prefill_item
+                            ptx::tc_mma_ts(tbase + C::kTmemO + k * D, tbase + k * 128 + pcol, bd, kIdescPV,
+                                           (jj > 0 || ks > 0 || pass > 0) ? 1u : 0u);
                         }
                     ptx::tc_commit(&ctl->p_empty[k]);
                 }
@@ -613,49 +656,6 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
 
 // ----------------------------------------------------- prefill (compute) --
 
-// Probabilities of one S row for rows that see fewer than 128 keys: P as
-// bf16 pairs into columns 0..63 of the S buffer and the bf16 residual
-// p - bf16(p) into columns 64..127, for a second PV pass (one rounding of a
-// few large probabilities would otherwise not average away).  Half 0's
-// residual is held in registers until half 1's scores have been read.
-// Returns (sum of p, sum of what the two PV passes consume).  Kept out of
-// line: it is rare, and its registers must not crowd the common path.
-__device__ __noinline__ float2 precise_probs(uint32_t tS, int lim, float m, float sl) {
-    float sum = 0.f, sumr = 0.f;
-    uint32_t lo0[32];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        float s[64];
-        ptx::tmem_ld64(tS + 64 * h, s);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-            s[c] = 64 * h + c < lim ? ptx::ex2(fmaf(s[c], sl, -m)) : 0.f;
-            sum += s[c];
-        }
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            pk[i] = ptx::pack_bf16x2(s[2 * i], s[2 * i + 1]);
-            sumr += bf16x2_sum(pk[i]);
-        }
-        ptx::tmem_st32(tS + 32 * h, reinterpret_cast<const float*>(pk));
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float a = s[2 * i], b = s[2 * i + 1];
-            const uint32_t hi = pk[i];
-            const uint32_t lo = ptx::pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
-            sumr += bf16x2_sum(lo);
-            if (h == 0) lo0[i] = lo; else pk[i] = lo;
-        }
-        if (h == 1) {
-            ptx::tmem_st32(tS + 64, reinterpret_cast<const float*>(lo0));
-            ptx::tmem_st32(tS + 96, reinterpret_cast<const float*>(pk));
-        }
-    }
-    ptx::tmem_wait_st();
-    return make_float2(sum, sumr);
-}
-
 // Softmax and epilogue of Q tile `k` (warpgroup k) of a prefill item.
 // Thread = tile row = TMEM lane.
 template <int D, bool DEC>
@@ -674,10 +674,11 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
     const uint32_t tO = tlane + C::kTmemO + k * D;  // O_k
     const int T = it.pad;
     const float sl = p.scale_log2;
-    // l: sum of the fp32 probabilities (gives lse); lr: sum of the values the
-    // PV MMA actually consumes (bf16-rounded, plus the residual pass where
-    // there is one), the normaliser of the output
-    float m = -INFINITY, l = 0.f, lr = 0.f;
+    // l: sum of the fp32 probabilities: the normaliser of the output and the
+    // lse.  P reaches the PV MMA rounded to bf16; rows with fewer than 128
+    // keys add the bf16 residual, so the MMA sees p to ~2^-17 where single
+    // roundings would not average away.
+    float m = -INFINITY, l = 0.f;
 
     for (int j = 0; j < T; ++j) {
         const uint32_t kj = kv_cnt + j;
@@ -694,21 +695,26 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
         // with the residual p - bf16(p)
         const bool precise = kt0 < kTileKeys && pmin < kTileKeys;
         const int lim = max(0, min(n, prow - kt0 + 1));  // visible columns of this row
-        // row max, over two 64-column halves of S (eight independent chains)
+        float s[128];
+        ptx::tmem_ld128(tS, s);
+        if (!__all_sync(0xffffffffu, lim >= kTileKeys)) {
+            // some row of the warp does not see the whole tile: mask in place
+            // (a select, so garbage past the valid keys cannot leak through)
+#pragma unroll
+            for (int c = 0; c < 128; ++c) s[c] = c < lim ? s[c] : -INFINITY;
+        }
         float mx;
         {
-            float m8[8];
+            // row max: four independent chains of 3-input max, then a tree
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float s[64];
-                ptx::tmem_ld64(tS + 64 * h, s);
-#pragma unroll
-                for (int c = 0; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], 64 * h + c < lim ? s[c] : -INFINITY);
+            for (int c = 0; c < 128; c += 8) {
+                m4[0] = ptx::fmax3(m4[0], s[c], s[c + 1]);
+                m4[1] = ptx::fmax3(m4[1], s[c + 2], s[c + 3]);
+                m4[2] = ptx::fmax3(m4[2], s[c + 4], s[c + 5]);
+                m4[3] = ptx::fmax3(m4[3], s[c + 6], s[c + 7]);
             }
-            mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         }
         float alpha = 1.f;
         bool resc = false;
@@ -737,37 +743,43 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
             }
             ptx::tmem_wait_st();
         }
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-        float sr4[4] = {0.f, 0.f, 0.f, 0.f};
-        if (!precise) {
-            // probabilities of each half, packed as bf16 pairs into the first
-            // 64 columns of S_k (half h's P overwrites columns already read)
+        // Probabilities p = 2^(s*scale*log2e - m) on f32x2 pairs (masked
+        // scores are -inf and give 0), summed in two packed accumulators.
+        // Common case: P as bf16 pairs, keys 2i and 2i+1 in column i
+        // (columns 0..63).  Rows that see fewer than 128 keys ("precise"): per
+        // 16-key step, 8 columns of P followed by 8 columns of the bf16
+        // residual p - bf16(p), for a second PV pass.
+        const uint64_t sl2 = ptx::f2pack(sl, sl);
+        const float nm = m == -INFINITY ? 0.f : -m;
+        const uint64_t nm2 = ptx::f2pack(nm, nm);
+        uint64_t acc2[2] = {0ull, 0ull};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float s[64];
-                ptx::tmem_ld64(tS + 64 * h, s);
-                uint32_t pk[32];
+        for (int ks = 0; ks < 8; ++ks) {  // 16-key steps
+            uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = 64 * h + 2 * i;
-                    const float a = c < lim ? ptx::ex2(fmaf(s[2 * i], sl, -m)) : 0.f;
-                    const float b = c + 1 < lim ? ptx::ex2(fmaf(s[2 * i + 1], sl, -m)) : 0.f;
-                    sum4[(2 * i) & 3] += a;
-                    sum4[(2 * i + 1) & 3] += b;
-                    pk[i] = ptx::pack_bf16x2(a, b);
-                    sr4[i & 3] += bf16x2_sum(pk[i]);
-                }
-                ptx::tmem_st32(tS + 32 * h, reinterpret_cast<const float*>(pk));
+            for (int i = 0; i < 8; ++i) {
+                const int col = 16 * ks + 2 * i;
+                float a, b;
+                ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[col], s[col + 1]), sl2, nm2), a, b);
+                a = ptx::ex2(a);
+                b = ptx::ex2(b);
+                acc2[i & 1] = ptx::fadd2(acc2[i & 1], ptx::f2pack(a, b));
+                pk[i] = ptx::pack_bf16x2(a, b);
+                if (precise)
+                    pk[8 + i] = ptx::pack_bf16x2(a - __uint_as_float(pk[i] << 16),
+                                                 b - __uint_as_float(pk[i] & 0xffff0000u));
             }
-        } else {
-            const float2 r = precise_probs(tS, lim, m, sl);
-            sum4[0] += r.x;
-            sr4[0] += r.y;
+            if (!precise) ptx::tmem_st8(tS + 8 * ks, pk);  // P
+            else ptx::tmem_st16(tS + 16 * ks, pk);         // P, then its residual
         }
-        const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-        const float sumr = (sr4[0] + sr4[1]) + (sr4[2] + sr4[3]);
+        float sum;
+        {
+            float a0, a1, b0, b1;
+            ptx::f2unpack(acc2[0], a0, a1);
+            ptx::f2unpack(acc2[1], b0, b1);
+            sum = (a0 + a1) + (b0 + b1);
+        }
         l = l * alpha + sum;
-        lr = lr * alpha + sumr;
         if (k == 0 && (n & (kBlock - 1))) {
             // The tile ends inside a block: rows [n, ceil16(n)) of the V stage
             // may be pool rows past L_s holding anything.  The PV MMA covers
@@ -795,7 +807,7 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
     if (!wait_bar(p, ctl, &ctl->o_full, ok_cnt & 1, kErrTimeoutCompute)) return false;
     ++ok_cnt;
     ptx::tc_fence_after();
-    const float inv = lr > 0.f ? 1.f / lr : 0.f;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
     const float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
     const bool split = g.n_parts > 1;
     const int64_t slot0 = split ? ((int64_t)(g.slot + it.part) * 2 + k) * kTileRows : 0;
@@ -884,12 +896,15 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
 }
 
 template <int D, bool DEC>
-__device__ void compute(const AttnParams& p, uint8_t* smem, Ctl* ctl, int i0, int i1, int warp, int lane) {
-    const int wg = (warp - 2) >> 2;  // warpgroup 0 or 1
-    const int cw = (warp - 2) & 3;
-    uint32_t kv_cnt = 0, sk = 0, pvk = 0, ok_cnt = 0, cs = 0;
-    for (int ii = i0; ii < i1; ++ii) {
-        const Item it = p.items[p.cta_items[ii]];
+__device__ void compute(const AttnParams& p, uint8_t* smem, Ctl* ctl, int warp, int lane) {
+    using C = Cfg<D, DEC>;
+    const int wg = (warp - C::kFirstCompute) >> 2;  // softmax warpgroup 0 or 1
+    const int cw = (warp - C::kFirstCompute) & 3;
+    uint32_t kv_cnt = 0, sk = 0, pvk = 0, ok_cnt = 0, cs = 0, n_taken = 0;
+    for (;;) {
+        const int ii = take_item(p, ctl, n_taken, kErrTimeoutCompute);
+        if (ii < 0) return;
+        const Item it = p.items[ii];
         const Group g = p.groups[it.group];
         bool ok = true;
         if (DEC || it.kind == kDecode) {
@@ -937,6 +952,11 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
         }
         ptx::mbar_init(&ctl->o_full, 1);
         ptx::mbar_init(&ctl->drain, 1);
+        for (int r = 0; r < 4; ++r) {
+            ptx::mbar_init(&ctl->item_full[r], 1);
+            // consumers of every item id: the compute threads, plus the MMA thread
+            ptx::mbar_init(&ctl->item_empty[r], (C::kWarps - C::kFirstCompute) * 32 + (DEC ? 0 : 1));
+        }
         ctl->abort = 0;
         ctl->flag_last[0] = ctl->flag_last[1] = 0;
         ptx::fence_mbar_init();
@@ -955,29 +975,43 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-
-    const int i0 = p.cta_indptr[blockIdx.x], i1 = p.cta_indptr[blockIdx.x + 1];
-    if (warp == 0) {
-        if (lane == 0) producer<D, DEC>(p, smem, ctl, i0, i1, &tmK, &tmK16, &tmV, &tmV16, &tmQ);
-    } else if (warp == 1) {
-        if constexpr (!DEC) {
-            if (lane == 0 && p.has_prefill) {
-                mma_issuer<D, DEC>(p, smem, ctl, i0, i1);
-                // every MMA issued must have completed before TMEM is released
-                ptx::tc_commit(&ctl->drain);
-                static __shared__ int never;
-                never = 0;
-                ptx::mbar_wait(&ctl->drain, 0, &never, 100000000ull);
+    // Each role sits inside the branch that sets its register budget.
+    if (warp < C::kFirstCompute) {
+        if constexpr (!DEC) ptx::setmaxnreg_dec<C::kRegsLow>();
+        if (warp == 0) {
+            if (lane == 0) producer<D, DEC>(p, smem, ctl, &tmK, &tmK16, &tmV, &tmV16, &tmQ);
+        } else if (warp == 1) {
+            if constexpr (!DEC) {
+                if (lane == 0 && p.has_prefill) {
+                    mma_issuer<D, DEC>(p, smem, ctl);
+                    // every MMA issued must have completed before TMEM is released
+                    ptx::tc_commit(&ctl->drain);
+                    static __shared__ int never;
+                    never = 0;
+                    ptx::mbar_wait(&ctl->drain, 0, &never, 100000000ull);
+                }
             }
         }
     } else {
-        compute<D, DEC>(p, smem, ctl, i0, i1, warp, lane);
+        if constexpr (!DEC) ptx::setmaxnreg_inc<C::kRegsHigh>();
+        compute<D, DEC>(p, smem, ctl, warp, lane);
     }
     __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     if (!DEC && warp == 1 && p.has_prefill) ptx::tmem_dealloc(ctl->tmem_base, C::kTmemCols);
+    if (threadIdx.x == 0) {
+        // every CTA has stopped taking items once its producer saw the end of
+        // the queue; the last CTA to finish leaves the queue reset for the
+        // next launch with this workspace
+        __threadfence();
+        if (atomicAdd(&p.sched[1], 1) == (int)gridDim.x - 1) {
+            p.sched[0] = 0;
+            p.sched[1] = 0;
+            __threadfence();
+        }
+    }
 }
 
 // ------------------------------------------------------------ host side --
@@ -1021,6 +1055,18 @@ static int launch_d(const msa_plan_s* P, const AttnParams& prm, const CUtensorMa
         if (cudaFuncSetAttribute(msa_attention_kernel<D, DEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmem) != cudaSuccess)
             return MSA_ERR_CUDA;
+        if (!DEC) {
+            // The register split only balances if the kernel launches with
+            // exactly kRegsLaunch registers per thread; otherwise a growing
+            // warpgroup would wait for registers that never come.  Refuse.
+            cudaFuncAttributes fa;
+            if (cudaFuncGetAttributes(&fa, msa_attention_kernel<D, DEC>) != cudaSuccess ||
+                fa.numRegs != C::kRegsLaunch) {
+                fprintf(stderr, "libmsa: attention kernel has %d registers per thread, expected %d\n", fa.numRegs,
+                        C::kRegsLaunch);
+                return MSA_ERR_CUDA;
+            }
+        }
         configured = true;
     }
     msa_attention_kernel<D, DEC>
@@ -1052,8 +1098,9 @@ int launch_attention_ws(const msa_plan_s* P, void* workspace, const void* q, con
     prm.groups = reinterpret_cast<const Group*>(ws + W.groups);
     prm.runs = reinterpret_cast<const Run*>(ws + W.runs);
     prm.pos = reinterpret_cast<const int32_t*>(ws + W.pos);
-    prm.cta_indptr = reinterpret_cast<const int32_t*>(ws + W.cta_indptr);
-    prm.cta_items = reinterpret_cast<const int32_t*>(ws + W.cta_items);
+    prm.order = reinterpret_cast<const int32_t*>(ws + W.order);
+    prm.sched = reinterpret_cast<int32_t*>(ws + W.sched);
+    prm.n_items = (int32_t)P->items.size();
     prm.counters = reinterpret_cast<int32_t*>(ws + W.counters);
     prm.error_word = reinterpret_cast<int32_t*>(ws + W.error);
     prm.dec_part = reinterpret_cast<float*>(ws + W.dec_part);

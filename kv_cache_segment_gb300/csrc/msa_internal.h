@@ -63,10 +63,10 @@ struct WsLayout {
     size_t groups;      // Group[n_groups]
     size_t runs;        // Run[n_runs]
     size_t pos;         // int32[n_q]: logical position of each packed row
-    size_t cta_indptr;  // int32[grid + 1]
-    size_t cta_items;   // int32[n_items]: item ids per CTA, in processing order
+    size_t order;       // int32[n_items]: item ids in processing order (longest first)
     size_t image_end;   // end of the part copied from the host image
     size_t counters;    // int32[2 * n_groups]: merge arrival counters per head slot (zeroed)
+    size_t sched;       // int32[2]: queue head, CTAs finished (zeroed; the last CTA resets them)
     size_t counters_end;
     size_t dec_part;    // float[n_dec_slots][kDecRows][D]
     size_t dec_lse;     // float[n_dec_slots][kDecRows]

@@ -25,8 +25,7 @@ struct msa_plan_s {
     std::vector<int32_t> pos;
     std::vector<msa::Group> groups;
     std::vector<msa::Item> items;
-    std::vector<int32_t> cta_indptr;
-    std::vector<int32_t> cta_items;
+    std::vector<int32_t> order;  // processing order of the items (longest first)
 
     msa::WsLayout lay{};
     std::vector<uint8_t> image;  // host copy of the workspace's int sections

@@ -2,7 +2,8 @@
 // query ranges, splits every sequence's live blocks into physically
 // contiguous segments (runs), forms output groups (GQA-packed decode rows or
 // 128-row prefill tiles per query head), splits long key ranges for SM
-// balance and assigns the work items to the CTAs of one persistent launch.
+// balance and orders the work items (longest first) for the dynamic queue of
+// one persistent launch.
 //
 // Segment rule (AsymCache explainer, "核心方法 1. Multi-Segment Attention"):
 // live blocks are regrouped by physical contiguity; an eviction hole, or any
@@ -19,7 +20,6 @@
 #include <cmath>
 #include <cstring>
 #include <new>
-#include <queue>
 #include <vector>
 
 #include "msa_internal.h"
@@ -234,27 +234,16 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
     // KV tiles of every item (the kernels walk exactly these)
     for (auto& it : P->items) it.pad = (int32_t)count_tiles(it.kb, it.ke);
 
-    // ---- LPT assignment of items to CTAs ------------------------------------
+    // ---- processing order --------------------------------------------------
+    // One global queue, longest first: every CTA of the persistent launch
+    // takes the next item when it is free (list scheduling in LPT order), so
+    // the load balances itself on the device.  Equal-cost items stay in
+    // generation order (sequence, tile, head), which keeps CTAs that run at
+    // the same time on the same sequences' K/V in L2.
     const int32_t n_items = (int32_t)P->items.size();
-    std::vector<int32_t> order(n_items);
-    for (int32_t i = 0; i < n_items; ++i) order[i] = i;
-    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
-    typedef std::pair<double, int32_t> Load;
-    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-    for (int32_t c = 0; c < P->grid; ++c) heap.push(Load(0.0, c));
-    std::vector<std::vector<int32_t>> per(P->grid);
-    for (int32_t i : order) {
-        Load l = heap.top();
-        heap.pop();
-        per[l.second].push_back(i);
-        l.first += cost[i];
-        heap.push(l);
-    }
-    P->cta_indptr.assign(1, 0);
-    for (int32_t c = 0; c < P->grid; ++c) {
-        for (int32_t i : per[c]) P->cta_items.push_back(i);
-        P->cta_indptr.push_back((int32_t)P->cta_items.size());
-    }
+    P->order.resize(n_items);
+    for (int32_t i = 0; i < n_items; ++i) P->order[i] = i;
+    std::stable_sort(P->order.begin(), P->order.end(), [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
 
     // ---- info ---------------------------------------------------------------
     msa_plan_info& I = P->info;
@@ -290,10 +279,10 @@ void build_image(msa_plan_s* P) {
     W.groups = sec(P->groups.size() * sizeof(Group));
     W.runs = sec(P->runs.size() * sizeof(Run));
     W.pos = sec(P->pos.size() * sizeof(int32_t));
-    W.cta_indptr = sec(P->cta_indptr.size() * sizeof(int32_t));
-    W.cta_items = sec(P->cta_items.size() * sizeof(int32_t));
+    W.order = sec(P->order.size() * sizeof(int32_t));
     W.image_end = o;
     W.counters = sec(2 * P->groups.size() * sizeof(int32_t));
+    W.sched = sec(2 * sizeof(int32_t));
     W.counters_end = o;
     W.dec_part = sec((size_t)P->n_dec_slots * kDecRows * D * sizeof(float));
     W.dec_lse = sec((size_t)P->n_dec_slots * kDecRows * sizeof(float));
@@ -309,8 +298,7 @@ void build_image(msa_plan_s* P) {
     put(W.groups, P->groups.data(), P->groups.size() * sizeof(Group));
     put(W.runs, P->runs.data(), P->runs.size() * sizeof(Run));
     put(W.pos, P->pos.data(), P->pos.size() * sizeof(int32_t));
-    put(W.cta_indptr, P->cta_indptr.data(), P->cta_indptr.size() * sizeof(int32_t));
-    put(W.cta_items, P->cta_items.data(), P->cta_items.size() * sizeof(int32_t));
+    put(W.order, P->order.data(), P->order.size() * sizeof(int32_t));
 }
 
 }  // namespace msa
