@@ -573,6 +573,8 @@ def profile_main(args):
         wl = W.batched_decode(seed=1002, pool_tokens=1 << 19)
     elif args.profile == "prefill":
         wl = W.config(3)
+    elif args.profile == "mixed":
+        wl = W.config(5)
     else:
         wl = W.long_context(seed=1004, num_seqs=1)
     case = Case(wl, dev)
@@ -597,7 +599,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only (no e2e, extras or CPU baseline)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--profile", choices=["decode", "prefill", "long"], default=None,
+    ap.add_argument("--profile", choices=["decode", "prefill", "mixed", "long"], default=None,
                     help="run a small case for an ncu capture and exit")
     args = ap.parse_args()
     if args.warmup < 3:
