@@ -77,6 +77,7 @@ struct Cfg {
     static constexpr int kWarps = DEC ? 6 : 12;
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kFirstCompute = DEC ? 2 : 4;  // first compute warp
+    static constexpr int kVWarp = DEC ? 1 : 2;          // the V-tile producer
     // Register split of the mixed launch (setmaxnreg): 384 threads launch with
     // 168 registers each (3 warps share an SM sub-partition's 16K registers);
     // warpgroup 0 gives back down to kRegsLow, the two softmax warpgroups grow
@@ -111,7 +112,8 @@ struct Ctl {
     uint64_t drain;
     uint64_t csync[2];  // bounded barriers of warpgroup 0 / 1 (128 threads each)
     uint64_t item_full[4], item_empty[4];  // ring of item ids from the producer to the other roles
-    int4 meta[8];       // per stage: first logical key, valid keys, item, unused
+    uint64_t meta_full[8];  // tile metadata ring (K producer -> readers), slot = tile % 8
+    int2 tmeta[8];          // per tile: first logical key, valid keys
     uint32_t tmem_base;
     int abort;
     int flag_last[2];
@@ -186,28 +188,39 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c16) {
 
 // ------------------------------------------------------------ producer --
 
-template <int D, bool DEC>
-__device__ void producer(const AttnParams& p, uint8_t* smem, Ctl* ctl, const CUtensorMap* tmK,
-                         const CUtensorMap* tmK16, const CUtensorMap* tmV, const CUtensorMap* tmV16,
-                         const CUtensorMap* tmQ) {
+// Two producer threads, one per ring: KSIDE (warp 0) takes items from the
+// queue and publishes them, loads the Q tiles of prefill items and the K
+// tiles, and records each tile's (first key, valid keys) in the metadata
+// ring; the V side (its own warp) follows the same items and loads the V
+// tiles.  The rings advance independently, so K for tile j+2 is fetched as
+// soon as the S MMAs of tile j have read K(j), long before PV(j) frees V(j).
+template <int D, bool DEC, bool KSIDE>
+__device__ void producer(const AttnParams& p, uint8_t* smem, Ctl* ctl, const CUtensorMap* tm128,
+                         const CUtensorMap* tm16, const CUtensorMap* tmQ) {
     using C = Cfg<D, DEC>;
+    uint64_t* full = KSIDE ? ctl->k_full : ctl->v_full;
+    uint64_t* empty = KSIDE ? ctl->k_empty : ctl->v_empty;
+    uint8_t* ring = smem + (KSIDE ? C::kOffK : C::kOffV);
+    const int code = kErrTimeoutProducer;
     uint32_t kv_cnt = 0, q_cnt = 0, n_taken = 0;
     for (;;) {
-        const int ii = publish_item(p, ctl, n_taken);
+        const int ii = KSIDE ? publish_item(p, ctl, n_taken) : take_item(p, ctl, n_taken, code);
         if (ii < 0) break;
         const Item it = p.items[ii];
         const Group g = p.groups[it.group];
         int kvh = g.head;
         if (!DEC && it.kind == kPrefill) {
             kvh = g.head / p.G;
-            const int nh = g.pad;  // query heads of the item: 1 or 2 (consecutive, same kv head)
-            if (!wait_bar(p, ctl, &ctl->q_empty, (q_cnt & 1) ^ 1, kErrTimeoutProducer)) goto drain;
-            ptx::mbar_arrive_expect_tx(&ctl->q_full, nh * C::kTileBytes);
-            for (int k = 0; k < nh; ++k)
-                for (int pn = 0; pn < C::kPanels; ++pn)
-                    ptx::tma_load_3d(smem + C::kOffQ + k * C::kTileBytes + pn * C::kPanelBytes, tmQ, pn * 64,
-                                     g.head + k, g.row0, &ctl->q_full);
-            ++q_cnt;
+            if (KSIDE) {
+                const int nh = g.pad;  // query heads of the item: 1 or 2 (consecutive, same kv head)
+                if (!wait_bar(p, ctl, &ctl->q_empty, (q_cnt & 1) ^ 1, code)) goto drain;
+                ptx::mbar_arrive_expect_tx(&ctl->q_full, nh * C::kTileBytes);
+                for (int k = 0; k < nh; ++k)
+                    for (int pn = 0; pn < C::kPanels; ++pn)
+                        ptx::tma_load_3d(smem + C::kOffQ + k * C::kTileBytes + pn * C::kPanelBytes, tmQ, pn * 64,
+                                         g.head + k, g.row0, &ctl->q_full);
+                ++q_cnt;
+            }
         }
         {
             // KV tiles are 128-key windows of the item's logical key range.  A
@@ -226,14 +239,13 @@ __device__ void producer(const AttnParams& p, uint8_t* smem, Ctl* ctl, const CUt
                 const int n = t1 - t0;
                 const int st = kv_cnt % C::kStages;
                 const uint32_t ph = (kv_cnt / C::kStages) & 1;
-                if (!wait_bar(p, ctl, &ctl->k_empty[st], ph ^ 1, kErrTimeoutProducer)) goto drain;
-                if (!wait_bar(p, ctl, &ctl->v_empty[st], ph ^ 1, kErrTimeoutProducer)) goto drain;
-                ctl->meta[st] = make_int4(t0, n, ii, 0);
-                uint8_t* ks = smem + C::kOffK + st * C::kTileBytes;
-                uint8_t* vs = smem + C::kOffV + st * C::kTileBytes;
-                const uint32_t bytes = (uint32_t)(((n + kBlock - 1) & ~(kBlock - 1)) * D * 2);
-                ptx::mbar_arrive_expect_tx(&ctl->k_full[st], bytes);
-                ptx::mbar_arrive_expect_tx(&ctl->v_full[st], bytes);
+                if (!wait_bar(p, ctl, &empty[st], ph ^ 1, code)) goto drain;
+                if (KSIDE) {
+                    ctl->tmeta[kv_cnt & 7] = make_int2(t0, n);
+                    ptx::mbar_arrive(&ctl->meta_full[kv_cnt & 7]);
+                }
+                uint8_t* dst = ring + st * C::kTileBytes;
+                ptx::mbar_arrive_expect_tx(&full[st], (uint32_t)(((n + kBlock - 1) & ~(kBlock - 1)) * D * 2));
                 int cur = t0;
                 while (cur < t1) {
                     if (r < 0 || r >= p.n_runs) {
@@ -247,18 +259,14 @@ __device__ void producer(const AttnParams& p, uint8_t* smem, Ctl* ctl, const CUt
                     const int phys = R.phys_row + (cur - R.log_start);
                     const int off = cur - t0;
                     if (off == 0 && pend - cur == kTileKeys) {
-                        for (int pn = 0; pn < C::kPanels; ++pn) {
-                            ptx::tma_load_3d(ks + pn * C::kPanelBytes, tmK, pn * 64, kvh, phys, &ctl->k_full[st]);
-                            ptx::tma_load_3d(vs + pn * C::kPanelBytes, tmV, pn * 64, kvh, phys, &ctl->v_full[st]);
-                        }
+                        for (int pn = 0; pn < C::kPanels; ++pn)
+                            ptx::tma_load_3d(dst + pn * C::kPanelBytes, tm128, pn * 64, kvh, phys, &full[st]);
                     } else {
                         const int nb = (pend - cur + kBlock - 1) / kBlock;
                         for (int b = 0; b < nb; ++b)
-                            for (int pn = 0; pn < C::kPanels; ++pn) {
-                                const int so = pn * C::kPanelBytes + (off + b * kBlock) * 128;
-                                ptx::tma_load_3d(ks + so, tmK16, pn * 64, kvh, phys + b * kBlock, &ctl->k_full[st]);
-                                ptx::tma_load_3d(vs + so, tmV16, pn * 64, kvh, phys + b * kBlock, &ctl->v_full[st]);
-                            }
+                            for (int pn = 0; pn < C::kPanels; ++pn)
+                                ptx::tma_load_3d(dst + pn * C::kPanelBytes + (off + b * kBlock) * 128, tm16, pn * 64,
+                                                 kvh, phys + b * kBlock, &full[st]);
                     }
                     cur = pend;
                 }
@@ -273,13 +281,9 @@ drain:
         static __shared__ int never;  // an abort flag nobody sets
         never = 0;
         const uint32_t tail = kv_cnt < (uint32_t)C::kStages ? kv_cnt : (uint32_t)C::kStages;
-        for (uint32_t k = kv_cnt - tail; k < kv_cnt; ++k) {
-            const int st = k % C::kStages;
-            const uint32_t ph = (k / C::kStages) & 1;
-            ptx::mbar_wait(&ctl->k_full[st], ph, &never, 100000000ull);
-            ptx::mbar_wait(&ctl->v_full[st], ph, &never, 100000000ull);
-        }
-        if (q_cnt > 0) ptx::mbar_wait(&ctl->q_full, (q_cnt - 1) & 1, &never, 100000000ull);
+        for (uint32_t k = kv_cnt - tail; k < kv_cnt; ++k)
+            ptx::mbar_wait(&full[k % C::kStages], (k / C::kStages) & 1, &never, 100000000ull);
+        if (KSIDE && q_cnt > 0) ptx::mbar_wait(&ctl->q_full, (q_cnt - 1) & 1, &never, 100000000ull);
     }
 }
 
@@ -307,12 +311,14 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
         const int pmin = p.pos[g.row0];  // rows ascend: the tile's smallest position
         if (!wait_bar(p, ctl, &ctl->q_full, q_cnt & 1, kErrTimeoutMma)) return;
         ++q_cnt;
+        int2 mt_prev = make_int2(0, 0);  // metadata of tile j-1, read when its S was issued
         for (int j = 0; j <= T; ++j) {
             const int jj = j - 1;
             const uint32_t kj = kv_cnt + j, kp = kv_cnt + jj;
             const int st = kj % C::kStages, stp = kp % C::kStages;
-            bool precise = false;
-            int nk = 0;
+            const bool precise = j >= 1 && mt_prev.x < kTileKeys && pmin < kTileKeys;
+            const int nk = (mt_prev.y + 15) >> 4;
+            int2 mt_cur = mt_prev;
             for (int k = 0; k < nh; ++k) {
                 // O_k += P_k V for tile j-1: P_k read from TMEM columns of S_k;
                 // rows that see fewer than 128 keys add a second pass with the
@@ -324,11 +330,6 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
                         return;
                     if (jj == 0 && !wait_bar(p, ctl, &ctl->o_empty[k], (oc[k] & 1) ^ 1, kErrTimeoutMma)) return;
                     ptx::tc_fence_after();
-                    if (k == 0) {
-                        const int4 mt = ctl->meta[stp];
-                        precise = mt.x < kTileKeys && pmin < kTileKeys;
-                        nk = (mt.y + 15) >> 4;
-                    }
                     const uint32_t vbase = sV + stp * C::kTileBytes;
                     for (int pass = 0; pass < (precise ? 2 : 1); ++pass)
                         for (int ks = 0; ks < nk; ++ks) {
@@ -341,8 +342,10 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
                 }
                 // S_k = Q_k K^T for tile j
                 if (j < T) {
-                    if (k == 0 && !wait_bar(p, ctl, &ctl->k_full[st], (kj / C::kStages) & 1, kErrTimeoutMma))
-                        return;
+                    if (k == 0) {
+                        if (!wait_bar(p, ctl, &ctl->k_full[st], (kj / C::kStages) & 1, kErrTimeoutMma)) return;
+                        mt_cur = ctl->tmeta[kj & 7];
+                    }
                     ptx::tc_fence_after();
                     const uint32_t kbase = sK + st * C::kTileBytes;
                     const uint32_t qbase = sQ + k * C::kTileBytes;
@@ -366,6 +369,7 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
                 ptx::tc_commit(&ctl->k_empty[st]);
                 if (j == T - 1) ptx::tc_commit(&ctl->q_empty);
             }
+            mt_prev = mt_cur;
         }
         kv_cnt += T;
     }
@@ -431,7 +435,7 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
         const uint32_t ph = (k / C::kStages) & 1;
         if (!wait_bar(p, ctl, &ctl->k_full[st], ph, kErrTimeoutCompute)) return false;
         if (!wait_bar(p, ctl, &ctl->v_full[st], ph, kErrTimeoutCompute)) return false;
-        const int4 mt = ctl->meta[st];
+        const int2 mt = ctl->tmeta[k & 7];
         const int kt0 = mt.x, n = mt.y;
         if (key0 < n) {
             const uint32_t kb = ptx::smem_u32(smem + C::kOffK + st * C::kTileBytes);
@@ -686,9 +690,9 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
         const uint32_t ph = (kj / C::kStages) & 1;
         if (!wait_bar(p, ctl, &ctl->s_full[k], sk & 1, kErrTimeoutCompute)) return false;
         ++sk;
-        if (!wait_bar(p, ctl, &ctl->k_full[st], ph, kErrTimeoutCompute)) return false;  // tile metadata
+        if (!wait_bar(p, ctl, &ctl->meta_full[kj & 7], (kj >> 3) & 1, kErrTimeoutCompute)) return false;
         ptx::tc_fence_after();
-        const int4 mt = ctl->meta[st];
+        const int2 mt = ctl->tmeta[kj & 7];
         const int kt0 = mt.x, n = mt.y;
         // rows that see fewer than 128 keys in total: a bf16 rounding of one
         // probability is not averaged away, so the PV MMA gets a second pass
@@ -954,9 +958,10 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
         ptx::mbar_init(&ctl->drain, 1);
         for (int r = 0; r < 4; ++r) {
             ptx::mbar_init(&ctl->item_full[r], 1);
-            // consumers of every item id: the compute threads, plus the MMA thread
-            ptx::mbar_init(&ctl->item_empty[r], (C::kWarps - C::kFirstCompute) * 32 + (DEC ? 0 : 1));
+            // consumers of every item id: the compute threads, the MMA thread, the V producer
+            ptx::mbar_init(&ctl->item_empty[r], (C::kWarps - C::kFirstCompute) * 32 + (DEC ? 0 : 1) + 1);
         }
+        for (int r = 0; r < 8; ++r) ptx::mbar_init(&ctl->meta_full[r], 1);
         ctl->abort = 0;
         ctl->flag_last[0] = ctl->flag_last[1] = 0;
         ptx::fence_mbar_init();
@@ -979,7 +984,9 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
     if (warp < C::kFirstCompute) {
         if constexpr (!DEC) ptx::setmaxnreg_dec<C::kRegsLow>();
         if (warp == 0) {
-            if (lane == 0) producer<D, DEC>(p, smem, ctl, &tmK, &tmK16, &tmV, &tmV16, &tmQ);
+            if (lane == 0) producer<D, DEC, true>(p, smem, ctl, &tmK, &tmK16, &tmQ);
+        } else if (warp == C::kVWarp) {
+            if (lane == 0) producer<D, DEC, false>(p, smem, ctl, &tmV, &tmV16, &tmQ);
         } else if (warp == 1) {
             if constexpr (!DEC) {
                 if (lane == 0 && p.has_prefill) {
