@@ -397,12 +397,30 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
     const int prow0 = gr < M ? p.pos[g.row0 + gr / G] : -1;
     const int prow1 = gr + 8 < M ? p.pos[g.row0 + (gr + 8) / G] : -1;
 
-    // Q (rows = query row x head, zero past M) staged in shared memory as
-    // [16][D] bf16 with 16-byte chunks XOR-swizzled by row, read back as MMA
-    // A fragments with ldmatrix (the merge scratch is free until the tiles
-    // are done)
+    // Q fragments (rows = query row x head, zero past M).  The decode-only
+    // kernel has the registers to hold all of them; the mixed kernel stages Q
+    // in shared memory as [16][D] bf16 (16-byte chunks XOR-swizzled by row)
+    // and reads fragments back with ldmatrix (the merge scratch is free until
+    // the tiles are done).
+    constexpr int KSR = DEC ? D / 16 : 1;
+    uint32_t qa_r[KSR][4];
     uint8_t* qs = smem + C::kOffScr;
-    {
+    if constexpr (DEC) {
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
+        auto qword = [&](int m, int dim) -> uint32_t {
+            if (m >= M) return 0u;
+            const int64_t row = g.row0 + m / G;
+            const int64_t h = (int64_t)kvh * G + m % G;
+            return qw[((row * p.Hq + h) * D + dim) >> 1];
+        };
+#pragma unroll
+        for (int ks = 0; ks < KSR; ++ks) {
+            qa_r[ks][0] = qword(gr, ks * 16 + 2 * tq);
+            qa_r[ks][1] = qword(gr + 8, ks * 16 + 2 * tq);
+            qa_r[ks][2] = qword(gr, ks * 16 + 8 + 2 * tq);
+            qa_r[ks][3] = qword(gr + 8, ks * 16 + 8 + 2 * tq);
+        }
+    } else {
         const int tid = cw * 32 + lane;
         const uint4* qg = reinterpret_cast<const uint4*>(p.q);
         for (int e = tid; e < kDecRows * (D / 8); e += 128) {
@@ -446,7 +464,13 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
 #pragma unroll
             for (int kk = 0; kk < D / 32; ++kk) {
                 uint32_t qa0[4], qa1[4];
-                {
+                if constexpr (DEC) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        qa0[i] = qa_r[(2 * kk) % KSR][i];
+                        qa1[i] = qa_r[(2 * kk + 1) % KSR][i];
+                    }
+                } else {
                     const int c0 = 4 * kk + (lane >> 4);  // chunk of k-step 2kk
                     ptx::ldmatrix_x4(qsa + qrow * (D * 2) + ((c0 ^ (qrow & 7)) << 4), qa0[0], qa0[1], qa0[2], qa0[3]);
                     const int c1 = c0 + 2;                 // k-step 2kk+1

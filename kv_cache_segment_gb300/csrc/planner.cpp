@@ -198,7 +198,10 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
     for (size_t gi = 0; gi < pend.size(); ++gi) {
         Pending& pd = pend[gi];
         const int32_t kind = pd.g.kind;
-        int64_t chunk = std::max<int64_t>(min_tiles[kind], (int64_t)std::ceil(per_cta / 16.0 / w_tile[kind]));
+        // decode items end with a cross-CTA merge (a fence and an atomic round
+        // trip), so they are cut coarser than prefill items
+        const double per_item = kind == kDecode ? per_cta / 6.0 : per_cta / 16.0;
+        int64_t chunk = std::max<int64_t>(min_tiles[kind], (int64_t)std::ceil(per_item / w_tile[kind]));
         int32_t parts = (int32_t)std::max<int64_t>(1, (pd.tiles + chunk - 1) / chunk);
         const int32_t s = pd.g.seq;
         const int32_t ra = P->run_indptr[s], rb = P->run_indptr[s + 1];
