@@ -81,10 +81,10 @@ struct Cfg {
     // Register split of the mixed launch (setmaxnreg): 384 threads launch with
     // 168 registers each (3 warps share an SM sub-partition's 16K registers);
     // warpgroup 0 gives back down to kRegsLow, the two softmax warpgroups grow
-    // to kRegsHigh.  128*72 + 256*216 = 384*168 exactly.
+    // to kRegsHigh.  128*88 + 256*208 = 384*168 exactly.
     static constexpr int kRegsLaunch = 168;
-    static constexpr int kRegsLow = 72;
-    static constexpr int kRegsHigh = 216;
+    static constexpr int kRegsLow = 88;
+    static constexpr int kRegsHigh = 208;
     static_assert(DEC || 128 * kRegsLow + 256 * kRegsHigh == kThreads * kRegsLaunch, "register split must balance");
     static constexpr int kPanels = D / 64;            // 64-element (128-byte) column panels
     static constexpr int kPanelBytes = 128 * 128;     // one panel of a 128-row tile
@@ -295,9 +295,18 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, 128, 0, 0);  // Q K-major, K K-major
     constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, 0, 1);   // P (TMEM), V MN-major
     const uint32_t tbase = ctl->tmem_base;
-    const uint32_t sQ = ptx::smem_u32(smem + C::kOffQ);
-    const uint32_t sK = ptx::smem_u32(smem + C::kOffK);
-    const uint32_t sV = ptx::smem_u32(smem + C::kOffV);
+    // Shared-memory descriptors: the high word (stride 1024 bytes, version,
+    // 128-byte swizzle) is common to every operand; the low words are built
+    // once and advanced by byte offsets >> 4 added to their 14-bit address
+    // field (every operand lies in this CTA's shared memory, < 256 KB, so
+    // the field never carries over).  A single issuing thread needs a short
+    // per-MMA instruction chain to keep up with the tensor pipe (64 cycles
+    // per 128x128x16 MMA).
+    const uint64_t dQ = ptx::smem_desc(ptx::smem_u32(smem + C::kOffQ), 16, 1024, 2);
+    const uint32_t hi = (uint32_t)(dQ >> 32);
+    const uint32_t lQ = (uint32_t)dQ;
+    const uint32_t lK = (uint32_t)ptx::smem_desc(ptx::smem_u32(smem + C::kOffK), 16, 1024, 2);
+    const uint32_t lV = (uint32_t)ptx::smem_desc(ptx::smem_u32(smem + C::kOffV), C::kPanelBytes, 1024, 2);
     uint32_t kv_cnt = 0, q_cnt = 0, pf[2] = {0u, 0u}, oc[2] = {0u, 0u}, n_taken = 0;
 
     for (;;) {
@@ -330,14 +339,22 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
                         return;
                     if (jj == 0 && !wait_bar(p, ctl, &ctl->o_empty[k], (oc[k] & 1) ^ 1, kErrTimeoutMma)) return;
                     ptx::tc_fence_after();
-                    const uint32_t vbase = sV + stp * C::kTileBytes;
-                    for (int pass = 0; pass < (precise ? 2 : 1); ++pass)
-                        for (int ks = 0; ks < nk; ++ks) {
-                            const uint64_t bd = ptx::smem_desc(vbase + ks * 16 * 128, C::kPanelBytes, 1024, 2);
-                            const uint32_t pcol = precise ? ks * 16 + pass * 8 : ks * 8;  // see prefill_item
-                            ptx::tc_mma_ts(tbase + C::kTmemO + k * D, tbase + k * 128 + pcol, bd, kIdescPV,
-                                           (jj > 0 || ks > 0 || pass > 0) ? 1u : 0u);
-                        }
+                    const uint32_t vl = lV + (uint32_t)((stp * C::kTileBytes) >> 4);
+                    const uint32_t to = tbase + C::kTmemO + k * D, tp = tbase + k * 128;
+                    // 16 keys per MMA: V rows ks*16.. start 16*128 bytes further
+                    if (!precise && nk == kTileKeys / 16) {
+                        ptx::tc_mma_ts_lo<-1>(to, tp, vl, hi, kIdescPV, jj > 0 ? 1u : 0u);
+#pragma unroll
+                        for (int ks = 1; ks < kTileKeys / 16; ++ks)
+                            ptx::tc_mma_ts_lo<1>(to, tp + ks * 8, vl + ks * 128, hi, kIdescPV);
+                    } else {
+                        for (int pass = 0; pass < (precise ? 2 : 1); ++pass)
+                            for (int ks = 0; ks < nk; ++ks) {
+                                const uint32_t pcol = precise ? ks * 16 + pass * 8 : ks * 8;  // see prefill_item
+                                ptx::tc_mma_ts_lo<-1>(to, tp + pcol, vl + ks * 128, hi, kIdescPV,
+                                                      (jj > 0 || ks > 0 || pass > 0) ? 1u : 0u);
+                            }
+                    }
                     ptx::tc_commit(&ctl->p_empty[k]);
                 }
                 // S_k = Q_k K^T for tile j
@@ -347,13 +364,16 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
                         mt_cur = ctl->tmeta[kj & 7];
                     }
                     ptx::tc_fence_after();
-                    const uint32_t kbase = sK + st * C::kTileBytes;
-                    const uint32_t qbase = sQ + k * C::kTileBytes;
+                    const uint32_t kl = lK + (uint32_t)((st * C::kTileBytes) >> 4);
+                    const uint32_t ql = lQ + (uint32_t)((k * C::kTileBytes) >> 4);
+                    const uint32_t ts = tbase + k * 128;
+                    // 16 dims per MMA: 32 bytes along a 128-byte swizzled row,
+                    // the next 64 dims in the next panel
+                    ptx::tc_mma_ss_lo<0>(ts, ql, kl, hi, kIdescS);
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * C::kPanelBytes + (ks & 3) * 32;
-                        ptx::tc_mma_ss(tbase + k * 128, ptx::smem_desc(qbase + off, 16, 1024, 2),
-                                       ptx::smem_desc(kbase + off, 16, 1024, 2), kIdescS, ks > 0);
+                    for (int ks = 1; ks < D / 16; ++ks) {
+                        const uint32_t off = (uint32_t)(((ks >> 2) * C::kPanelBytes + (ks & 3) * 32) >> 4);
+                        ptx::tc_mma_ss_lo<1>(ts, ql + off, kl + off, hi, kIdescS);
                     }
                     ptx::tc_commit(&ctl->s_full[k]);
                 }
@@ -773,32 +793,54 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
         }
         // Probabilities p = 2^(s*scale*log2e - m) on f32x2 pairs (masked
         // scores are -inf and give 0), summed in two packed accumulators.
-        // Common case: P as bf16 pairs, keys 2i and 2i+1 in column i
-        // (columns 0..63).  Rows that see fewer than 128 keys ("precise"): per
-        // 16-key step, 8 columns of P followed by 8 columns of the bf16
-        // residual p - bf16(p), for a second PV pass.
         const uint64_t sl2 = ptx::f2pack(sl, sl);
         const float nm = m == -INFINITY ? 0.f : -m;
         const uint64_t nm2 = ptx::f2pack(nm, nm);
         uint64_t acc2[2] = {0ull, 0ull};
+        if (!precise) {
+            // P as bf16 pairs, keys 2i and 2i+1 in column i (columns 0..63)
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {  // 16-key steps
-            uint32_t pk[16];
+            for (int ks = 0; ks < 8; ++ks) {  // 16-key steps
+                uint32_t pk[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int col = 16 * ks + 2 * i;
-                float a, b;
-                ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[col], s[col + 1]), sl2, nm2), a, b);
-                a = ptx::ex2(a);
-                b = ptx::ex2(b);
-                acc2[i & 1] = ptx::fadd2(acc2[i & 1], ptx::f2pack(a, b));
-                pk[i] = ptx::pack_bf16x2(a, b);
-                if (precise)
+                for (int i = 0; i < 8; ++i) {
+                    const int col = 16 * ks + 2 * i;
+                    float a, b;
+                    ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[col], s[col + 1]), sl2, nm2), a, b);
+                    a = ptx::ex2(a);
+                    b = ptx::ex2(b);
+                    acc2[i & 1] = ptx::fadd2(acc2[i & 1], ptx::f2pack(a, b));
+                    pk[i] = ptx::pack_bf16x2(a, b);
+                }
+                ptx::tmem_st8(tS + 8 * ks, pk);
+            }
+        } else {
+            // Rows that see fewer than 128 keys (the first key tile of rows
+            // near the start of a sequence): per 16-key step, 8 columns of P
+            // followed by 8 columns of the bf16 residual p - bf16(p), for a
+            // second PV pass.  Kept out of the hot loop above: a rolled loop
+            // that re-reads the 16 score columns it then overwrites.
+#pragma unroll 1
+            for (int ks = 0; ks < 8; ++ks) {
+                float v[16];
+                ptx::tmem_ld16(tS + 16 * ks, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int col = 16 * ks + 2 * i;
+                    const float s0 = col < lim ? v[2 * i] : -INFINITY;
+                    const float s1 = col + 1 < lim ? v[2 * i + 1] : -INFINITY;
+                    float a, b;
+                    ptx::f2unpack(ptx::ffma2(ptx::f2pack(s0, s1), sl2, nm2), a, b);
+                    a = ptx::ex2(a);
+                    b = ptx::ex2(b);
+                    acc2[i & 1] = ptx::fadd2(acc2[i & 1], ptx::f2pack(a, b));
+                    pk[i] = ptx::pack_bf16x2(a, b);
                     pk[8 + i] = ptx::pack_bf16x2(a - __uint_as_float(pk[i] << 16),
                                                  b - __uint_as_float(pk[i] & 0xffff0000u));
+                }
+                ptx::tmem_st16(tS + 16 * ks, pk);
             }
-            if (!precise) ptx::tmem_st8(tS + 8 * ks, pk);  // P
-            else ptx::tmem_st16(tS + 16 * ks, pk);         // P, then its residual
         }
         float sum;
         {
