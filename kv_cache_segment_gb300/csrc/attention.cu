@@ -177,6 +177,25 @@ __device__ __forceinline__ int take_item(const AttnParams& p, Ctl* ctl, uint32_t
     return id;
 }
 
+// Warp-wide forms for the MMA warp.  Every lane waits (each with acquire
+// semantics, so each may then read what the barrier guards) and the warp
+// votes, so it leaves converged with the same outcome everywhere.
+__device__ __forceinline__ bool wait_bar_w(const AttnParams& p, Ctl* ctl, uint64_t* bar, uint32_t parity, int code) {
+    const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, &ctl->abort, p.limit_ns));
+    if (!ok) fail(p, ctl, code);
+    return ok;
+}
+
+__device__ __forceinline__ int take_item_w(const AttnParams& p, Ctl* ctl, uint32_t& n, int code, int lane) {
+    const int slot = n & 3;
+    if (!wait_bar_w(p, ctl, &ctl->item_full[slot], (n >> 2) & 1, code)) return -2;
+    const int id = ctl->ring[slot];
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&ctl->item_empty[slot]);  // one arrival per role
+    ++n;
+    return id;
+}
+
 // Byte offset of 16-byte chunk `c16` (0..D/8-1) of row `r` in a 128-row
 // tile stored as 128-byte-swizzled 64-column panels (the TMA SWIZZLE_128B
 // layout, which is also the tcgen05 canonical K-major layout).
@@ -289,8 +308,10 @@ drain:
 
 // ------------------------------------------------------------ MMA warp --
 
+// The whole MMA warp runs this loop; elect.sync inside the MMA and commit
+// instructions lets one lane issue.
 template <int D, bool DEC>
-__device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
+__device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lane) {
     using C = Cfg<D, DEC>;
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, 128, 0, 0);  // Q K-major, K K-major
     constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, 0, 1);   // P (TMEM), V MN-major
@@ -310,7 +331,7 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
     uint32_t kv_cnt = 0, q_cnt = 0, pf[2] = {0u, 0u}, oc[2] = {0u, 0u}, n_taken = 0;
 
     for (;;) {
-        const int ii = take_item(p, ctl, n_taken, kErrTimeoutMma);
+        const int ii = take_item_w(p, ctl, n_taken, kErrTimeoutMma, lane);
         if (ii < 0) return;
         const Item it = p.items[ii];
         const int T = it.pad;  // KV tiles of this item
@@ -318,7 +339,7 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
         const Group g = p.groups[it.group];
         const int nh = g.pad;
         const int pmin = p.pos[g.row0];  // rows ascend: the tile's smallest position
-        if (!wait_bar(p, ctl, &ctl->q_full, q_cnt & 1, kErrTimeoutMma)) return;
+        if (!wait_bar_w(p, ctl, &ctl->q_full, q_cnt & 1, kErrTimeoutMma)) return;
         ++q_cnt;
         int2 mt_prev = make_int2(0, 0);  // metadata of tile j-1, read when its S was issued
         for (int j = 0; j <= T; ++j) {
@@ -333,34 +354,34 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
                 // rows that see fewer than 128 keys add a second pass with the
                 // bf16 residual of P (interleaved per 16-key step)
                 if (j >= 1) {
-                    if (!wait_bar(p, ctl, &ctl->p_full[k], pf[k] & 1, kErrTimeoutMma)) return;
+                    if (!wait_bar_w(p, ctl, &ctl->p_full[k], pf[k] & 1, kErrTimeoutMma)) return;
                     ++pf[k];
-                    if (k == 0 && !wait_bar(p, ctl, &ctl->v_full[stp], (kp / C::kStages) & 1, kErrTimeoutMma))
+                    if (k == 0 && !wait_bar_w(p, ctl, &ctl->v_full[stp], (kp / C::kStages) & 1, kErrTimeoutMma))
                         return;
-                    if (jj == 0 && !wait_bar(p, ctl, &ctl->o_empty[k], (oc[k] & 1) ^ 1, kErrTimeoutMma)) return;
+                    if (jj == 0 && !wait_bar_w(p, ctl, &ctl->o_empty[k], (oc[k] & 1) ^ 1, kErrTimeoutMma)) return;
                     ptx::tc_fence_after();
                     const uint32_t vl = lV + (uint32_t)((stp * C::kTileBytes) >> 4);
                     const uint32_t to = tbase + C::kTmemO + k * D, tp = tbase + k * 128;
                     // 16 keys per MMA: V rows ks*16.. start 16*128 bytes further
                     if (!precise && nk == kTileKeys / 16) {
-                        ptx::tc_mma_ts_lo<-1>(to, tp, vl, hi, kIdescPV, jj > 0 ? 1u : 0u);
+                        ptx::tc_mma_ts_e<-1>(to, tp, vl, hi, kIdescPV, jj > 0 ? 1u : 0u);
 #pragma unroll
                         for (int ks = 1; ks < kTileKeys / 16; ++ks)
-                            ptx::tc_mma_ts_lo<1>(to, tp + ks * 8, vl + ks * 128, hi, kIdescPV);
+                            ptx::tc_mma_ts_e<1>(to, tp + ks * 8, vl + ks * 128, hi, kIdescPV);
                     } else {
                         for (int pass = 0; pass < (precise ? 2 : 1); ++pass)
                             for (int ks = 0; ks < nk; ++ks) {
                                 const uint32_t pcol = precise ? ks * 16 + pass * 8 : ks * 8;  // see prefill_item
-                                ptx::tc_mma_ts_lo<-1>(to, tp + pcol, vl + ks * 128, hi, kIdescPV,
+                                ptx::tc_mma_ts_e<-1>(to, tp + pcol, vl + ks * 128, hi, kIdescPV,
                                                       (jj > 0 || ks > 0 || pass > 0) ? 1u : 0u);
                             }
                     }
-                    ptx::tc_commit(&ctl->p_empty[k]);
+                    ptx::tc_commit_e(&ctl->p_empty[k]);
                 }
                 // S_k = Q_k K^T for tile j
                 if (j < T) {
                     if (k == 0) {
-                        if (!wait_bar(p, ctl, &ctl->k_full[st], (kj / C::kStages) & 1, kErrTimeoutMma)) return;
+                        if (!wait_bar_w(p, ctl, &ctl->k_full[st], (kj / C::kStages) & 1, kErrTimeoutMma)) return;
                         mt_cur = ctl->tmeta[kj & 7];
                     }
                     ptx::tc_fence_after();
@@ -369,25 +390,25 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl) {
                     const uint32_t ts = tbase + k * 128;
                     // 16 dims per MMA: 32 bytes along a 128-byte swizzled row,
                     // the next 64 dims in the next panel
-                    ptx::tc_mma_ss_lo<0>(ts, ql, kl, hi, kIdescS);
+                    ptx::tc_mma_ss_e<0>(ts, ql, kl, hi, kIdescS);
 #pragma unroll
                     for (int ks = 1; ks < D / 16; ++ks) {
                         const uint32_t off = (uint32_t)(((ks >> 2) * C::kPanelBytes + (ks & 3) * 32) >> 4);
-                        ptx::tc_mma_ss_lo<1>(ts, ql + off, kl + off, hi, kIdescS);
+                        ptx::tc_mma_ss_e<1>(ts, ql + off, kl + off, hi, kIdescS);
                     }
-                    ptx::tc_commit(&ctl->s_full[k]);
+                    ptx::tc_commit_e(&ctl->s_full[k]);
                 }
             }
             if (j >= 1) {
-                ptx::tc_commit(&ctl->v_empty[stp]);
+                ptx::tc_commit_e(&ctl->v_empty[stp]);
                 if (jj == T - 1) {
-                    ptx::tc_commit(&ctl->o_full);
+                    ptx::tc_commit_e(&ctl->o_full);
                     for (int k = 0; k < nh; ++k) ++oc[k];
                 }
             }
             if (j < T) {
-                ptx::tc_commit(&ctl->k_empty[st]);
-                if (j == T - 1) ptx::tc_commit(&ctl->q_empty);
+                ptx::tc_commit_e(&ctl->k_empty[st]);
+                if (j == T - 1) ptx::tc_commit_e(&ctl->q_empty);
             }
             mt_prev = mt_cur;
         }
@@ -1055,13 +1076,16 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
             if (lane == 0) producer<D, DEC, false>(p, smem, ctl, &tmV, &tmV16, &tmQ);
         } else if (warp == 1) {
             if constexpr (!DEC) {
-                if (lane == 0 && p.has_prefill) {
-                    mma_issuer<D, DEC>(p, smem, ctl);
-                    // every MMA issued must have completed before TMEM is released
-                    ptx::tc_commit(&ctl->drain);
-                    static __shared__ int never;
-                    never = 0;
-                    ptx::mbar_wait(&ctl->drain, 0, &never, 100000000ull);
+                if (p.has_prefill) {
+                    mma_issuer<D, DEC>(p, smem, ctl, lane);
+                    __syncwarp();
+                    if (lane == 0) {
+                        // every MMA lane 0 issued must have completed before TMEM is released
+                        ptx::tc_commit(&ctl->drain);
+                        static __shared__ int never;
+                        never = 0;
+                        ptx::mbar_wait(&ctl->drain, 0, &never, 100000000ull);
+                    }
                 }
             }
         }

@@ -265,6 +265,42 @@ __device__ __forceinline__ void tc_mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, u
         : "memory");
 }
 
+// Warp-wide issue: the whole (converged) warp executes these and the lane
+// chosen by elect.sync (the lowest active one, lane 0 of a full warp) issues.
+// Issuing this way costs the warp about 43 cycles per MMA and 17 per commit,
+// against about 53 and 55 from a single diverged thread, which matters when
+// each MMA keeps the tensor pipe busy for only 64 cycles.
+template <int ACC>
+__device__ __forceinline__ void tc_mma_ss_e(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                            uint32_t idesc, uint32_t acc = 0) {
+    const uint32_t en = ACC < 0 ? acc : (uint32_t)ACC;
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(en)
+        : "memory");
+}
+
+template <int ACC>
+__device__ __forceinline__ void tc_mma_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                            uint32_t idesc, uint32_t acc = 0) {
+    const uint32_t en = ACC < 0 ? acc : (uint32_t)ACC;
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 db;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 db, {%2, %3};\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(en)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_e(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
+
 // Arrive on `bar` once all tcgen05 operations issued so far by this thread complete.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
