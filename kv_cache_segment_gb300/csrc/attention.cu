@@ -29,6 +29,7 @@
 // Each softmax warpgroup has the other's PV + S (about 1024 tensor cycles) to
 // produce its P before the tensor core needs it.
 #include <cuda.h>
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -572,53 +573,59 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
                 }
             }
             const bool tail = key0 + 32 > n;
+            // O += P V over this warp's 32 keys (two 16-key MMA steps).  Keys
+            // below 128: rows may see few keys, so the bf16 residual of P goes
+            // through a second MMA (see prefill_item).  Two instantiations
+            // keep that rare path out of the common loop.
+            auto pv = [&](auto precise_tag) {
+                constexpr bool kPrecise = decltype(precise_tag)::value;
 #pragma unroll
-            for (int kst = 0; kst < 2; ++kst) {
-                uint32_t a[4];
-                a[0] = ptx::pack_bf16x2(s[2 * kst][0], s[2 * kst][1]);
-                a[1] = ptx::pack_bf16x2(s[2 * kst][2], s[2 * kst][3]);
-                a[2] = ptx::pack_bf16x2(s[2 * kst + 1][0], s[2 * kst + 1][1]);
-                a[3] = ptx::pack_bf16x2(s[2 * kst + 1][2], s[2 * kst + 1][3]);
-                const int kbase = key0 + kst * 16;
-                if (kbase >= n) break;
-                rrun0 += bf16x2_sum(a[0]) + bf16x2_sum(a[2]);
-                rrun1 += bf16x2_sum(a[1]) + bf16x2_sum(a[3]);
-                // keys below 128: rows may see few keys, add the bf16 residual
-                // of P as a second MMA (see prefill_item)
-                const bool precise = kt0 < kTileKeys;
-                uint32_t alo[4] = {0u, 0u, 0u, 0u};
-                if (precise) {
-                    alo[0] = ptx::pack_bf16x2(s[2 * kst][0] - __uint_as_float(a[0] << 16),
-                                              s[2 * kst][1] - __uint_as_float(a[0] & 0xffff0000u));
-                    alo[1] = ptx::pack_bf16x2(s[2 * kst][2] - __uint_as_float(a[1] << 16),
-                                              s[2 * kst][3] - __uint_as_float(a[1] & 0xffff0000u));
-                    alo[2] = ptx::pack_bf16x2(s[2 * kst + 1][0] - __uint_as_float(a[2] << 16),
-                                              s[2 * kst + 1][1] - __uint_as_float(a[2] & 0xffff0000u));
-                    alo[3] = ptx::pack_bf16x2(s[2 * kst + 1][2] - __uint_as_float(a[3] << 16),
-                                              s[2 * kst + 1][3] - __uint_as_float(a[3] & 0xffff0000u));
-                    rrun0 += bf16x2_sum(alo[0]) + bf16x2_sum(alo[2]);
-                    rrun1 += bf16x2_sum(alo[1]) + bf16x2_sum(alo[3]);
-                }
-                // V rows past the valid keys may hold anything (even NaN): zero them
-                uint32_t m0 = 0xffffffffu, m1 = 0xffffffffu;
-                if (tail) {
-                    const int k0 = kbase + 2 * tq;
-                    m0 = (k0 < n ? 0x0000ffffu : 0u) | (k0 + 1 < n ? 0xffff0000u : 0u);
-                    m1 = (k0 + 8 < n ? 0x0000ffffu : 0u) | (k0 + 9 < n ? 0xffff0000u : 0u);
-                }
-                const int vkey = kbase + (lane & 7) + ((lane >> 3) & 1) * 8;
+                for (int kst = 0; kst < 2; ++kst) {
+                    uint32_t a[4];
+                    a[0] = ptx::pack_bf16x2(s[2 * kst][0], s[2 * kst][1]);
+                    a[1] = ptx::pack_bf16x2(s[2 * kst][2], s[2 * kst][3]);
+                    a[2] = ptx::pack_bf16x2(s[2 * kst + 1][0], s[2 * kst + 1][1]);
+                    a[3] = ptx::pack_bf16x2(s[2 * kst + 1][2], s[2 * kst + 1][3]);
+                    const int kbase = key0 + kst * 16;
+                    if (kbase >= n) break;
+                    rrun0 += bf16x2_sum(a[0]) + bf16x2_sum(a[2]);
+                    rrun1 += bf16x2_sum(a[1]) + bf16x2_sum(a[3]);
+                    uint32_t alo[4] = {0u, 0u, 0u, 0u};
+                    if constexpr (kPrecise) {
+                        alo[0] = ptx::pack_bf16x2(s[2 * kst][0] - __uint_as_float(a[0] << 16),
+                                                  s[2 * kst][1] - __uint_as_float(a[0] & 0xffff0000u));
+                        alo[1] = ptx::pack_bf16x2(s[2 * kst][2] - __uint_as_float(a[1] << 16),
+                                                  s[2 * kst][3] - __uint_as_float(a[1] & 0xffff0000u));
+                        alo[2] = ptx::pack_bf16x2(s[2 * kst + 1][0] - __uint_as_float(a[2] << 16),
+                                                  s[2 * kst + 1][1] - __uint_as_float(a[2] & 0xffff0000u));
+                        alo[3] = ptx::pack_bf16x2(s[2 * kst + 1][2] - __uint_as_float(a[3] << 16),
+                                                  s[2 * kst + 1][3] - __uint_as_float(a[3] & 0xffff0000u));
+                        rrun0 += bf16x2_sum(alo[0]) + bf16x2_sum(alo[2]);
+                        rrun1 += bf16x2_sum(alo[1]) + bf16x2_sum(alo[3]);
+                    }
+                    // V rows past the valid keys may hold anything (even NaN): zero them
+                    uint32_t m0 = 0xffffffffu, m1 = 0xffffffffu;
+                    if (tail) {
+                        const int k0 = kbase + 2 * tq;
+                        m0 = (k0 < n ? 0x0000ffffu : 0u) | (k0 + 1 < n ? 0xffff0000u : 0u);
+                        m1 = (k0 + 8 < n ? 0x0000ffffu : 0u) | (k0 + 9 < n ? 0xffff0000u : 0u);
+                    }
+                    const int vkey = kbase + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-                for (int dp = 0; dp < D / 16; ++dp) {
-                    uint32_t b0, b1, b2, b3;
-                    ptx::ldmatrix_x4_trans(vb + sw128_off<D>(vkey, dp * 2 + (lane >> 4)), b0, b1, b2, b3);
-                    ptx::mma_bf16_16816(o[2 * dp], a, b0 & m0, b1 & m1);
-                    ptx::mma_bf16_16816(o[2 * dp + 1], a, b2 & m0, b3 & m1);
-                    if (precise) {
-                        ptx::mma_bf16_16816(o[2 * dp], alo, b0 & m0, b1 & m1);
-                        ptx::mma_bf16_16816(o[2 * dp + 1], alo, b2 & m0, b3 & m1);
+                    for (int dp = 0; dp < D / 16; ++dp) {
+                        uint32_t b0, b1, b2, b3;
+                        ptx::ldmatrix_x4_trans(vb + sw128_off<D>(vkey, dp * 2 + (lane >> 4)), b0, b1, b2, b3);
+                        ptx::mma_bf16_16816(o[2 * dp], a, b0 & m0, b1 & m1);
+                        ptx::mma_bf16_16816(o[2 * dp + 1], a, b2 & m0, b3 & m1);
+                        if constexpr (kPrecise) {
+                            ptx::mma_bf16_16816(o[2 * dp], alo, b0 & m0, b1 & m1);
+                            ptx::mma_bf16_16816(o[2 * dp + 1], alo, b2 & m0, b3 & m1);
+                        }
                     }
                 }
-            }
+            };
+            if (kt0 < kTileKeys) pv(std::true_type{});
+            else pv(std::false_type{});
         }
         if (!compute_sync(p, ctl, 0, cs)) return false;
         if (cw == 0 && lane == 0) {
