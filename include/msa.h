@@ -190,10 +190,13 @@ int msa_append_kv(const void* k_new, const void* v_new, const int64_t* slot_mapp
  * Attention of every query row of the plan, one persistent launch.
  *
  *   q            device bf16 [n_q, Hq, D], rows in the plan's packed order
+ *                (16-byte aligned)
  *   k_pool, v_pool  device bf16 [pool_tokens, Hkv, D] (16-byte aligned)
  *   pool_tokens  rows in each pool; must cover every block the plan reads
  *   plan         an uploaded plan
- *   out          device [n_q, Hq, D], bf16 or fp32 per out_dtype
+ *   out          device [n_q, Hq, D], bf16 or fp32 per out_dtype (16-byte
+ *                aligned); a misaligned q, pool or out pointer returns
+ *                MSA_ERR_INVALID_ARG before anything is launched
  *   lse          device fp32 [n_q, Hq] (natural log of the sum of
  *                exp(scaled scores)), or NULL
  *   stream       CUDA stream

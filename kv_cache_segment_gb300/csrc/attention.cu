@@ -75,9 +75,13 @@ template <int D, bool DEC>
 struct Cfg {
     // mixed launch: 3 warpgroups (producer/MMA, softmax 0, softmax 1) with
     // a register split; decode-only: producer + 4 compute warps
-    static constexpr int kWarps = DEC ? 6 : 12;
+    static constexpr int kWarps = DEC ? 7 : 12;
     static constexpr int kThreads = kWarps * 32;
     static constexpr int kFirstCompute = DEC ? 2 : 4;  // first compute warp
+    static constexpr int kComputeWarps = DEC ? 4 : 8;
+    // combines the four compute warps' decode states and runs the cross-CTA
+    // merge, so the compute warps go on to the next item at once
+    static constexpr int kMergeWarp = DEC ? 6 : 3;
     static constexpr int kVWarp = DEC ? 1 : 2;          // the V-tile producer
     // Register split of the mixed launch (setmaxnreg): 384 threads launch with
     // 168 registers each (3 warps share an SM sub-partition's 16K registers);
@@ -122,6 +126,8 @@ struct Ctl {
     float dec_m[4][kDecRows];
     float dec_l[4][kDecRows];
     float dec_lr[4][kDecRows];
+    uint64_t merge_full, merge_empty;  // decode states in the scratch: compute warps <-> merge warp
+    int merge_item;                    // item whose states are in the scratch (-1: no more)
 };
 
 static_assert(sizeof(Ctl) <= Cfg<128, false>::kCtlBytes, "control block too large");
@@ -419,6 +425,18 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
 
 // ----------------------------------------------------- output helpers --
 
+// Four consecutive output elements starting at idx (idx a multiple of 4).
+__device__ __forceinline__ void store_out4(const AttnParams& p, int64_t idx, float4 v) {
+    if (p.out_fp32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + idx) = v;
+    } else {
+        uint2 w;
+        w.x = ptx::pack_bf16x2(v.x, v.y);
+        w.y = ptx::pack_bf16x2(v.z, v.w);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + idx) = w;
+    }
+}
+
 __device__ __forceinline__ void store_out(const AttnParams& p, int64_t idx, float v) {
     if (p.out_fp32) static_cast<float*>(p.out)[idx] = v;
     else static_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
@@ -427,8 +445,8 @@ __device__ __forceinline__ void store_out(const AttnParams& p, int64_t idx, floa
 // ------------------------------------------------------ decode (compute) --
 
 template <int D, bool DEC>
-__device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const Item& it, const Group& g,
-                            uint32_t& kv_cnt, uint32_t& cs, int cw, int lane) {
+__device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii, const Item& it, const Group& g,
+                            uint32_t& kv_cnt, uint32_t& cs, uint32_t& mg, int cw, int lane) {
     using C = Cfg<D, DEC>;
     constexpr int NT = D / 8;   // 8-column output tiles
     const int G = p.G;
@@ -463,6 +481,8 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
             qa_r[ks][3] = qword(gr + 8, ks * 16 + 8 + 2 * tq);
         }
     } else {
+        // the scratch must have been read by the merge warp (previous item)
+        if (mg > 0 && !wait_bar(p, ctl, &ctl->merge_empty, (mg - 1) & 1, kErrTimeoutCompute)) return false;
         const int tid = cw * 32 + lane;
         const uint4* qg = reinterpret_cast<const uint4*>(p.q);
         for (int e = tid; e < kDecRows * (D / 8); e += 128) {
@@ -644,6 +664,8 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
     rrun0 += __shfl_xor_sync(0xffffffffu, rrun0, 2);
     rrun1 += __shfl_xor_sync(0xffffffffu, rrun1, 1);
     rrun1 += __shfl_xor_sync(0xffffffffu, rrun1, 2);
+    // hand the four warps' states to the merge warp through the scratch
+    if (DEC && mg > 0 && !wait_bar(p, ctl, &ctl->merge_empty, (mg - 1) & 1, kErrTimeoutCompute)) return false;
     float* scr = reinterpret_cast<float*>(smem + C::kOffScr);  // [4][16][D]
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
@@ -659,75 +681,165 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const 
         ctl->dec_lr[cw][gr] = rrun0;
         ctl->dec_lr[cw][gr + 8] = rrun1;
     }
-    if (!compute_sync(p, ctl, 0, cs)) return false;
-    const int tid = cw * 32 + lane;
-    const bool split = g.n_parts > 1;
-    float* part = split ? p.dec_part + (int64_t)(g.slot + it.part) * kDecRows * D : nullptr;
-    float* plse = split ? p.dec_lse + (int64_t)(g.slot + it.part) * kDecRows : nullptr;
-    for (int e = tid; e < M * D; e += 128) {
-        const int m = e / D, d = e % D;
-        float mm = -INFINITY;
+    if (cw == 0 && lane == 0) ctl->merge_item = ii;
+    ptx::mbar_arrive(&ctl->merge_full);
+    ++mg;
+    return true;
+}
+
+// Merge warp: for each decode item handed over by the compute warps, combine
+// the four warps' (max, sums, unnormalised out) states of every query row
+// and head (log-sum-exp), write the output, or, for one part of a split group,
+// the normalised fp32 partial and its lse; then the last part to arrive
+// (atomic counter after a fence) merges the group's parts and resets the
+// counter.  Runs while the compute warps process the next item.
+template <int D, bool DEC>
+__device__ void merge_warp(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lane) {
+    using C = Cfg<D, DEC>;
+    const float* scr = reinterpret_cast<const float*>(smem + C::kOffScr);  // [4][16][D]
+    const int G = p.G;
+    for (uint32_t n = 0;; ++n) {
+        // The wait for the next hand-over spans whatever prefill work the
+        // compute warps do in between, so it may take up to 30 wait limits;
+        // it ends at once when another role aborts.
+        bool ok = false;
+        for (int r = 0; r < 30; ++r) {
+            ok = __all_sync(0xffffffffu,
+                            ptx::mbar_wait_sleep(&ctl->merge_full, n & 1, &ctl->abort, p.limit_ns, 1000));
+            if (ok || *reinterpret_cast<volatile int*>(&ctl->abort)) break;
+        }
+        if (!ok) {
+            fail(p, ctl, kErrTimeoutCompute);
+            return;
+        }
+        const int ii = ctl->merge_item;
+        if (ii < 0) return;
+        const Item it = p.items[ii];
+        const Group g = p.groups[it.group];
+        const int M = g.nrows * G;  // rows m = query row x head, <= 16
+        const int kvh = g.head;
+        const bool split = g.n_parts > 1;
+        // Lane m < M owns row m: the log-sum-exp weights of the four warps'
+        // states, normalised by the bf16-probability sum the PV MMAs used.
+        float fw[4] = {0.f, 0.f, 0.f, 0.f};
+        float lse_row = -INFINITY;
+        if (lane < M) {
+            float mm = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) mm = fmaxf(mm, ctl->dec_m[w][m]);
-        float val = 0.f, lse2 = -INFINITY;
-        if (mm != -INFINITY) {
-            float L = 0.f, LR = 0.f, acc = 0.f;
+            for (int w = 0; w < 4; ++w) mm = fmaxf(mm, ctl->dec_m[w][lane]);
+            if (mm != -INFINITY) {
+                float L = 0.f, LR = 0.f;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const float f = ptx::ex2(ctl->dec_m[w][m] - mm);
-                L += ctl->dec_l[w][m] * f;
-                LR += ctl->dec_lr[w][m] * f;
-                acc += scr[(w * kDecRows + m) * D + d] * f;
+                for (int w = 0; w < 4; ++w) {
+                    fw[w] = ptx::ex2(ctl->dec_m[w][lane] - mm);
+                    L += ctl->dec_l[w][lane] * fw[w];
+                    LR += ctl->dec_lr[w][lane] * fw[w];
+                }
+                const float inv = 1.f / LR;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) fw[w] *= inv;
+                lse_row = mm + log2f(L);
             }
-            val = acc / LR;
-            lse2 = mm + log2f(L);
         }
-        if (split) {
-            part[m * D + d] = val;
-            if (d == 0) plse[m] = lse2;
-        } else {
-            const int64_t row = g.row0 + m / G;
-            const int64_t h = (int64_t)kvh * G + m % G;
-            store_out(p, (row * p.Hq + h) * D + d, val);
-            if (d == 0 && p.lse) p.lse[row * p.Hq + h] = lse2 * kLn2;
+        float* part = split ? p.dec_part + (int64_t)(g.slot + it.part) * kDecRows * D : nullptr;
+        // elements as float4 chunks of D/4 per row; kIt uniform trips per lane
+        const int n_chunks = M * (D / 4);
+        const int kIt = (n_chunks + 31) / 32;
+        for (int k = 0; k < kIt; ++k) {
+            const int c = k * 32 + lane;
+            const int m = min(c / (D / 4), M - 1), d = (c % (D / 4)) * 4;
+            float f[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) f[w] = __shfl_sync(0xffffffffu, fw[w], m);
+            if (c < n_chunks) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float4 v = *reinterpret_cast<const float4*>(&scr[(w * kDecRows + m) * D + d]);
+                    acc.x += f[w] * v.x; acc.y += f[w] * v.y; acc.z += f[w] * v.z; acc.w += f[w] * v.w;
+                }
+                if (split) {
+                    *reinterpret_cast<float4*>(part + m * D + d) = acc;
+                } else {
+                    const int64_t row = g.row0 + m / G;
+                    const int64_t h = (int64_t)kvh * G + m % G;
+                    store_out4(p, (row * p.Hq + h) * D + d, acc);
+                }
+            }
         }
-    }
-    if (split) {
+        if (lane < M) {
+            if (split) {
+                p.dec_lse[(int64_t)(g.slot + it.part) * kDecRows + lane] = lse_row;
+            } else if (p.lse) {
+                const int64_t row = g.row0 + lane / G;
+                p.lse[row * p.Hq + (int64_t)kvh * G + lane % G] = lse_row * kLn2;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ctl->merge_empty);  // scratch free for the next item
+        if (!split) continue;
         __threadfence();
-        if (!compute_sync(p, ctl, 0, cs)) return false;
-        if (tid == 0) {
-            const int old = atomicAdd(&p.counters[2 * it.group], 1);
-            ctl->flag_last[0] = (old == g.n_parts - 1);
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&p.counters[2 * it.group], 1) == g.n_parts - 1;
+        if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+        __threadfence();
+        // last part: merge the group's parts by log-sum-exp (lane m owns row m)
+        const float* base = p.dec_part + (int64_t)g.slot * kDecRows * D;
+        const float* lbase = p.dec_lse + (int64_t)g.slot * kDecRows;
+        const int np = g.n_parts;
+        float mm = -INFINITY, invL = 0.f;
+        if (lane < M) {
+            for (int q = 0; q < np; ++q) mm = fmaxf(mm, __ldcg(lbase + q * kDecRows + lane));
+            if (mm != -INFINITY) {
+                float L = 0.f;
+                for (int q = 0; q < np; ++q) L += ptx::ex2(__ldcg(lbase + q * kDecRows + lane) - mm);
+                invL = 1.f / L;
+                lse_row = mm + log2f(L);
+            } else {
+                lse_row = -INFINITY;
+            }
         }
-        if (!compute_sync(p, ctl, 0, cs)) return false;
-        if (ctl->flag_last[0]) {
-            __threadfence();
-            const float* base = p.dec_part + (int64_t)g.slot * kDecRows * D;
-            const float* lbase = p.dec_lse + (int64_t)g.slot * kDecRows;
-            for (int e = tid; e < M * D; e += 128) {
-                const int m = e / D, d = e % D;
-                float mm = -INFINITY;
-                for (int q = 0; q < g.n_parts; ++q) mm = fmaxf(mm, __ldcg(lbase + q * kDecRows + m));
-                float val = 0.f, lse2 = -INFINITY;
-                if (mm != -INFINITY) {
-                    float L = 0.f, acc = 0.f;
-                    for (int q = 0; q < g.n_parts; ++q) {
-                        const float f = ptx::ex2(__ldcg(lbase + q * kDecRows + m) - mm);
-                        L += f;
-                        acc += f * __ldcg(base + ((int64_t)q * kDecRows + m) * D + d);
+        for (int k = 0; k < kIt; ++k) {
+            const int c = k * 32 + lane;
+            const int m = min(c / (D / 4), M - 1), d = (c % (D / 4)) * 4;
+            const float mm_m = __shfl_sync(0xffffffffu, mm, m);
+            const float inv_m = __shfl_sync(0xffffffffu, invL, m);
+            if (c < n_chunks) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (mm_m != -INFINITY) {
+                    int q = 0;
+                    for (; q + 2 <= np; q += 2) {  // two parts per step: independent loads in flight
+                        const float l0 = __ldcg(lbase + q * kDecRows + m);
+                        const float l1 = __ldcg(lbase + (q + 1) * kDecRows + m);
+                        const float4 v0 = __ldcg(reinterpret_cast<const float4*>(base + ((int64_t)q * kDecRows + m) * D + d));
+                        const float4 v1 =
+                            __ldcg(reinterpret_cast<const float4*>(base + ((int64_t)(q + 1) * kDecRows + m) * D + d));
+                        const float w0 = ptx::ex2(l0 - mm_m) * inv_m, w1 = ptx::ex2(l1 - mm_m) * inv_m;
+                        acc.x += w0 * v0.x + w1 * v1.x;
+                        acc.y += w0 * v0.y + w1 * v1.y;
+                        acc.z += w0 * v0.z + w1 * v1.z;
+                        acc.w += w0 * v0.w + w1 * v1.w;
                     }
-                    val = acc / L;
-                    lse2 = mm + log2f(L);
+                    if (q < np) {
+                        const float l0 = __ldcg(lbase + q * kDecRows + m);
+                        const float4 v0 = __ldcg(reinterpret_cast<const float4*>(base + ((int64_t)q * kDecRows + m) * D + d));
+                        const float w0 = ptx::ex2(l0 - mm_m) * inv_m;
+                        acc.x += w0 * v0.x; acc.y += w0 * v0.y; acc.z += w0 * v0.z; acc.w += w0 * v0.w;
+                    }
                 }
                 const int64_t row = g.row0 + m / G;
                 const int64_t h = (int64_t)kvh * G + m % G;
-                store_out(p, (row * p.Hq + h) * D + d, val);
-                if (d == 0 && p.lse) p.lse[row * p.Hq + h] = lse2 * kLn2;
+                store_out4(p, (row * p.Hq + h) * D + d, acc);
             }
-            if (tid == 0) p.counters[2 * it.group] = 0;  // ready for the next launch
         }
+        if (lane < M && p.lse) {
+            const int64_t row = g.row0 + lane / G;
+            p.lse[row * p.Hq + (int64_t)kvh * G + lane % G] = lse_row * kLn2;
+        }
+        __syncwarp();
+        if (lane == 0) p.counters[2 * it.group] = 0;  // ready for the next launch
     }
-    return compute_sync(p, ctl, 0, cs);  // scratch and flag free for the next item
 }
 
 // ----------------------------------------------------- prefill (compute) --
@@ -998,16 +1110,23 @@ __device__ void compute(const AttnParams& p, uint8_t* smem, Ctl* ctl, int warp, 
     using C = Cfg<D, DEC>;
     const int wg = (warp - C::kFirstCompute) >> 2;  // softmax warpgroup 0 or 1
     const int cw = (warp - C::kFirstCompute) & 3;
-    uint32_t kv_cnt = 0, sk = 0, pvk = 0, ok_cnt = 0, cs = 0, n_taken = 0;
+    uint32_t kv_cnt = 0, sk = 0, pvk = 0, ok_cnt = 0, cs = 0, n_taken = 0, mg = 0;
     for (;;) {
         const int ii = take_item(p, ctl, n_taken, kErrTimeoutCompute);
-        if (ii < 0) return;
+        if (ii < 0) {
+            if (wg == 0) {  // tell the merge warp there is nothing more
+                if (mg > 0 && !wait_bar(p, ctl, &ctl->merge_empty, (mg - 1) & 1, kErrTimeoutCompute)) return;
+                if (cw == 0 && lane == 0) ctl->merge_item = -1;
+                ptx::mbar_arrive(&ctl->merge_full);
+            }
+            return;
+        }
         const Item it = p.items[ii];
         const Group g = p.groups[it.group];
         bool ok = true;
         if (DEC || it.kind == kDecode) {
             // decode items run on warpgroup 0; warpgroup 1 only keeps count
-            if (wg == 0) ok = decode_item<D, DEC>(p, smem, ctl, it, g, kv_cnt, cs, cw, lane);
+            if (wg == 0) ok = decode_item<D, DEC>(p, smem, ctl, ii, it, g, kv_cnt, cs, mg, cw, lane);
             else kv_cnt += it.pad;
         } else if constexpr (!DEC) {
             if (wg < g.pad) {
@@ -1050,10 +1169,12 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
         }
         ptx::mbar_init(&ctl->o_full, 1);
         ptx::mbar_init(&ctl->drain, 1);
+        ptx::mbar_init(&ctl->merge_full, 128);
+        ptx::mbar_init(&ctl->merge_empty, 1);
         for (int r = 0; r < 4; ++r) {
             ptx::mbar_init(&ctl->item_full[r], 1);
             // consumers of every item id: the compute threads, the MMA thread, the V producer
-            ptx::mbar_init(&ctl->item_empty[r], (C::kWarps - C::kFirstCompute) * 32 + (DEC ? 0 : 1) + 1);
+            ptx::mbar_init(&ctl->item_empty[r], C::kComputeWarps * 32 + (DEC ? 0 : 1) + 1);
         }
         for (int r = 0; r < 8; ++r) ptx::mbar_init(&ctl->meta_full[r], 1);
         ctl->abort = 0;
@@ -1095,7 +1216,11 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
                     }
                 }
             }
+        } else if (warp == C::kMergeWarp) {
+            merge_warp<D, DEC>(p, smem, ctl, lane);
         }
+    } else if (DEC && warp == C::kMergeWarp) {
+        merge_warp<D, DEC>(p, smem, ctl, lane);
     } else {
         if constexpr (!DEC) ptx::setmaxnreg_inc<C::kRegsHigh>();
         compute<D, DEC>(p, smem, ctl, warp, lane);

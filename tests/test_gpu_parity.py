@@ -190,3 +190,30 @@ def test_full_size_configs_sampled(idx):
         rows.sort()
     ro, rl = oracle_ref(wl, k.cpu(), v.cpu(), q.cpu(), rows=rows)
     compare(out[torch.as_tensor(rows, device=dev)], lse[torch.as_tensor(rows, device=dev)], ro, rl, wl.name)
+
+
+def test_misaligned_pointers_are_rejected_before_launch():
+    """q and out must be 16-byte aligned (TMA, vector stores): a misaligned
+    pointer comes back as MSA_ERR_INVALID_ARG and nothing is written."""
+    wl = W.small_config(2)
+    k, v, q = W.make_values(wl)
+    dev = torch.device("cuda")
+    kp, vp = W.make_pool(wl, k.to(dev), v.to(dev))
+    sess = MsaSession.from_workload(wl)
+    try:
+        qd = q.to(dev)
+        n = qd.numel()
+        big = torch.full((n + 8,), 7.0, dtype=torch.bfloat16, device=dev)
+        out_bad = big[1:n + 1].view(qd.shape)  # 2 bytes past a 16-byte boundary
+        with pytest.raises(msa.MsaError) as e:
+            sess.attention(qd, kp, vp, out=out_bad)
+        assert e.value.status == msa.MSA_ERR_INVALID_ARG
+        torch.cuda.synchronize()
+        assert torch.all(big == 7.0)
+        qbig = torch.zeros((n + 8,), dtype=torch.bfloat16, device=dev)
+        qbig[1:n + 1] = qd.reshape(-1)
+        with pytest.raises(msa.MsaError) as e:
+            sess.attention(qbig[1:n + 1].view(qd.shape), kp, vp)
+        assert e.value.status == msa.MSA_ERR_INVALID_ARG
+    finally:
+        sess.close()
