@@ -460,6 +460,24 @@ def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
             lb = by / (peaks["hbm_gbs"] * 1e9) + fl / (peaks["bf16_tflops"] * 1e12)
             ent["roofline_frac_additive"] = round(lb / (attn_ms * 1e-3), 4)
             ent["traffic"] = traffic.get(key)
+            if key in ("long_context", "mixed_batch"):
+                # graded per-kind rates: the same sequences, layout and tiling
+                # with only the decode rows, then only the prefill rows
+                for kind in ("decode", "prefill"):
+                    sub = Case(W.restrict_rows(wl, kind), dev)
+                    _, sub_ms = time_case(sub, steps, warm, stream, with_append=False)
+                    if kind == "decode":
+                        gbs = sub.decode_bytes() / (sub_ms * 1e-3) / 1e9
+                        ent["decode_only"] = {"attention_ms": round(sub_ms, 4), "decode_gbs": round(gbs, 1),
+                                              "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                                              "items": int(sub.info["num_items"])}
+                    else:
+                        tf = sub.flops() / (sub_ms * 1e-3) / 1e12
+                        ent["prefill_only"] = {"attention_ms": round(sub_ms, 4), "prefill_tflops": round(tf, 2),
+                                               "tensor_frac": round(tf / peaks["bf16_tflops"], 4),
+                                               "items": int(sub.info["num_items"])}
+                    del sub
+                    torch.cuda.empty_cache()
             lines[key] = ent
         if key in ("hole_recompute", "batched_decode", "long_context"):
             _, seg_ms = time_case(case, steps, warm, stream, with_append=False)

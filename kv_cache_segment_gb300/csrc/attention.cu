@@ -235,6 +235,17 @@ __device__ void producer(const AttnParams& p, uint8_t* smem, Ctl* ctl, const CUt
         const Item it = p.items[ii];
         const Group g = p.groups[it.group];
         int kvh = g.head;
+        if (KSIDE && DEC) {
+            // The compute warps read this item's Q rows (G heads x D each,
+            // contiguous per row) when they reach it, several tiles from now:
+            // bring them into L2 first.  (Measured: +3 % in the decode-only
+            // configuration, -2 % in the mixed one, where it is left out.)
+            const uint32_t bytes = (uint32_t)(p.G * D * 2);
+            for (int r = 0; r < g.nrows; ++r)
+                ptx::prefetch_l2_bulk(static_cast<const __nv_bfloat16*>(p.q) +
+                                          ((int64_t)(g.row0 + r) * p.Hq + (int64_t)g.head * p.G) * D,
+                                      bytes);
+        }
         if (!DEC && it.kind == kPrefill) {
             kvh = g.head / p.G;
             if (KSIDE) {

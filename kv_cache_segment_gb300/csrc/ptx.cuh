@@ -97,6 +97,13 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
 
 // ----------------------------------------------------------------- TMA --
 
+// Bulk prefetch of [src, src + bytes) into L2 (src 16-byte aligned, bytes
+// a multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }

@@ -366,6 +366,38 @@ def small_config(index: int, seed: Optional[int] = None) -> Workload:
     raise KeyError(index)
 
 
+def restrict_rows(wl: Workload, kind: str) -> Workload:
+    """The same sequences, block tables and pool with only part of the query
+    rows: kind="decode" keeps the rows a plan serves as decode rows (a
+    sequence's trailing rows when they number at most 16/G, the rest of its
+    rows filling whole 128-row tiles or the sequence having no other rows),
+    kind="prefill" keeps all the others.  The two together partition the rows;
+    each keeps the tiling the full plan gives its rows."""
+    assert kind in ("decode", "prefill")
+    G = wl.num_q_heads // wl.num_kv_heads
+    dec_rows = max(1, 16 // G)
+    ranges = []
+    for rs in wl.q_ranges:
+        pos = [p for a, b in rs for p in range(a, b)]
+        n = len(pos)
+        if n == 0:
+            n_dec = 0
+        elif n <= dec_rows:
+            n_dec = n
+        else:
+            rem = n % 128
+            n_dec = rem if 0 < rem <= dec_rows else 0
+        keep = pos[n - n_dec:] if kind == "decode" else pos[:n - n_dec]
+        out = []
+        for p in keep:
+            if out and out[-1][1] == p:
+                out[-1][1] = p + 1
+            else:
+                out.append([p, p + 1])
+        ranges.append([tuple(r) for r in out])
+    return dataclasses.replace(wl, q_ranges=ranges, name=f"{wl.name}/{kind}-rows")
+
+
 # ------------------------------------------------------------------ values --
 
 def make_values(wl: Workload, device="cpu", seed: Optional[int] = None, dtype=None):

@@ -200,3 +200,27 @@ def test_empty_sequence_and_split_groups():
         assert long[:, 8].max() > 0  # split into several parts
     finally:
         msa.msa_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("idx", [4, 5])
+def test_restricted_rows_partition_the_plan(idx):
+    """Decode-only and prefill-only restrictions of a mixed workload (the
+    bench's graded legs) split its rows, decode bytes and prefill flops
+    exactly as the full plan classifies them."""
+    wl = W.config(idx)
+    dec, pre = W.restrict_rows(wl, "decode"), W.restrict_rows(wl, "prefill")
+    assert dec.num_q_rows + pre.num_q_rows == wl.num_q_rows
+    for s in range(wl.num_seqs):
+        full = sorted(p for a, b in wl.q_ranges[s] for p in range(a, b))
+        parts = sorted(p for r in (dec.q_ranges[s], pre.q_ranges[s]) for a, b in r for p in range(a, b))
+        assert full == parts
+    infos = []
+    for w in (wl, dec, pre):
+        plan = _plan(w)
+        try:
+            infos.append(msa.msa_plan_get_info(plan))
+        finally:
+            msa.msa_plan_destroy(plan)
+    full, di, pi = infos
+    assert di["decode_kv_bytes"] == full["decode_kv_bytes"] and di["prefill_flops"] == 0
+    assert pi["decode_kv_bytes"] == 0 and pi["prefill_flops"] == pytest.approx(full["prefill_flops"], rel=1e-12)
