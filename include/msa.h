@@ -165,6 +165,57 @@ int msa_plan_get_info(msa_plan_t plan, msa_plan_info* info);
  * part).  With items == NULL only *n_items is written. */
 int msa_plan_get_items(msa_plan_t plan, int32_t* items, int32_t* n_items);
 
+/* The plan's processing order: order[q] = index (into the msa_plan_get_items
+ * list) of the q-th item the persistent launch hands out.  With order ==
+ * NULL only *n_items is written.  For tests and the cost model's checks. */
+int msa_plan_get_order(msa_plan_t plan, int32_t* order, int32_t* n_items);
+
+/*
+ * Expected-latency model of one msa_attention launch.  AsymCache's eviction
+ * and chunking decisions weigh recompute cost against hit rate using the
+ * expected latency of the attention kernel (MSA paper abstract; AsymCache
+ * explainer, "核心方法 2/3"); this is that model for this kernel.
+ *
+ * Each work item costs
+ *     decode : dec_item_us + dec_tile_us * tiles
+ *     prefill: pre_item_us + pre_tile_us * tiles * heads   (heads = 1 or 2)
+ *   + box_us * (extra TMA boxes: a tile that is not a full 128-key window
+ *              inside one segment is fetched one 16-key block at a time;
+ *              each box beyond the first of its tile counts)
+ *   + merge_us (items of a group split into several parts)
+ * where tiles = 128-key windows the item walks.  The items are handed out in
+ * the plan's order to `grid` CTAs, each taking the next item as soon as it is
+ * free (earliest-free CTA first, lower CTA index on ties), as the kernel's
+ * queue does.  time_us = launch_us + the time the last CTA finishes.
+ * Parameters fitted on this GPU ship with the Python package
+ * (kv_cache_segment_gb300/cost_params_gb300.json).
+ */
+typedef struct {
+    double launch_us;
+    double dec_item_us;
+    double dec_tile_us;
+    double pre_item_us;
+    double pre_tile_us;
+    double box_us;
+    double merge_us;
+} msa_cost_params;
+
+typedef struct {
+    double time_us;          /* launch_us + makespan_us                       */
+    double makespan_us;      /* finish time of the last CTA                   */
+    double busy_us;          /* sum of all item costs                         */
+    int64_t n_items;
+    int64_t n_split_items;   /* items of groups split into several parts      */
+    int64_t decode_tiles;    /* sum over decode items of their tiles          */
+    int64_t prefill_tile_heads; /* sum over prefill items of tiles * heads    */
+    int64_t extra_boxes;     /* see above                                     */
+    int64_t decode_kv_bytes; /* as msa_plan_info                              */
+    double prefill_flops;    /* as msa_plan_info                              */
+} msa_cost_estimate;
+
+/* Fill *est for the plan under the given parameters (host only). */
+int msa_plan_estimate(msa_plan_t plan, const msa_cost_params* params, msa_cost_estimate* est);
+
 int msa_plan_destroy(msa_plan_t plan);
 
 /*

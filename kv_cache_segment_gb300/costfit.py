@@ -1,0 +1,176 @@
+"""Fit the attention-latency model (msa_plan_estimate, include/msa.h) to
+kernel times measured on this GPU, and check it on workloads it was not fitted
+on.
+
+AsymCache weighs recompute cost against hit rate with the attention kernel's
+expected latency (MSA paper abstract; AsymCache explainer, "核心方法 2/3");
+this script gives that model its constants for this kernel and GPU.
+
+    python -m kv_cache_segment_gb300.costfit --out cost_params_gb300.json
+
+Training and validation workloads are synthetic, drawn with the same
+generators as the bench (decode batches of several sizes, lengths and
+segment counts; hole recompute; long-context chunks; mixed batches) at
+different seeds and sizes for the two sets.  Each is timed as the median of
+`--reps` launches of msa_attention alone (CUDA events on the launching
+stream, after warm-up launches).  The seven parameters are fitted by
+bounded least squares on log(predicted / measured).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import sys
+import time
+
+import numpy as np
+
+from . import msa
+from . import workloads as W
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+DEFAULT_PATH = os.path.join(_HERE, "cost_params_gb300.json")
+
+
+def _decode(seed, n, lr, seg, name, hq=32, hkv=8):
+    """A decode batch in a pool of twice its largest possible size (the
+    generator scatters the segments over the whole pool)."""
+    pool = -(-2 * n * lr[1] // 16) * 16
+    return name, W.batched_decode(seed=seed, num_seqs=n, len_range=lr, max_seg=seg, pool_tokens=pool, hq=hq, hkv=hkv)
+
+
+def training_set():
+    s = []
+    for i, (n, lr, seg) in enumerate([(8, (512, 4096), 1), (32, (2048, 16384), 8), (96, (2048, 8192), 4),
+                                      (16, (16384, 32768), 64), (64, (256, 2048), 16), (128, (4096, 8192), 2)]):
+        s.append(_decode(2000 + i, n, lr, seg, f"decode{i}"))
+    for i, (n, G) in enumerate([(24, 8), (48, 2)]):
+        s.append(_decode(2010 + i, n, (2048, 16384), 8, f"decode_g{G}", hq=8 * G))
+    for i, (n, cb, ev) in enumerate([(2, 128, 32), (8, 256, 64), (16, 512, 128), (4, 512, 256)]):
+        s.append((f"holes{i}", W.hole_recompute(seed=2020 + i, num_seqs=n, cached_blocks=cb, evict_blocks=ev)))
+    for i, (length, runs, chunk) in enumerate([(16384, 1, 512), (65536, 64, 2048), (32768, 16, 1024)]):
+        s.append((f"long{i}", W.long_context(seed=2030 + i, num_seqs=1, length=length, n_runs=runs, chunk=chunk)))
+    for i, (nd, npf, chunk) in enumerate([(16, 1, 512), (64, 4, 2048), (128, 2, 1024)]):
+        s.append((f"mixed{i}", W.mixed_batch(seed=2040 + i, num_decode=nd, num_prefill=npf, chunk=chunk)))
+    return s
+
+
+def validation_set():
+    s = []
+    for i, (n, lr, seg) in enumerate([(20, (1024, 8192), 3), (48, (8192, 16384), 32), (200, (512, 4096), 8)]):
+        s.append(_decode(3000 + i, n, lr, seg, f"v_decode{i}"))
+    for i, (n, cb, ev) in enumerate([(4, 384, 96), (12, 512, 64)]):
+        s.append((f"v_holes{i}", W.hole_recompute(seed=3010 + i, num_seqs=n, cached_blocks=cb, evict_blocks=ev)))
+    s.append(("v_long", W.long_context(seed=3020, num_seqs=2, length=49152, n_runs=32, chunk=1536)))
+    for i, (nd, npf, chunk) in enumerate([(32, 2, 1024), (96, 3, 2048)]):
+        s.append((f"v_mixed{i}", W.mixed_batch(seed=3030 + i, num_decode=nd, num_prefill=npf, chunk=chunk)))
+    return s
+
+
+def measure(wl, dev, reps=15, warmup=3):
+    """Median msa_attention time (us) and the plan's estimate inputs."""
+    import torch
+    from .runner import MsaSession
+    k, v, q = W.make_values(wl, device=dev)
+    kp, vp = W.make_pool(wl, k, v, fill=0.0)
+    del k, v
+    sess = MsaSession.from_workload(wl, device=dev)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        sess.attention(q, kp, vp, out=out)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        sess.attention(q, kp, vp, out=out)
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b) * 1e3)
+    rc, word = sess.check_device()
+    if rc != 0:
+        raise RuntimeError(f"device error word {word:#x}")
+    return float(np.median(times)), sess
+
+
+def predict(plan, params):
+    return msa.msa_plan_estimate(plan, params)["time_us"]
+
+
+def fit(records, x0=None):
+    """records: [(plan, measured_us)] -> params dict (least squares on logs)."""
+    from scipy.optimize import least_squares
+    names = msa.COST_PARAM_NAMES
+    x0 = np.asarray(x0 if x0 is not None else [8.0, 2.0, 1.3, 4.0, 1.0, 0.02, 2.0], float)
+
+    def resid(x):
+        p = dict(zip(names, x))
+        return np.array([math.log(max(predict(pl, p), 1e-3) / t) for pl, t in records])
+
+    r = least_squares(resid, x0, bounds=(np.zeros(len(names)), np.full(len(names), np.inf)), x_scale="jac")
+    return dict(zip(names, (float(v) for v in r.x)))
+
+
+def errors(records, params):
+    e = [predict(pl, params) / t - 1.0 for pl, t in records]
+    return {"mean_abs_rel_err": float(np.mean(np.abs(e))), "max_abs_rel_err": float(np.max(np.abs(e)))}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", default=DEFAULT_PATH)
+    ap.add_argument("--reps", type=int, default=15)
+    args = ap.parse_args(argv)
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    msa.load()
+    t0 = time.time()
+    rows = {"train": [], "validation": []}
+    keep = {"train": [], "validation": []}
+    for which, wls in (("train", training_set()), ("validation", validation_set())):
+        for name, wl in wls:
+            us, sess = measure(wl, dev, reps=args.reps)
+            info = sess.info
+            rows[which].append({"workload": name, "measured_us": round(us, 2), "items": info["num_items"],
+                                "decode_kv_bytes": info["decode_kv_bytes"], "prefill_flops": info["prefill_flops"]})
+            keep[which].append((sess, us))
+            torch.cuda.empty_cache()
+            print(f"{which:10s} {name:12s} {us:10.1f} us  items {info['num_items']}", file=sys.stderr)
+    train = [(s.plan, t) for s, t in keep["train"]]
+    val = [(s.plan, t) for s, t in keep["validation"]]
+    params = fit(train)
+    for which, recs in (("train", train), ("validation", val)):
+        for row, (pl, t) in zip(rows[which], recs):
+            row["predicted_us"] = round(predict(pl, params), 2)
+    doc = {
+        "device": torch.cuda.get_device_name(dev),
+        "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count,
+        "params": {k: round(v, 5) for k, v in params.items()},
+        "fit": {"train": errors(train, params), "validation": errors(val, params)},
+        "records": rows,
+        "seconds": round(time.time() - t0, 1),
+        "command": "python -m kv_cache_segment_gb300.costfit --out <path>",
+    }
+    with open(args.out, "w") as f:
+        json.dump(doc, f, indent=1)
+    print(json.dumps({"params": doc["params"], "fit": doc["fit"]}))
+    for s, _ in keep["train"] + keep["validation"]:
+        s.close()
+    return 0
+
+
+def load_params(path: str = DEFAULT_PATH):
+    """The fitted parameters (dict), or None when no fit has been stored."""
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        return json.load(f)["params"]
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -198,9 +198,11 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
     for (size_t gi = 0; gi < pend.size(); ++gi) {
         Pending& pd = pend[gi];
         const int32_t kind = pd.g.kind;
-        // decode items end with a cross-CTA merge (a fence and an atomic round
-        // trip), so they are cut coarser than prefill items
-        const double per_item = kind == kDecode ? per_cta / 6.0 : per_cta / 16.0;
+        // Each part of a split group costs a partial write and a share of the
+        // merge, and each item a pipeline start and an epilogue; measured on
+        // GB300, parts of about a third (decode) and a quarter (prefill) of
+        // a CTA's share beat finer cuts on every bench workload.
+        const double per_item = kind == kDecode ? per_cta / 3.0 : per_cta / 4.0;
         int64_t chunk = std::max<int64_t>(min_tiles[kind], (int64_t)std::ceil(per_item / w_tile[kind]));
         int32_t parts = (int32_t)std::max<int64_t>(1, (pd.tiles + chunk - 1) / chunk);
         const int32_t s = pd.g.seq;

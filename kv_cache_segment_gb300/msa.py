@@ -54,6 +54,23 @@ class msa_plan_info(ctypes.Structure):
                 ("host_plan_us", ctypes.c_double)]
 
 
+class msa_cost_params(ctypes.Structure):
+    _fields_ = [("launch_us", ctypes.c_double), ("dec_item_us", ctypes.c_double),
+                ("dec_tile_us", ctypes.c_double), ("pre_item_us", ctypes.c_double),
+                ("pre_tile_us", ctypes.c_double), ("box_us", ctypes.c_double),
+                ("merge_us", ctypes.c_double)]
+
+
+class msa_cost_estimate(ctypes.Structure):
+    _fields_ = [("time_us", ctypes.c_double), ("makespan_us", ctypes.c_double),
+                ("busy_us", ctypes.c_double), ("n_items", ctypes.c_int64),
+                ("n_split_items", ctypes.c_int64), ("decode_tiles", ctypes.c_int64),
+                ("prefill_tile_heads", ctypes.c_int64), ("extra_boxes", ctypes.c_int64),
+                ("decode_kv_bytes", ctypes.c_int64), ("prefill_flops", ctypes.c_double)]
+
+
+COST_PARAM_NAMES = tuple(name for name, _ in msa_cost_params._fields_)
+
 _lib = None
 
 
@@ -74,6 +91,9 @@ def load(path: str = LIB_PATH):
         "msa_plan_get_runs": ([vp, i32, vp, ctypes.POINTER(i32)], ctypes.c_int),
         "msa_plan_get_info": ([vp, ctypes.POINTER(msa_plan_info)], ctypes.c_int),
         "msa_plan_get_items": ([vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
+        "msa_plan_get_order": ([vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
+        "msa_plan_estimate": ([vp, ctypes.POINTER(msa_cost_params), ctypes.POINTER(msa_cost_estimate)],
+                              ctypes.c_int),
         "msa_plan_destroy": ([vp], ctypes.c_int),
         "msa_append_kv": ([vp, vp, vp, i32, vp, vp, i64, ctypes.POINTER(msa_dims), vp, vp], ctypes.c_int),
         "msa_attention": ([vp, vp, vp, i64, vp, vp, i32, vp, vp], ctypes.c_int),
@@ -176,6 +196,24 @@ def msa_plan_get_items(plan) -> np.ndarray:
     out = np.zeros((max(n.value, 1), 9), np.int32)
     _check(lib.msa_plan_get_items(plan, out.ctypes.data, ctypes.byref(n)), "msa_plan_get_items")
     return out[: n.value]
+
+
+def msa_plan_get_order(plan) -> np.ndarray:
+    lib = load()
+    n = ctypes.c_int32(0)
+    _check(lib.msa_plan_get_order(plan, None, ctypes.byref(n)), "msa_plan_get_order")
+    out = np.zeros(max(n.value, 1), np.int32)
+    _check(lib.msa_plan_get_order(plan, out.ctypes.data, ctypes.byref(n)), "msa_plan_get_order")
+    return out[: n.value]
+
+
+def msa_plan_estimate(plan, params) -> dict:
+    """Expected launch time and work features of a plan (see include/msa.h);
+    `params` is a dict with the msa_cost_params field names."""
+    c = msa_cost_params(*[float(params[k]) for k in COST_PARAM_NAMES])
+    e = msa_cost_estimate()
+    _check(load().msa_plan_estimate(plan, ctypes.byref(c), ctypes.byref(e)), "msa_plan_estimate")
+    return {name: getattr(e, name) for name, _ in msa_cost_estimate._fields_}
 
 
 def msa_plan_destroy(plan):

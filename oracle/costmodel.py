@@ -1,0 +1,102 @@
+"""Plain Python restatement of the attention-latency model (test
+infrastructure only: the library's msa_plan_estimate is checked against it).
+
+AsymCache weighs a block's recompute cost and hit rate against the attention
+kernel's expected latency (MSA paper abstract; AsymCache explainer, "核心方法
+2" and "3").  The model prices each work item and replays the kernel's work
+queue:
+
+  cost(item) = dec_item + dec_tile * tiles                    (decode)
+             | pre_item + pre_tile * tiles * heads             (prefill)
+             + box * extra_boxes + merge * [group split into parts]
+
+  tiles        128-key windows [kb + 128 i, min(kb + 128 (i+1), ke))
+  extra_boxes  per tile, the TMA boxes beyond one: a full 128-key window
+               inside one segment is one box, any other tile one box per
+               16-key block of each segment piece it touches
+  makespan     items handed out in the plan's order, each to the CTA that is
+               free first (lowest index on ties); the last finish time
+  time         launch + makespan
+
+Segments come from oracle.segments (the brute-force splitter over the block
+table), never from the library; the work list and its order are the plan's
+(inputs here, not recomputed).  Pure Python loops: small and medium plans.
+"""
+from __future__ import annotations
+
+from .segments import split_into_contiguous_segments
+
+TILE = 128
+BLOCK = 16
+
+
+def _token_segments(table_row, seq_len):
+    """[(first logical token, n_tokens)] of one sequence's segments."""
+    return [(b0 * BLOCK, ntok) for (b0, _p, _nb, ntok) in split_into_contiguous_segments(table_row, seq_len, BLOCK)]
+
+
+def _boxes(segs, t0, t1):
+    """TMA boxes for the tile [t0, t1) of a sequence with segments `segs`."""
+    boxes = 0
+    for (a, n) in segs:
+        lo, hi = max(a, t0), min(a + n, t1)
+        if hi <= lo:
+            continue
+        if lo == t0 and hi - lo == TILE:
+            boxes += 1
+        else:
+            boxes += -(-(hi - lo) // BLOCK)
+    return boxes
+
+
+def estimate(items, order, block_table, seq_lens, grid, params):
+    """items: rows (kind, seq, head, heads, row0, nrows, kb, ke, part) as
+    msa_plan_get_items returns them; order: msa_plan_get_order; params: dict
+    of the msa_cost_params names.  Returns a dict like msa_plan_estimate."""
+    segs = {}
+    parts = {}
+    for (kind, seq, head, heads, row0, nrows, kb, ke, part) in items:
+        key = (kind, seq, head, row0)
+        parts[key] = parts.get(key, 0) + 1
+    cost = []
+    out = {"n_items": len(items), "n_split_items": 0, "decode_tiles": 0, "prefill_tile_heads": 0,
+           "extra_boxes": 0, "busy_us": 0.0}
+    for (kind, seq, head, heads, row0, nrows, kb, ke, part) in items:
+        if seq not in segs:
+            segs[seq] = _token_segments(block_table[seq], int(seq_lens[seq]))
+        tiles = 0
+        extra = 0
+        t0 = kb
+        while t0 < ke:
+            t1 = min(t0 + TILE, ke)
+            tiles += 1
+            extra += max(0, _boxes(segs[seq], t0, t1) - 1)
+            t0 += TILE
+        split = parts[(kind, seq, head, row0)] > 1
+        if kind == 0:
+            c = params["dec_item_us"] + params["dec_tile_us"] * tiles
+            out["decode_tiles"] += tiles
+        else:
+            c = params["pre_item_us"] + params["pre_tile_us"] * tiles * heads
+            out["prefill_tile_heads"] += tiles * heads
+        c += params["box_us"] * extra + (params["merge_us"] if split else 0.0)
+        out["extra_boxes"] += extra
+        out["n_split_items"] += 1 if split else 0
+        out["busy_us"] += c
+        cost.append(c)
+    free = [0.0] * max(1, int(grid))
+    makespan = 0.0
+    for idx in order:
+        b = min(range(len(free)), key=lambda i: (free[i], i))
+        free[b] += cost[idx]
+        makespan = max(makespan, free[b])
+    out["makespan_us"] = makespan
+    out["time_us"] = params["launch_us"] + makespan
+    return out
+
+
+def hole_recompute_flops(head_dim, num_q_heads, start, end, seq_len):
+    """Attention flops of recomputing query rows [start, end) of a sequence
+    holding seq_len tokens: 4 * D * Hq * sum over p of min(p + 1, seq_len),
+    the position-aware recompute cost (a row at p attends to p + 1 keys)."""
+    return 4.0 * head_dim * num_q_heads * sum(min(p + 1, seq_len) for p in range(start, end))

@@ -1,0 +1,116 @@
+"""Attention-latency model (msa_plan_estimate): the library against the plain
+Python restatement in oracle/costmodel.py, and both against closed forms."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle.costmodel as OC
+from kv_cache_segment_gb300 import msa, workloads as W
+
+PARAMS = dict(launch_us=6.5, dec_item_us=2.25, dec_tile_us=1.375, pre_item_us=3.5, pre_tile_us=0.875,
+              box_us=0.0625, merge_us=1.75)
+
+
+def _plan(wl, num_sms=152):
+    dims = msa.make_dims(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, 16, wl.scale)
+    return msa.msa_plan_create(dims, wl.block_table, wl.seq_lens, wl.q_range_indptr, wl.q_ranges_flat, num_sms)
+
+
+def _both(wl, params=PARAMS, num_sms=152):
+    plan = _plan(wl, num_sms)
+    try:
+        lib = msa.msa_plan_estimate(plan, params)
+        items = msa.msa_plan_get_items(plan)
+        order = msa.msa_plan_get_order(plan)
+        grid = msa.msa_plan_get_info(plan)["grid"]
+        ref = OC.estimate(items.tolist(), order.tolist(), wl.block_table, wl.seq_lens, grid, params)
+        info = msa.msa_plan_get_info(plan)
+    finally:
+        msa.msa_plan_destroy(plan)
+    return lib, ref, info
+
+
+INT_KEYS = ("n_items", "n_split_items", "decode_tiles", "prefill_tile_heads", "extra_boxes")
+
+
+@pytest.mark.parametrize("wl_fn", [lambda: W.small_config(1), lambda: W.small_config(2), lambda: W.small_config(3),
+                                   lambda: W.small_config(5), lambda: W.config(2), lambda: W.config(5)],
+                         ids=["small1", "small2", "small3", "small5", "batched_decode", "mixed_batch"])
+def test_library_matches_oracle(wl_fn):
+    lib, ref, _ = _both(wl_fn())
+    for k in INT_KEYS:
+        assert lib[k] == ref[k], k
+    for k in ("busy_us", "makespan_us", "time_us"):
+        assert lib[k] == pytest.approx(ref[k], rel=1e-12), k
+
+
+@pytest.mark.parametrize("num_sms", [1, 7, 1500])
+def test_library_matches_oracle_other_grids(num_sms):
+    lib, ref, _ = _both(W.small_config(3), num_sms=num_sms)
+    for k in INT_KEYS:
+        assert lib[k] == ref[k], k
+    assert lib["makespan_us"] == pytest.approx(ref["makespan_us"], rel=1e-12)
+
+
+def test_one_cta_makespan_is_the_sum_of_item_costs():
+    lib, ref, info = _both(W.small_config(5), num_sms=1)
+    assert info["grid"] == 1
+    assert lib["makespan_us"] == pytest.approx(lib["busy_us"], rel=1e-12)
+    assert ref["makespan_us"] == pytest.approx(ref["busy_us"], rel=1e-12)
+
+
+@pytest.mark.parametrize("n_seqs,ctas", [(6, 4), (8, 8), (20, 3)])
+def test_equal_items_fill_ctas_in_rounds(n_seqs, ctas):
+    """N identical decode groups (one segment, one query, 3 tiles, no split)
+    on C CTAs finish in ceil(N/C) rounds of one item cost."""
+    L = 3 * 128
+    wl = W.custom([L] * n_seqs, [[L // 16]] * n_seqs, [[(L, L + 1)]] * n_seqs, hq=4, hkv=1)
+    params = dict(PARAMS, box_us=0.0)
+    lib, ref, info = _both(wl, params, num_sms=ctas)
+    assert lib["n_items"] == n_seqs and lib["n_split_items"] == 0 and lib["decode_tiles"] == 3 * n_seqs
+    item = params["dec_item_us"] + 3 * params["dec_tile_us"]
+    rounds = math.ceil(n_seqs / info["grid"])
+    assert lib["makespan_us"] == pytest.approx(rounds * item, rel=1e-12)
+    assert ref["makespan_us"] == pytest.approx(rounds * item, rel=1e-12)
+
+
+def test_single_block_segments_cost_seven_extra_boxes_per_full_tile():
+    """Every block its own segment: a full tile touches 8 segments (8 boxes),
+    a partial last tile of n keys ceil(n/16) boxes."""
+    L = 2 * 128 + 40
+    nb = -(-L // 16)
+    wl = W.custom([L], [[1] * nb], [[(L, L + 1)]], hq=4, hkv=1)
+    lib, ref, _ = _both(wl, num_sms=1)
+    want = 2 * 7 + (math.ceil(40 / 16) - 1)
+    assert lib["extra_boxes"] == want and ref["extra_boxes"] == want
+    one = W.custom([L], [[nb]], [[(L, L + 1)]], hq=4, hkv=1)
+    lib1, ref1, _ = _both(one, num_sms=1)
+    assert lib1["extra_boxes"] == ref1["extra_boxes"] == math.ceil(40 / 16) - 1  # only the partial tile
+
+
+@pytest.mark.parametrize("a,b,L", [(0, 37, 400), (100, 228, 400), (380, 401, 400)])
+def test_position_aware_recompute_flops(a, b, L):
+    """Rows [a, b) of one sequence: 4 D Hq sum_p min(p+1, L); the closed form
+    of the sum, the oracle and the plan agree."""
+    hq, d = 8, 128
+    closed = sum(p + 1 for p in range(a, min(b, L))) + (L if b == L + 1 else 0)
+    arith = (min(b, L) * (min(b, L) + 1) // 2 - a * (a + 1) // 2) + (L if b == L + 1 else 0)
+    assert closed == arith
+    assert OC.hole_recompute_flops(d, hq, a, b, L) == 4.0 * d * hq * arith
+    wl = W.custom([L], [[-(-L // 16)]], [[(a, b)]], hq=hq, hkv=2, d=d)
+    _, _, info = _both(wl)
+    dec_rows = 16 // (hq // 2)
+    if b - a > dec_rows:
+        n = b - a
+        rem = n % 128
+        if 0 < rem <= dec_rows:  # the trailing rows go to the decode path
+            pre = 4.0 * d * hq * sum(min(p + 1, L) for p in range(a, b - rem))
+        else:
+            pre = 4.0 * d * hq * arith
+        assert info["prefill_flops"] == pytest.approx(pre, rel=1e-12)
+
+
+def test_estimate_rejects_null():
+    with pytest.raises(msa.MsaError):
+        msa._check(msa.load().msa_plan_estimate(None, None, None), "msa_plan_estimate")
