@@ -99,6 +99,8 @@ typedef struct {
     double prefill_flops;        /* 4*D*sum over prefill (row, head) of n_vis(p) */
     int64_t max_pool_row;        /* highest pool row the plan reads, plus one    */
     double host_plan_us;         /* time msa_plan_create spent                   */
+    double decode_split;         /* split factors the work items were cut with   */
+    double prefill_split;        /* (see msa_plan_options)                       */
 } msa_plan_info;
 
 /*
@@ -176,24 +178,29 @@ int msa_plan_get_order(msa_plan_t plan, int32_t* order, int32_t* n_items);
  * expected latency of the attention kernel (MSA paper abstract; AsymCache
  * explainer, "核心方法 2/3"); this is that model for this kernel.
  *
- * Each work item costs
- *     decode : dec_item_us + dec_tile_us * tiles
- *     prefill: pre_item_us + pre_tile_us * tiles * heads   (heads = 1 or 2)
- *   + box_us * (extra TMA boxes: a tile that is not a full 128-key window
- *              inside one segment is fetched one 16-key block at a time;
- *              each box beyond the first of its tile counts)
- *   + merge_us (items of a group split into several parts)
- * where tiles = 128-key windows the item walks.  The items are handed out in
- * the plan's order to `grid` CTAs, each taking the next item as soon as it is
- * free (earliest-free CTA first, lower CTA index on ties), as the kernel's
- * queue does.  time_us = launch_us + the time the last CTA finishes.
- * Parameters fitted on this GPU ship with the Python package
+ * Each work item runs two phases on the CTA that takes it:
+ *   fixed phase (time):
+ *     decode : dec_item_us            prefill: pre_item_us + pre_tile_us * tiles * heads
+ *     + box_us * extra_boxes + merge_us (if its group is split into parts)
+ *   stream phase (decode items only, bytes): tiles * 128 keys * D * 2 B * 2
+ *     (K and V); every CTA in a stream phase progresses at
+ *     min(dec_cta_gbs, dec_gbs / number of CTAs in a stream phase), so the
+ *     CTAs share HBM and the last ones run faster.
+ * tiles = 128-key windows the item walks; heads = 1 or 2 query heads of a
+ * prefill item; extra_boxes = TMA boxes beyond one per tile (a tile that is
+ * not a full 128-key window inside one segment is fetched one 16-key block
+ * at a time).  Items are handed out in the plan's order to `grid` CTAs, a
+ * CTA taking the next one when it becomes free (several freed at once take
+ * in CTA order), as the kernel's queue does.  The replay is event by event:
+ * time_us = launch_us + the time the last CTA finishes.  Parameters fitted
+ * on this GPU ship with the Python package
  * (kv_cache_segment_gb300/cost_params_gb300.json).
  */
 typedef struct {
     double launch_us;
     double dec_item_us;
-    double dec_tile_us;
+    double dec_gbs;      /* HBM bandwidth the decode streams share (GB/s)   */
+    double dec_cta_gbs;  /* most one CTA streams on its own (GB/s)          */
     double pre_item_us;
     double pre_tile_us;
     double box_us;
@@ -203,18 +210,42 @@ typedef struct {
 typedef struct {
     double time_us;          /* launch_us + makespan_us                       */
     double makespan_us;      /* finish time of the last CTA                   */
-    double busy_us;          /* sum of all item costs                         */
+    double fixed_us;         /* sum of all items' fixed phases                */
     int64_t n_items;
     int64_t n_split_items;   /* items of groups split into several parts      */
     int64_t decode_tiles;    /* sum over decode items of their tiles          */
     int64_t prefill_tile_heads; /* sum over prefill items of tiles * heads    */
     int64_t extra_boxes;     /* see above                                     */
+    int64_t stream_bytes;    /* sum of the decode items' stream phases        */
     int64_t decode_kv_bytes; /* as msa_plan_info                              */
     double prefill_flops;    /* as msa_plan_info                              */
 } msa_cost_estimate;
 
 /* Fill *est for the plan under the given parameters (host only). */
 int msa_plan_estimate(msa_plan_t plan, const msa_cost_params* params, msa_cost_estimate* est);
+
+/*
+ * msa_plan_create with options.  Work items: a group (decode rows of one kv
+ * head, or a 128-row tile of one or two query heads) whose key range is
+ * long is cut into parts of about (the launch's work per CTA) / split tiles;
+ * each part is an item, and the parts are merged by log-sum-exp.  Parts
+ * balance the CTAs but each costs a partial write, a merge share and a
+ * pipeline start.  Adaptive chunking (AsymCache explainer, "核心方法 3"):
+ * with choose_with set, the planner tries decode_split in {1, 1.5, 2, 3, 4,
+ * 6}, then prefill_split in {1, 2, 4, 8}, and keeps the plan with the lowest
+ * msa_plan_estimate time under those parameters.  msa_plan_info reports the
+ * factors used.
+ */
+typedef struct {
+    int32_t num_sms;        /* CTAs of the launch; 0 = the current device's SMs   */
+    double decode_split;    /* > 0: split factor for decode groups; 0 = default 3  */
+    double prefill_split;   /* > 0: split factor for prefill groups; 0 = default 4 */
+    const msa_cost_params* choose_with;  /* non-NULL: choose the factors (above) */
+} msa_plan_options;
+
+int msa_plan_create_ex(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks_per_seq,
+                       const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_range_indptr,
+                       const int32_t* q_ranges, const msa_plan_options* opts, msa_plan_t* out);
 
 int msa_plan_destroy(msa_plan_t plan);
 

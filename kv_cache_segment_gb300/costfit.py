@@ -11,9 +11,10 @@ this script gives that model its constants for this kernel and GPU.
 Training and validation workloads are synthetic, drawn with the same
 generators as the bench (decode batches of several sizes, lengths and
 segment counts; hole recompute; long-context chunks; mixed batches) at
-different seeds and sizes for the two sets.  Each is timed as the median of
+different seeds and sizes for the two sets, each planned with three
+different split factors (msa_plan_create_ex).  Each plan is timed as the median of
 `--reps` launches of msa_attention alone (CUDA events on the launching
-stream, after warm-up launches).  The seven parameters are fitted by
+stream, after warm-up launches).  The eight parameters are fitted by
 bounded least squares on log(predicted / measured).
 """
 from __future__ import annotations
@@ -69,32 +70,41 @@ def validation_set():
     return s
 
 
-def measure(wl, dev, reps=15, warmup=3):
-    """Median msa_attention time (us) and the plan's estimate inputs."""
+# Each workload is measured under these (decode_split, prefill_split) plans:
+# the same work cut into more or fewer items, so that the per-item and merge
+# constants are told apart from the per-tile ones.
+SPLITS = ((3.0, 4.0), (1.0, 1.0), (6.0, 8.0))
+
+
+def measure(wl, dev, reps=15, warmup=3, splits=SPLITS):
+    """[(median msa_attention time in us, session)] for each split plan."""
     import torch
     from .runner import MsaSession
     k, v, q = W.make_values(wl, device=dev)
     kp, vp = W.make_pool(wl, k, v, fill=0.0)
     del k, v
-    sess = MsaSession.from_workload(wl, device=dev)
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
-    for _ in range(warmup):
-        sess.attention(q, kp, vp, out=out)
-    torch.cuda.synchronize()
-    times = []
-    for _ in range(reps):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        sess.attention(q, kp, vp, out=out)
-        b.record(stream)
-        b.synchronize()
-        times.append(a.elapsed_time(b) * 1e3)
-    rc, word = sess.check_device()
-    if rc != 0:
-        raise RuntimeError(f"device error word {word:#x}")
-    return float(np.median(times)), sess
+    res = []
+    for ds, ps in splits:
+        sess = MsaSession.from_workload(wl, device=dev, decode_split=ds, prefill_split=ps)
+        for _ in range(warmup):
+            sess.attention(q, kp, vp, out=out)
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            sess.attention(q, kp, vp, out=out)
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b) * 1e3)
+        rc, word = sess.check_device()
+        if rc != 0:
+            raise RuntimeError(f"device error word {word:#x}")
+        res.append((float(np.median(times)), sess))
+    return res
 
 
 def predict(plan, params):
@@ -105,7 +115,7 @@ def fit(records, x0=None):
     """records: [(plan, measured_us)] -> params dict (least squares on logs)."""
     from scipy.optimize import least_squares
     names = msa.COST_PARAM_NAMES
-    x0 = np.asarray(x0 if x0 is not None else [8.0, 2.0, 1.3, 4.0, 1.0, 0.02, 2.0], float)
+    x0 = np.asarray(x0 if x0 is not None else [5.0, 2.0, 6400.0, 80.0, 5.0, 1.0, 0.02, 5.0], float)
 
     def resid(x):
         p = dict(zip(names, x))
@@ -134,13 +144,16 @@ def main(argv=None):
     keep = {"train": [], "validation": []}
     for which, wls in (("train", training_set()), ("validation", validation_set())):
         for name, wl in wls:
-            us, sess = measure(wl, dev, reps=args.reps)
-            info = sess.info
-            rows[which].append({"workload": name, "measured_us": round(us, 2), "items": info["num_items"],
-                                "decode_kv_bytes": info["decode_kv_bytes"], "prefill_flops": info["prefill_flops"]})
-            keep[which].append((sess, us))
+            for us, sess in measure(wl, dev, reps=args.reps):
+                info = sess.info
+                rows[which].append({"workload": name, "decode_split": info["decode_split"],
+                                    "prefill_split": info["prefill_split"], "measured_us": round(us, 2),
+                                    "items": info["num_items"], "decode_kv_bytes": info["decode_kv_bytes"],
+                                    "prefill_flops": info["prefill_flops"]})
+                keep[which].append((sess, us))
+                print(f"{which:10s} {name:12s} split {info['decode_split']:.1f}/{info['prefill_split']:.1f} "
+                      f"{us:10.1f} us  items {info['num_items']}", file=sys.stderr)
             torch.cuda.empty_cache()
-            print(f"{which:10s} {name:12s} {us:10.1f} us  items {info['num_items']}", file=sys.stderr)
     train = [(s.plan, t) for s, t in keep["train"]]
     val = [(s.plan, t) for s, t in keep["validation"]]
     params = fit(train)

@@ -27,7 +27,19 @@ int msa_plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks_p
                     const int32_t* q_ranges, int32_t num_sms, msa_plan_t* out) {
     try {
         return msa::plan_create(dims, num_seqs, max_blocks_per_seq, block_table, seq_lens, q_range_indptr,
-                                q_ranges, num_sms, out);
+                                q_ranges, num_sms, nullptr, out);
+    } catch (...) {
+        if (out) *out = nullptr;
+        return MSA_ERR_INVALID_ARG;
+    }
+}
+
+int msa_plan_create_ex(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks_per_seq,
+                       const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_range_indptr,
+                       const int32_t* q_ranges, const msa_plan_options* opts, msa_plan_t* out) {
+    try {
+        return msa::plan_create(dims, num_seqs, max_blocks_per_seq, block_table, seq_lens, q_range_indptr,
+                                q_ranges, opts ? opts->num_sms : 0, opts, out);
     } catch (...) {
         if (out) *out = nullptr;
         return MSA_ERR_INVALID_ARG;

@@ -5,8 +5,10 @@
 // recompute cost and hit rate against the attention kernel's expected
 // latency (MSA paper abstract; AsymCache explainer, "核心方法 2" and "3").
 // The model below prices each work item from its shape and replays the
-// kernel's work queue over the launch's CTAs.
+// kernel's work queue over the launch's CTAs, with the decode streams
+// sharing HBM bandwidth.
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <queue>
 #include <utility>
@@ -19,32 +21,181 @@ namespace {
 using msa::kBlock;
 using msa::kTileKeys;
 
-// TMA boxes the producer issues for the tiles of one item beyond one per
-// tile: a full 128-key window inside one segment is one rectangle; any other
-// tile is fetched per 16-key block of each segment piece.
-int64_t extra_boxes(const msa_plan_s* P, const msa::Item& it) {
-    const int32_t rb = P->run_indptr[it.seq + 1];
-    int32_t r = it.first_run;
-    int64_t extra = 0;
-    for (int32_t t0 = it.kb; t0 < it.ke; t0 += kTileKeys) {
-        const int32_t t1 = std::min(t0 + kTileKeys, it.ke);
-        int64_t boxes = 0;
-        int32_t cur = t0;
-        while (cur < t1 && r < rb) {
-            const msa::Run& R = P->runs[r];
-            const int32_t rend = R.log_start + R.n_tok;
-            if (cur >= rend) { ++r; continue; }
-            const int32_t pend = std::min(t1, rend);
-            if (cur == t0 && pend - cur == kTileKeys) boxes += 1;
-            else boxes += (pend - cur + kBlock - 1) / kBlock;
-            cur = pend;
-        }
-        if (boxes > 1) extra += boxes - 1;
+// TMA boxes the producer issues for the tile [t0, t1) of sequence `seq`
+// beyond one: a full 128-key window inside one segment is one rectangle; any
+// other tile is fetched per 16-key block of each segment piece.
+int64_t tile_extra_boxes(const msa_plan_s* P, int32_t seq, int32_t t0, int32_t t1) {
+    const int32_t ra = P->run_indptr[seq], rb = P->run_indptr[seq + 1];
+    // first run that ends after t0 (runs are in logical order)
+    int32_t lo = ra, hi = rb;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi) / 2;
+        if (P->runs[mid].log_start + P->runs[mid].n_tok <= t0) lo = mid + 1;
+        else hi = mid;
     }
-    return extra;
+    int64_t boxes = 0;
+    int32_t cur = t0;
+    for (int32_t r = lo; r < rb && cur < t1; ++r) {
+        const msa::Run& R = P->runs[r];
+        const int32_t pend = std::min(t1, R.log_start + R.n_tok);
+        if (pend <= cur) continue;
+        if (cur == t0 && pend - cur == kTileKeys) boxes += 1;
+        else boxes += (pend - cur + kBlock - 1) / kBlock;
+        cur = pend;
+    }
+    return boxes > 1 ? boxes - 1 : 0;
+}
+
+// Per sequence, prefix sums of the extra boxes of its full 128-key tiles:
+// items start on tile boundaries, so an item's count is a difference of two
+// prefix sums plus, when its end is not on a boundary, its partial last tile.
+struct BoxCounts {
+    std::vector<std::vector<int64_t>> prefix;  // [seq][i] = sum over full tiles j < i
+    explicit BoxCounts(const msa_plan_s* P) : prefix(P->seq_lens.size()) {
+        for (size_t s = 0; s < P->seq_lens.size(); ++s) {
+            const int32_t full = P->seq_lens[s] / kTileKeys;
+            prefix[s].assign((size_t)full + 1, 0);
+            for (int32_t i = 0; i < full; ++i)
+                prefix[s][i + 1] = prefix[s][i] + tile_extra_boxes(P, (int32_t)s, i * kTileKeys, (i + 1) * kTileKeys);
+        }
+    }
+    int64_t item(const msa_plan_s* P, const msa::Item& it) const {
+        if (it.ke <= it.kb) return 0;
+        const std::vector<int64_t>& pf = prefix[it.seq];
+        const int32_t i0 = it.kb / kTileKeys, i1 = it.ke / kTileKeys;  // full tiles [i0, i1)
+        int64_t n = pf[std::min<size_t>(i1, pf.size() - 1)] - pf[std::min<size_t>(i0, pf.size() - 1)];
+        if (it.ke % kTileKeys) n += tile_extra_boxes(P, it.seq, i1 * kTileKeys, it.ke);
+        return n;
+    }
+};
+
+bool params_ok(const msa_cost_params* c) {
+    const double prm[8] = {c->launch_us, c->dec_item_us, c->dec_gbs, c->dec_cta_gbs,
+                           c->pre_item_us, c->pre_tile_us, c->box_us, c->merge_us};
+    for (double v : prm)
+        if (!(v >= 0.0) || !std::isfinite(v)) return false;
+    return true;
+}
+
+int estimate(const msa_plan_s* P, const msa_cost_params* c, const BoxCounts& box_counts, msa_cost_estimate* e) {
+    const size_t n = P->items.size();
+    msa_cost_estimate out{};
+    std::vector<double> fixed(n, 0.0), bytes(n, 0.0);
+    const double tile_bytes = 2.0 * kTileKeys * P->dims.head_dim * 2.0;  // K and V, bf16
+    for (size_t i = 0; i < n; ++i) {
+        const msa::Item& it = P->items[i];
+        const msa::Group& g = P->groups[it.group];
+        const int64_t tiles = it.pad;
+        const int64_t boxes = box_counts.item(P, it);
+        const bool split = g.n_parts > 1;
+        double f;
+        if (it.kind == msa::kDecode) {
+            f = c->dec_item_us;
+            bytes[i] = tile_bytes * (double)tiles;
+            out.decode_tiles += tiles;
+            out.stream_bytes += (int64_t)bytes[i];
+        } else {
+            f = c->pre_item_us + c->pre_tile_us * (double)(tiles * g.pad);
+            out.prefill_tile_heads += tiles * g.pad;
+        }
+        f += c->box_us * (double)boxes + (split ? c->merge_us : 0.0);
+        fixed[i] = f;
+        out.extra_boxes += boxes;
+        out.n_split_items += split ? 1 : 0;
+        out.fixed_us += f;
+    }
+    if (out.stream_bytes > 0 && (c->dec_gbs <= 0.0 || c->dec_cta_gbs <= 0.0)) return MSA_ERR_INVALID_ARG;
+
+    // Event-by-event replay.  A CTA's item is a fixed phase (time) then a
+    // stream phase (bytes); a CTA that finishes takes the next item of the
+    // order at once.  All streaming CTAs advance at the same rate, so their
+    // progress is one clock `sigma` (bytes per streaming CTA so far) and a
+    // CTA's stream ends when sigma reaches its target: two min-heaps, one in
+    // time (fixed phases) and one in sigma (streams).  Which of several CTAs
+    // freed at the same instant takes which item does not change the finish
+    // times, the CTAs being alike.
+    using Ev = std::pair<double, int32_t>;
+    std::priority_queue<Ev, std::vector<Ev>, std::greater<Ev>> fixed_q, stream_q;
+    const int32_t grid = std::max(1, P->grid);
+    std::vector<int32_t> item(grid, -1);
+    size_t next = 0;
+    double t = 0.0, sigma = 0.0;
+    auto rate_of = [&](size_t n_stream) {
+        return n_stream > 0 ? std::min(c->dec_cta_gbs, c->dec_gbs / (double)n_stream) * 1e3 : 0.0;  // B/us
+    };
+    // start the next item on CTA b at time t (its fixed phase)
+    auto take = [&](int32_t b) {
+        if (next >= P->order.size()) { item[b] = -1; return; }
+        item[b] = P->order[next++];
+        fixed_q.push({t + fixed[item[b]], b});
+    };
+    for (int32_t b = 0; b < grid; ++b) take(b);
+    while (!fixed_q.empty() || !stream_q.empty()) {
+        const double r = rate_of(stream_q.size());
+        const double t_fixed = fixed_q.empty() ? INFINITY : fixed_q.top().first;
+        const double t_stream = stream_q.empty() ? INFINITY : t + (stream_q.top().first - sigma) / r;
+        if (t_fixed <= t_stream) {
+            const int32_t b = fixed_q.top().second;
+            fixed_q.pop();
+            if (r > 0.0) sigma += (t_fixed - t) * r;
+            t = t_fixed;
+            if (bytes[item[b]] > 0.0) stream_q.push({sigma + bytes[item[b]], b});
+            else take(b);
+        } else {
+            const int32_t b = stream_q.top().second;
+            sigma = stream_q.top().first;
+            stream_q.pop();
+            t = t_stream;
+            take(b);
+        }
+    }
+    out.makespan_us = t;
+    out.time_us = c->launch_us + t;
+    out.n_items = (int64_t)n;
+    out.decode_kv_bytes = P->info.decode_kv_bytes;
+    out.prefill_flops = P->info.prefill_flops;
+    *e = out;
+    return MSA_OK;
 }
 
 }  // namespace
+
+namespace msa {
+
+// Adaptive chunking (AsymCache explainer, "核心方法 3": chunk sizes adjusted
+// so the attention kernel stays busy without per-chunk overheads dominating):
+// the decode split, then the prefill split, with the lowest expected launch
+// time under the latency model.
+void choose_split(msa_plan_s* P, const std::vector<Pending>& pend, const msa_cost_params& c, double* dec_split,
+                  double* pre_split) {
+    bool has[2] = {false, false};
+    for (auto& pd : pend) has[pd.g.kind] = true;
+    const BoxCounts box_counts(P);
+    auto time_of = [&](double d, double p) {
+        split_items(P, pend, d, p);
+        msa_cost_estimate e{};
+        return estimate(P, &c, box_counts, &e) == MSA_OK ? e.time_us : INFINITY;
+    };
+    static const double kDec[] = {1.0, 1.5, 2.0, 3.0, 4.0};
+    static const double kPre[] = {1.0, 2.0, 4.0};
+    double best = INFINITY;
+    if (has[kDecode]) {
+        const double p = *pre_split;
+        for (double d : kDec) {
+            const double t = time_of(d, p);
+            if (t < best) { best = t; *dec_split = d; }
+        }
+    }
+    if (has[kPrefill]) {
+        const double d = *dec_split;
+        for (double p : kPre) {
+            const double t = time_of(d, p);
+            if (t < best) { best = t; *pre_split = p; }
+        }
+    }
+}
+
+}  // namespace msa
 
 extern "C" {
 
@@ -58,50 +209,9 @@ int msa_plan_get_order(msa_plan_t plan, int32_t* order, int32_t* n_items) {
 
 int msa_plan_estimate(msa_plan_t plan, const msa_cost_params* c, msa_cost_estimate* e) {
     if (!plan || !c || !e) return MSA_ERR_INVALID_ARG;
-    const msa_plan_s* P = plan;
-    msa_cost_estimate out{};
-    std::vector<double> cost(P->items.size(), 0.0);
-    for (size_t i = 0; i < P->items.size(); ++i) {
-        const msa::Item& it = P->items[i];
-        const msa::Group& g = P->groups[it.group];
-        const int64_t tiles = it.pad;
-        const int64_t boxes = extra_boxes(P, it);
-        const bool split = g.n_parts > 1;
-        double ci;
-        if (it.kind == msa::kDecode) {
-            ci = c->dec_item_us + c->dec_tile_us * (double)tiles;
-            out.decode_tiles += tiles;
-        } else {
-            ci = c->pre_item_us + c->pre_tile_us * (double)(tiles * g.pad);
-            out.prefill_tile_heads += tiles * g.pad;
-        }
-        ci += c->box_us * (double)boxes + (split ? c->merge_us : 0.0);
-        out.extra_boxes += boxes;
-        out.n_split_items += split ? 1 : 0;
-        cost[i] = ci;
-        out.busy_us += ci;
-    }
-    // replay the queue: the earliest-free CTA (lowest index on ties) takes
-    // the next item of the plan's order
-    using Slot = std::pair<double, int32_t>;
-    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
-    const int32_t grid = std::max(1, P->grid);
-    for (int32_t b = 0; b < grid; ++b) free_at.push({0.0, b});
-    double makespan = 0.0;
-    for (int32_t idx : P->order) {
-        Slot s = free_at.top();
-        free_at.pop();
-        s.first += cost[idx];
-        if (s.first > makespan) makespan = s.first;
-        free_at.push(s);
-    }
-    out.makespan_us = makespan;
-    out.time_us = c->launch_us + makespan;
-    out.n_items = (int64_t)P->items.size();
-    out.decode_kv_bytes = P->info.decode_kv_bytes;
-    out.prefill_flops = P->info.prefill_flops;
-    *e = out;
-    return MSA_OK;
+    if (!params_ok(c)) return MSA_ERR_INVALID_ARG;
+    const BoxCounts box_counts(plan);
+    return estimate(plan, c, box_counts, e);
 }
 
 }  // extern "C"

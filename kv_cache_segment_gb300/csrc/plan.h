@@ -37,9 +37,35 @@ struct msa_plan_s {
 
 namespace msa {
 
+// Default split factors (a part of a split group holds about the work per
+// CTA divided by these): measured on GB300, parts of about a third (decode)
+// and a quarter (prefill) of a CTA's share beat finer cuts on every bench
+// workload; each part costs a partial write and a share of the merge, each
+// item a pipeline start and an epilogue.
+constexpr double kDefaultDecodeSplit = 3.0;
+constexpr double kDefaultPrefillSplit = 4.0;
+
+// An output group before its key range is cut into work items.
+struct Pending {
+    Group g;
+    int32_t ke;     // key range [0, ke)
+    int64_t tiles;  // 128-key tiles of [0, ke)
+};
+
+// Cut every group's key range into parts and order the items (longest
+// first).  A part holds about (work per CTA) / split of a group's tiles:
+// `dec_split` for decode groups, `pre_split` for prefill groups.  Rebuilds
+// P->groups, items, order and the partial-slot counts from scratch.
+void split_items(msa_plan_s* P, const std::vector<Pending>& pend, double dec_split, double pre_split);
+
+// Pick the split factors with the lowest expected launch time under the
+// latency model (costmodel.cpp); leaves P's items unspecified.
+void choose_split(msa_plan_s* P, const std::vector<Pending>& pend, const msa_cost_params& c, double* dec_split,
+                  double* pre_split);
+
 int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks, const int32_t* table,
                 const int32_t* seq_lens, const int32_t* q_range_indptr, const int32_t* q_ranges,
-                int32_t num_sms, msa_plan_s** out);
+                int32_t num_sms, const msa_plan_options* opts, msa_plan_s** out);
 void build_image(msa_plan_s* P);
 int device_sm_count();
 

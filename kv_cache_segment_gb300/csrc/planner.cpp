@@ -54,15 +54,90 @@ static int32_t run_of(const Run* runs, int32_t r0, int32_t r1, int32_t k) {
     return lo;
 }
 
+// Cut every group's key range into parts and order the items (longest
+// first).  A part holds about (work per CTA) / split of a group's tiles:
+// `dec_split` for decode groups, `pre_split` for prefill groups.  Rebuilds
+// P->groups, items, order and the partial-slot counts from scratch.
+void split_items(msa_plan_s* P, const std::vector<Pending>& pend, double dec_split, double pre_split) {
+    P->groups.clear();
+    P->items.clear();
+    P->order.clear();
+    P->n_dec_slots = 0;
+    P->n_pre_slots = 0;
+    // Cost of an item ~ its KV tiles (a decode tile moves 2*128*D*2 bytes, a
+    // prefill tile does 4*128*128*D flops; on GB300 both take ~1.3-1.5 us per
+    // SM) plus a fixed per-item cost.
+    const double w_tile[2] = {1.1, 1.0};
+    const double w_item[2] = {0.5, 2.0};
+    double total = 0.0;
+    for (auto& pd : pend) total += pd.tiles * w_tile[pd.g.kind] + w_item[pd.g.kind];
+    const double per_cta = total / P->grid;
+    const int64_t min_tiles[2] = {4, 8};
+
+    std::vector<double> cost;
+    for (size_t gi = 0; gi < pend.size(); ++gi) {
+        const Pending& pd = pend[gi];
+        const int32_t kind = pd.g.kind;
+        const double per_item = per_cta / (kind == kDecode ? dec_split : pre_split);
+        int64_t chunk = std::max<int64_t>(min_tiles[kind], (int64_t)std::ceil(per_item / w_tile[kind]));
+        int32_t parts = (int32_t)std::max<int64_t>(1, (pd.tiles + chunk - 1) / chunk);
+        const int32_t s = pd.g.seq;
+        const int32_t ra = P->run_indptr[s], rb = P->run_indptr[s + 1];
+        Group g = pd.g;
+        g.n_parts = parts;
+        const int32_t gid = (int32_t)P->groups.size();
+        if (parts > 1) {
+            if (kind == kDecode) { g.slot = P->n_dec_slots; P->n_dec_slots += parts; }
+            else { g.slot = P->n_pre_slots; P->n_pre_slots += parts; }
+        }
+        P->groups.push_back(g);
+        // cut the key range into `parts` runs of whole tiles
+        if (pd.ke <= 0 || ra == rb) {
+            Item it{gid, 0, 0, ra, 0, kind, s, 0};
+            P->items.push_back(it);
+            cost.push_back(w_item[kind]);
+            continue;
+        }
+        const int64_t per = (pd.tiles + parts - 1) / parts;
+        int32_t part = 0;
+        for (int64_t t = 0; t < pd.tiles; t += per) {
+            const int32_t kb = (int32_t)(t * kTileKeys);
+            const int32_t ke = (int32_t)std::min<int64_t>((t + per) * kTileKeys, pd.ke);
+            Item it{gid, kb, ke, run_of(P->runs.data(), ra, rb, kb), part, kind, s, 0};
+            P->items.push_back(it);
+            cost.push_back(std::min<int64_t>(per, pd.tiles - t) * w_tile[kind] + w_item[kind]);
+            ++part;
+        }
+        P->groups[gid].n_parts = part;
+        if (part == 1) P->groups[gid].slot = -1;
+    }
+
+    // KV tiles of every item (the kernels walk exactly these)
+    for (auto& it : P->items) it.pad = (int32_t)count_tiles(it.kb, it.ke);
+
+    // One global queue, longest first: every CTA of the persistent launch
+    // takes the next item when it is free (list scheduling in LPT order), so
+    // the load balances itself on the device.  Equal-cost items stay in
+    // generation order (sequence, tile, head), which keeps CTAs that run at
+    // the same time on the same sequences' K/V in L2.
+    const int32_t n_items = (int32_t)P->items.size();
+    P->order.resize(n_items);
+    for (int32_t i = 0; i < n_items; ++i) P->order[i] = i;
+    std::stable_sort(P->order.begin(), P->order.end(), [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
+}
+
 int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
                 const int32_t* table, const int32_t* seq_lens, const int32_t* q_range_indptr,
-                const int32_t* q_ranges, int32_t num_sms, msa_plan_s** out) {
+                const int32_t* q_ranges, int32_t num_sms, const msa_plan_options* opts, msa_plan_s** out) {
     auto t0 = std::chrono::steady_clock::now();
     if (!out) return MSA_ERR_INVALID_ARG;
     *out = nullptr;
     int rc = validate_dims(dims);
     if (rc != MSA_OK) return rc;
     if (num_seqs < 0 || max_blocks < 0 || num_sms < 0) return MSA_ERR_INVALID_ARG;
+    if (opts && (!(opts->decode_split >= 0.0) || !(opts->prefill_split >= 0.0) ||
+                 !std::isfinite(opts->decode_split) || !std::isfinite(opts->prefill_split)))
+        return MSA_ERR_INVALID_ARG;
     if (num_seqs > 0 && (!seq_lens || !q_range_indptr)) return MSA_ERR_INVALID_ARG;
     if (num_seqs > 0 && max_blocks > 0 && !table) return MSA_ERR_INVALID_ARG;
     if (num_sms == 0) {
@@ -133,7 +208,6 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
     // ---- output groups ----------------------------------------------------
     // A sequence's trailing rows go to the GQA-packed decode path when they
     // number at most kDecRows / G; everything else is cut into 128-row tiles.
-    struct Pending { Group g; int32_t ke; int64_t tiles; };
     std::vector<Pending> pend;
     double prefill_flops = 0.0;
     int64_t dec_kv = 0, dec_qo = 0;
@@ -182,73 +256,13 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
         }
     }
 
-    // ---- split long key ranges, cost model ---------------------------------
-    // Cost of an item ~ its KV tiles (a decode tile moves 2*128*D*2 bytes, a
-    // prefill tile does 4*128*128*D flops; on GB300 both take ~1.3-1.5 us per
-    // SM) plus a fixed per-item cost.
-    const double w_tile[2] = {1.1, 1.0};
-    const double w_item[2] = {0.5, 2.0};
-    double total = 0.0;
-    for (auto& pd : pend) total += pd.tiles * w_tile[pd.g.kind] + w_item[pd.g.kind];
+    // ---- work items and their order ----------------------------------------
     P->grid = std::max(1, num_sms);
-    const double per_cta = total / P->grid;
-    const int64_t min_tiles[2] = {4, 8};
-
-    std::vector<double> cost;
-    for (size_t gi = 0; gi < pend.size(); ++gi) {
-        Pending& pd = pend[gi];
-        const int32_t kind = pd.g.kind;
-        // Each part of a split group costs a partial write and a share of the
-        // merge, and each item a pipeline start and an epilogue; measured on
-        // GB300, parts of about a third (decode) and a quarter (prefill) of
-        // a CTA's share beat finer cuts on every bench workload.
-        const double per_item = kind == kDecode ? per_cta / 3.0 : per_cta / 4.0;
-        int64_t chunk = std::max<int64_t>(min_tiles[kind], (int64_t)std::ceil(per_item / w_tile[kind]));
-        int32_t parts = (int32_t)std::max<int64_t>(1, (pd.tiles + chunk - 1) / chunk);
-        const int32_t s = pd.g.seq;
-        const int32_t ra = P->run_indptr[s], rb = P->run_indptr[s + 1];
-        Group g = pd.g;
-        g.n_parts = parts;
-        const int32_t gid = (int32_t)P->groups.size();
-        if (parts > 1) {
-            if (kind == kDecode) { g.slot = P->n_dec_slots; P->n_dec_slots += parts; }
-            else { g.slot = P->n_pre_slots; P->n_pre_slots += parts; }
-        }
-        P->groups.push_back(g);
-        // cut the key range into `parts` runs of whole tiles
-        if (pd.ke <= 0 || ra == rb) {
-            Item it{gid, 0, 0, ra, 0, kind, s, 0};
-            P->items.push_back(it);
-            cost.push_back(w_item[kind]);
-            continue;
-        }
-        const int64_t per = (pd.tiles + parts - 1) / parts;
-        int32_t part = 0;
-        for (int64_t t = 0; t < pd.tiles; t += per) {
-            const int32_t kb = (int32_t)(t * kTileKeys);
-            const int32_t ke = (int32_t)std::min<int64_t>((t + per) * kTileKeys, pd.ke);
-            Item it{gid, kb, ke, run_of(P->runs.data(), ra, rb, kb), part, kind, s, 0};
-            P->items.push_back(it);
-            cost.push_back(std::min<int64_t>(per, pd.tiles - t) * w_tile[kind] + w_item[kind]);
-            ++part;
-        }
-        P->groups[gid].n_parts = part;
-        if (part == 1) P->groups[gid].slot = -1;
-    }
-
-    // KV tiles of every item (the kernels walk exactly these)
-    for (auto& it : P->items) it.pad = (int32_t)count_tiles(it.kb, it.ke);
-
-    // ---- processing order --------------------------------------------------
-    // One global queue, longest first: every CTA of the persistent launch
-    // takes the next item when it is free (list scheduling in LPT order), so
-    // the load balances itself on the device.  Equal-cost items stay in
-    // generation order (sequence, tile, head), which keeps CTAs that run at
-    // the same time on the same sequences' K/V in L2.
+    double dec_split = opts && opts->decode_split > 0.0 ? opts->decode_split : kDefaultDecodeSplit;
+    double pre_split = opts && opts->prefill_split > 0.0 ? opts->prefill_split : kDefaultPrefillSplit;
+    if (opts && opts->choose_with) choose_split(P, pend, *opts->choose_with, &dec_split, &pre_split);
+    split_items(P, pend, dec_split, pre_split);
     const int32_t n_items = (int32_t)P->items.size();
-    P->order.resize(n_items);
-    for (int32_t i = 0; i < n_items; ++i) P->order[i] = i;
-    std::stable_sort(P->order.begin(), P->order.end(), [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
 
     // ---- info ---------------------------------------------------------------
     msa_plan_info& I = P->info;
@@ -266,6 +280,8 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
     I.decode_qo_bytes = dec_qo;
     I.prefill_flops = prefill_flops;
     I.max_pool_row = P->max_pool_row;
+    I.decode_split = dec_split;
+    I.prefill_split = pre_split;
 
     build_image(P);
     I.host_plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();

@@ -51,25 +51,32 @@ class msa_plan_info(ctypes.Structure):
                 ("num_prefill_rows", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("decode_kv_bytes", ctypes.c_int64), ("decode_qo_bytes", ctypes.c_int64),
                 ("prefill_flops", ctypes.c_double), ("max_pool_row", ctypes.c_int64),
-                ("host_plan_us", ctypes.c_double)]
+                ("host_plan_us", ctypes.c_double), ("decode_split", ctypes.c_double),
+                ("prefill_split", ctypes.c_double)]
 
 
 class msa_cost_params(ctypes.Structure):
     _fields_ = [("launch_us", ctypes.c_double), ("dec_item_us", ctypes.c_double),
-                ("dec_tile_us", ctypes.c_double), ("pre_item_us", ctypes.c_double),
-                ("pre_tile_us", ctypes.c_double), ("box_us", ctypes.c_double),
-                ("merge_us", ctypes.c_double)]
+                ("dec_gbs", ctypes.c_double), ("dec_cta_gbs", ctypes.c_double),
+                ("pre_item_us", ctypes.c_double), ("pre_tile_us", ctypes.c_double),
+                ("box_us", ctypes.c_double), ("merge_us", ctypes.c_double)]
 
 
 class msa_cost_estimate(ctypes.Structure):
     _fields_ = [("time_us", ctypes.c_double), ("makespan_us", ctypes.c_double),
-                ("busy_us", ctypes.c_double), ("n_items", ctypes.c_int64),
+                ("fixed_us", ctypes.c_double), ("n_items", ctypes.c_int64),
                 ("n_split_items", ctypes.c_int64), ("decode_tiles", ctypes.c_int64),
                 ("prefill_tile_heads", ctypes.c_int64), ("extra_boxes", ctypes.c_int64),
-                ("decode_kv_bytes", ctypes.c_int64), ("prefill_flops", ctypes.c_double)]
+                ("stream_bytes", ctypes.c_int64), ("decode_kv_bytes", ctypes.c_int64),
+                ("prefill_flops", ctypes.c_double)]
 
 
 COST_PARAM_NAMES = tuple(name for name, _ in msa_cost_params._fields_)
+
+
+class msa_plan_options(ctypes.Structure):
+    _fields_ = [("num_sms", ctypes.c_int32), ("decode_split", ctypes.c_double),
+                ("prefill_split", ctypes.c_double), ("choose_with", ctypes.POINTER(msa_cost_params))]
 
 _lib = None
 
@@ -86,6 +93,8 @@ def load(path: str = LIB_PATH):
     vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     sigs = {
         "msa_plan_create": ([ctypes.POINTER(msa_dims), i32, i32, vp, vp, vp, vp, i32, ctypes.POINTER(vp)], ctypes.c_int),
+        "msa_plan_create_ex": ([ctypes.POINTER(msa_dims), i32, i32, vp, vp, vp, vp, ctypes.POINTER(msa_plan_options),
+                                ctypes.POINTER(vp)], ctypes.c_int),
         "msa_plan_workspace_bytes": ([vp, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
         "msa_plan_upload": ([vp, vp, ctypes.c_size_t, vp], ctypes.c_int),
         "msa_plan_get_runs": ([vp, i32, vp, ctypes.POINTER(i32)], ctypes.c_int),
@@ -161,6 +170,30 @@ def msa_plan_create(dims: msa_dims, block_table, seq_lens, q_range_indptr, q_ran
                              indptr.ctypes.data, ranges.ctypes.data if ranges.size else None, int(num_sms),
                              ctypes.byref(plan))
     _check(rc, "msa_plan_create")
+    return plan.value
+
+
+def msa_plan_create_ex(dims: msa_dims, block_table, seq_lens, q_range_indptr, q_ranges, num_sms: int = 0,
+                       decode_split: float = 0.0, prefill_split: float = 0.0, choose_with=None):
+    """msa_plan_create with explicit split factors, or (choose_with = a dict of
+    msa_cost_params) factors chosen by the latency model."""
+    lib = load()
+    table = np.ascontiguousarray(block_table, np.int32)
+    if table.ndim != 2:
+        table = table.reshape(len(seq_lens), -1)
+    lens = np.ascontiguousarray(seq_lens, np.int32)
+    indptr = np.ascontiguousarray(q_range_indptr, np.int32)
+    ranges = np.ascontiguousarray(q_ranges, np.int32).reshape(-1, 2)
+    params = None
+    if choose_with is not None:
+        params = msa_cost_params(*[float(choose_with[k]) for k in COST_PARAM_NAMES])
+    opts = msa_plan_options(int(num_sms), float(decode_split), float(prefill_split),
+                            ctypes.pointer(params) if params is not None else None)
+    plan = ctypes.c_void_p()
+    rc = lib.msa_plan_create_ex(ctypes.byref(dims), len(lens), table.shape[1], table.ctypes.data, lens.ctypes.data,
+                                indptr.ctypes.data, ranges.ctypes.data if ranges.size else None, ctypes.byref(opts),
+                                ctypes.byref(plan))
+    _check(rc, "msa_plan_create_ex")
     return plan.value
 
 

@@ -13,10 +13,15 @@ from . import msa
 
 class MsaSession:
     def __init__(self, num_q_heads, num_kv_heads, head_dim, block_table, seq_lens, q_range_indptr, q_ranges,
-                 device="cuda", num_sms=0, softmax_scale=None, stream=None):
+                 device="cuda", num_sms=0, softmax_scale=None, stream=None, decode_split=0.0, prefill_split=0.0,
+                 choose_with=None):
         import torch
         self.dims = msa.make_dims(num_q_heads, num_kv_heads, head_dim, 16, softmax_scale)
-        self.plan = msa.msa_plan_create(self.dims, block_table, seq_lens, q_range_indptr, q_ranges, num_sms)
+        if decode_split or prefill_split or choose_with is not None:
+            self.plan = msa.msa_plan_create_ex(self.dims, block_table, seq_lens, q_range_indptr, q_ranges, num_sms,
+                                               decode_split, prefill_split, choose_with)
+        else:
+            self.plan = msa.msa_plan_create(self.dims, block_table, seq_lens, q_range_indptr, q_ranges, num_sms)
         self.info = msa.msa_plan_get_info(self.plan)
         self.ws_bytes = msa.msa_plan_workspace_bytes(self.plan)
         self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
@@ -24,9 +29,11 @@ class MsaSession:
         msa.msa_plan_upload(self.plan, self.workspace, self.ws_bytes, self._stream())
 
     @classmethod
-    def from_workload(cls, wl, device="cuda", num_sms=0, stream=None):
+    def from_workload(cls, wl, device="cuda", num_sms=0, stream=None, **plan_options):
+        """plan_options: decode_split, prefill_split, choose_with (see msa_plan_create_ex)."""
         return cls(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_table, wl.seq_lens, wl.q_range_indptr,
-                   wl.q_ranges_flat, device=device, num_sms=num_sms, softmax_scale=wl.scale, stream=stream)
+                   wl.q_ranges_flat, device=device, num_sms=num_sms, softmax_scale=wl.scale, stream=stream,
+                   **plan_options)
 
     def _stream(self):
         import torch

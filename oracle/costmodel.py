@@ -6,17 +6,19 @@ kernel's expected latency (MSA paper abstract; AsymCache explainer, "æ ¸å¿ƒæ–¹æ³
 2" and "3").  The model prices each work item and replays the kernel's work
 queue:
 
-  cost(item) = dec_item + dec_tile * tiles                    (decode)
-             | pre_item + pre_tile * tiles * heads             (prefill)
-             + box * extra_boxes + merge * [group split into parts]
-
+  fixed phase (us)   dec_item                                 (decode)
+                   | pre_item + pre_tile * tiles * heads      (prefill)
+                     + box * extra_boxes + merge * [group split into parts]
+  stream phase (B)   decode only: tiles * 128 * D * 2 * 2 (K and V, bf16),
+                     at min(dec_cta, dec / n_streaming) GB/s per CTA
   tiles        128-key windows [kb + 128 i, min(kb + 128 (i+1), ke))
   extra_boxes  per tile, the TMA boxes beyond one: a full 128-key window
                inside one segment is one box, any other tile one box per
                16-key block of each segment piece it touches
-  makespan     items handed out in the plan's order, each to the CTA that is
-               free first (lowest index on ties); the last finish time
-  time         launch + makespan
+  replay       CTAs 0..grid-1 take the first items of the plan's order; when
+               a CTA's phases are done it takes the next item; between
+               events every CTA advances at its phase's rate
+  time         launch + the time the last CTA finishes
 
 Segments come from oracle.segments (the brute-force splitter over the block
 table), never from the library; the work list and its order are the plan's
@@ -49,7 +51,7 @@ def _boxes(segs, t0, t1):
     return boxes
 
 
-def estimate(items, order, block_table, seq_lens, grid, params):
+def estimate(items, order, block_table, seq_lens, grid, params, head_dim):
     """items: rows (kind, seq, head, heads, row0, nrows, kb, ke, part) as
     msa_plan_get_items returns them; order: msa_plan_get_order; params: dict
     of the msa_cost_params names.  Returns a dict like msa_plan_estimate."""
@@ -58,9 +60,10 @@ def estimate(items, order, block_table, seq_lens, grid, params):
     for (kind, seq, head, heads, row0, nrows, kb, ke, part) in items:
         key = (kind, seq, head, row0)
         parts[key] = parts.get(key, 0) + 1
-    cost = []
+    fixed, stream = [], []
     out = {"n_items": len(items), "n_split_items": 0, "decode_tiles": 0, "prefill_tile_heads": 0,
-           "extra_boxes": 0, "busy_us": 0.0}
+           "extra_boxes": 0, "stream_bytes": 0, "fixed_us": 0.0}
+    tile_bytes = 2.0 * TILE * head_dim * 2.0
     for (kind, seq, head, heads, row0, nrows, kb, ke, part) in items:
         if seq not in segs:
             segs[seq] = _token_segments(block_table[seq], int(seq_lens[seq]))
@@ -74,24 +77,54 @@ def estimate(items, order, block_table, seq_lens, grid, params):
             t0 += TILE
         split = parts[(kind, seq, head, row0)] > 1
         if kind == 0:
-            c = params["dec_item_us"] + params["dec_tile_us"] * tiles
+            f = params["dec_item_us"]
+            b = tile_bytes * tiles
             out["decode_tiles"] += tiles
         else:
-            c = params["pre_item_us"] + params["pre_tile_us"] * tiles * heads
+            f = params["pre_item_us"] + params["pre_tile_us"] * tiles * heads
+            b = 0.0
             out["prefill_tile_heads"] += tiles * heads
-        c += params["box_us"] * extra + (params["merge_us"] if split else 0.0)
+        f += params["box_us"] * extra + (params["merge_us"] if split else 0.0)
         out["extra_boxes"] += extra
         out["n_split_items"] += 1 if split else 0
-        out["busy_us"] += c
-        cost.append(c)
-    free = [0.0] * max(1, int(grid))
-    makespan = 0.0
-    for idx in order:
-        b = min(range(len(free)), key=lambda i: (free[i], i))
-        free[b] += cost[idx]
-        makespan = max(makespan, free[b])
-    out["makespan_us"] = makespan
-    out["time_us"] = params["launch_us"] + makespan
+        out["stream_bytes"] += int(b)
+        out["fixed_us"] += f
+        fixed.append(f)
+        stream.append(b)
+    n_cta = max(1, int(grid))
+    queue = list(order)
+    cur = [None] * n_cta          # [item, phase, left] per CTA
+    for c in range(n_cta):
+        cur[c] = [queue.pop(0), 0, None] if queue else None
+        if cur[c] is not None:
+            cur[c][2] = fixed[cur[c][0]]
+    t = 0.0
+    while True:
+        for c in range(n_cta):
+            while cur[c] is not None and cur[c][2] <= 0.0:
+                i, ph, _ = cur[c]
+                if ph == 0 and stream[i] > 0.0:
+                    cur[c] = [i, 1, stream[i]]
+                elif queue:
+                    j = queue.pop(0)
+                    cur[c] = [j, 0, fixed[j]]
+                else:
+                    cur[c] = None
+        busy = [c for c in range(n_cta) if cur[c] is not None]
+        if not busy:
+            break
+        n_stream = sum(1 for c in busy if cur[c][1] == 1)
+        rate = min(params["dec_cta_gbs"], params["dec_gbs"] / n_stream) * 1e3 if n_stream else 0.0
+        ttf = {c: (cur[c][2] if cur[c][1] == 0 else cur[c][2] / rate) for c in busy}
+        dt = min(ttf[c] for c in busy)
+        t += dt
+        for c in busy:
+            if ttf[c] == dt:
+                cur[c][2] = 0.0
+            else:
+                cur[c][2] -= dt if cur[c][1] == 0 else dt * rate
+    out["makespan_us"] = t
+    out["time_us"] = params["launch_us"] + t
     return out
 
 

@@ -8,8 +8,8 @@ import pytest
 import oracle.costmodel as OC
 from kv_cache_segment_gb300 import msa, workloads as W
 
-PARAMS = dict(launch_us=6.5, dec_item_us=2.25, dec_tile_us=1.375, pre_item_us=3.5, pre_tile_us=0.875,
-              box_us=0.0625, merge_us=1.75)
+PARAMS = dict(launch_us=6.5, dec_item_us=2.25, dec_gbs=6400.0, dec_cta_gbs=96.0, pre_item_us=3.5,
+              pre_tile_us=0.875, box_us=0.0625, merge_us=1.75)
 
 
 def _plan(wl, num_sms=152):
@@ -24,14 +24,14 @@ def _both(wl, params=PARAMS, num_sms=152):
         items = msa.msa_plan_get_items(plan)
         order = msa.msa_plan_get_order(plan)
         grid = msa.msa_plan_get_info(plan)["grid"]
-        ref = OC.estimate(items.tolist(), order.tolist(), wl.block_table, wl.seq_lens, grid, params)
+        ref = OC.estimate(items.tolist(), order.tolist(), wl.block_table, wl.seq_lens, grid, params, wl.head_dim)
         info = msa.msa_plan_get_info(plan)
     finally:
         msa.msa_plan_destroy(plan)
     return lib, ref, info
 
 
-INT_KEYS = ("n_items", "n_split_items", "decode_tiles", "prefill_tile_heads", "extra_boxes")
+INT_KEYS = ("n_items", "n_split_items", "decode_tiles", "prefill_tile_heads", "extra_boxes", "stream_bytes")
 
 
 @pytest.mark.parametrize("wl_fn", [lambda: W.small_config(1), lambda: W.small_config(2), lambda: W.small_config(3),
@@ -41,8 +41,8 @@ def test_library_matches_oracle(wl_fn):
     lib, ref, _ = _both(wl_fn())
     for k in INT_KEYS:
         assert lib[k] == ref[k], k
-    for k in ("busy_us", "makespan_us", "time_us"):
-        assert lib[k] == pytest.approx(ref[k], rel=1e-12), k
+    for k in ("fixed_us", "makespan_us", "time_us"):
+        assert lib[k] == pytest.approx(ref[k], rel=1e-9), k
 
 
 @pytest.mark.parametrize("num_sms", [1, 7, 1500])
@@ -50,29 +50,39 @@ def test_library_matches_oracle_other_grids(num_sms):
     lib, ref, _ = _both(W.small_config(3), num_sms=num_sms)
     for k in INT_KEYS:
         assert lib[k] == ref[k], k
-    assert lib["makespan_us"] == pytest.approx(ref["makespan_us"], rel=1e-12)
+    assert lib["makespan_us"] == pytest.approx(ref["makespan_us"], rel=1e-9)
 
 
-def test_one_cta_makespan_is_the_sum_of_item_costs():
+def test_one_cta_runs_items_back_to_back():
+    """One CTA: every fixed phase plus every stream at min(per-CTA, shared)."""
     lib, ref, info = _both(W.small_config(5), num_sms=1)
     assert info["grid"] == 1
-    assert lib["makespan_us"] == pytest.approx(lib["busy_us"], rel=1e-12)
-    assert ref["makespan_us"] == pytest.approx(ref["busy_us"], rel=1e-12)
+    rate = min(PARAMS["dec_cta_gbs"], PARAMS["dec_gbs"]) * 1e3
+    want = lib["fixed_us"] + lib["stream_bytes"] / rate
+    assert lib["makespan_us"] == pytest.approx(want, rel=1e-9)
+    assert ref["makespan_us"] == pytest.approx(want, rel=1e-9)
 
 
-@pytest.mark.parametrize("n_seqs,ctas", [(6, 4), (8, 8), (20, 3)])
-def test_equal_items_fill_ctas_in_rounds(n_seqs, ctas):
+@pytest.mark.parametrize("n_seqs,ctas,dec_gbs", [(6, 4, 6400.0), (8, 8, 6400.0), (20, 3, 6400.0), (6, 4, 200.0),
+                                                 (9, 4, 150.0)])
+def test_equal_items_fill_ctas_in_rounds(n_seqs, ctas, dec_gbs):
     """N identical decode groups (one segment, one query, 3 tiles, no split)
-    on C CTAs finish in ceil(N/C) rounds of one item cost."""
+    on C CTAs run in rounds of k = min(C, items left) CTAs, each round one
+    fixed phase plus the stream at min(per-CTA, shared / k)."""
     L = 3 * 128
     wl = W.custom([L] * n_seqs, [[L // 16]] * n_seqs, [[(L, L + 1)]] * n_seqs, hq=4, hkv=1)
-    params = dict(PARAMS, box_us=0.0)
+    params = dict(PARAMS, box_us=0.0, dec_gbs=dec_gbs)
     lib, ref, info = _both(wl, params, num_sms=ctas)
     assert lib["n_items"] == n_seqs and lib["n_split_items"] == 0 and lib["decode_tiles"] == 3 * n_seqs
-    item = params["dec_item_us"] + 3 * params["dec_tile_us"]
-    rounds = math.ceil(n_seqs / info["grid"])
-    assert lib["makespan_us"] == pytest.approx(rounds * item, rel=1e-12)
-    assert ref["makespan_us"] == pytest.approx(rounds * item, rel=1e-12)
+    C = info["grid"]
+    tile_bytes = 2 * 128 * 128 * 2
+    want, left = 0.0, n_seqs
+    while left > 0:
+        k = min(C, left)
+        want += params["dec_item_us"] + 3 * tile_bytes / (min(params["dec_cta_gbs"], dec_gbs / k) * 1e3)
+        left -= k
+    assert lib["makespan_us"] == pytest.approx(want, rel=1e-9)
+    assert ref["makespan_us"] == pytest.approx(want, rel=1e-9)
 
 
 def test_single_block_segments_cost_seven_extra_boxes_per_full_tile():
@@ -114,3 +124,90 @@ def test_position_aware_recompute_flops(a, b, L):
 def test_estimate_rejects_null():
     with pytest.raises(msa.MsaError):
         msa._check(msa.load().msa_plan_estimate(None, None, None), "msa_plan_estimate")
+
+
+# ------------------------------------------------- adaptive chunking (create_ex)
+
+FITTED = dict(launch_us=17.3, dec_item_us=0.0, dec_gbs=7565.0, dec_cta_gbs=59.4, pre_item_us=30.1, pre_tile_us=0.787,
+              box_us=0.0, merge_us=8.43)
+DEC_CANDIDATES = (1.0, 1.5, 2.0, 3.0, 4.0)
+PRE_CANDIDATES = (1.0, 2.0, 4.0)
+
+
+def _args(wl):
+    dims = msa.make_dims(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, 16, wl.scale)
+    return (dims, wl.block_table, wl.seq_lens, wl.q_range_indptr, wl.q_ranges_flat)
+
+
+def _time(wl, d, p, params, num_sms=152):
+    plan = msa.msa_plan_create_ex(*_args(wl), num_sms=num_sms, decode_split=d, prefill_split=p)
+    try:
+        return msa.msa_plan_estimate(plan, params)["time_us"]
+    finally:
+        msa.msa_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("idx", [2, 4, 5])
+def test_explicit_splits_are_used_and_reported(idx):
+    wl = W.config(idx)
+    counts = []
+    for d, p in ((1.0, 1.0), (3.0, 4.0), (8.0, 8.0)):
+        plan = msa.msa_plan_create_ex(*_args(wl), num_sms=152, decode_split=d, prefill_split=p)
+        try:
+            info = msa.msa_plan_get_info(plan)
+            assert (info["decode_split"], info["prefill_split"]) == (d, p)
+            counts.append(info["num_items"])
+        finally:
+            msa.msa_plan_destroy(plan)
+    assert counts[0] <= counts[1] <= counts[2]  # finer splits, no fewer items
+    plan = msa.msa_plan_create_ex(*_args(wl), num_sms=152)
+    try:
+        info = msa.msa_plan_get_info(plan)
+        assert (info["decode_split"], info["prefill_split"]) == (3.0, 4.0)  # the defaults
+    finally:
+        msa.msa_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("wl_fn", [lambda: W.config(2), lambda: W.config(5), lambda: W.small_config(3),
+                                   lambda: W.restrict_rows(W.config(4), "decode")],
+                         ids=["batched_decode", "mixed_batch", "small3", "long_decode_rows"])
+def test_chooser_picks_the_model_minimum(wl_fn):
+    """Decode split first (prefill at its default), then prefill split, each
+    the candidate with the lowest msa_plan_estimate time (first on ties)."""
+    wl = wl_fn()
+    plan = msa.msa_plan_create_ex(*_args(wl), num_sms=152, choose_with=FITTED)
+    try:
+        info = msa.msa_plan_get_info(plan)
+        kinds = set(msa.msa_plan_get_items(plan)[:, 0].tolist())
+    finally:
+        msa.msa_plan_destroy(plan)
+    d, p, best = 3.0, 4.0, math.inf
+    if 0 in kinds:
+        for c in DEC_CANDIDATES:
+            t = _time(wl, c, 4.0, FITTED)
+            if t < best:
+                best, d = t, c
+    if 1 in kinds:
+        for c in PRE_CANDIDATES:
+            t = _time(wl, d, c, FITTED)
+            if t < best:
+                best, p = t, c
+    assert (info["decode_split"], info["prefill_split"]) == (d, p)
+
+
+@pytest.mark.parametrize("d,p", [(-1.0, 0.0), (0.0, float("nan")), (float("inf"), 1.0)])
+def test_bad_split_options_are_rejected(d, p):
+    with pytest.raises(msa.MsaError) as e:
+        msa.msa_plan_create_ex(*_args(W.small_config(2)), num_sms=152, decode_split=d, prefill_split=p)
+    assert e.value.status == msa.MSA_ERR_INVALID_ARG
+
+
+def test_bad_cost_params_are_rejected():
+    plan = msa.msa_plan_create_ex(*_args(W.small_config(2)), num_sms=152)
+    try:
+        with pytest.raises(msa.MsaError):
+            msa.msa_plan_estimate(plan, dict(FITTED, dec_gbs=-1.0))
+        with pytest.raises(msa.MsaError):
+            msa.msa_plan_estimate(plan, dict(FITTED, pre_tile_us=float("nan")))
+    finally:
+        msa.msa_plan_destroy(plan)
