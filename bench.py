@@ -142,7 +142,7 @@ class ClockSampler:
 class Case:
     """A workload resident on the GPU: pools, q, plan, workspace, outputs."""
 
-    def __init__(self, wl, dev, contiguous=False):
+    def __init__(self, wl, dev, contiguous=False, plan_opts=None):
         import torch
         from kv_cache_segment_gb300 import msa
         from kv_cache_segment_gb300 import workloads as W
@@ -155,7 +155,7 @@ class Case:
         self.kp, self.vp = W.make_pool(wl, k, v, fill=0.0)
         del k, v
         self.q = q
-        self.sess = MsaSession.from_workload(wl, device=dev)
+        self.sess = MsaSession.from_workload(wl, device=dev, **(plan_opts or {}))
         self.info = self.sess.info
         self.out = torch.empty((wl.num_q_rows, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((wl.num_q_rows, wl.num_q_heads), dtype=torch.float32, device=dev)
@@ -202,6 +202,14 @@ class Case:
         from kv_cache_segment_gb300 import msa
         msa.msa_attention(self.q, self.kp, self.vp, self.kp.shape[0], self.sess.plan, self.out, msa.MSA_OUT_BF16,
                           self.lse, stream)
+
+    def replan(self, **plan_opts):
+        """Replace the session's plan (same workload) by one made with other
+        msa_plan_create_ex options."""
+        from kv_cache_segment_gb300.runner import MsaSession
+        self.sess.close()
+        self.sess = MsaSession.from_workload(self.wl, device=self.dev, **plan_opts)
+        self.info = self.sess.info
 
     def decode_bytes(self):
         return self.info["decode_kv_bytes"] + self.info["decode_qo_bytes"]
@@ -276,7 +284,7 @@ def gpu_main(args):
 
     # ---- headline: batched decode -------------------------------------
     wl = W.config(2, seed=1002 + 1000 * rank)
-    case = Case(wl, dev)
+    case = Case(wl, dev, plan_opts=_plan_opts())
     step_bytes = case.decode_bytes() + case.append_bytes
     gpu_id = None
     try:
@@ -338,6 +346,7 @@ def gpu_main(args):
                    "items": int(case.info["num_items"]), "grid": int(case.info["grid"]),
                    "kv_bytes_per_step": int(case.info["decode_kv_bytes"]),
                    "l2": "inputs larger than L2 (K/V read per step >> 129 MB L2; 16 GiB pools)",
+                   "planner": _planner_note(case),
                    "parallelism": f"replicas x{world} (independent batches, no collective)"},
         "roofline": roofline,
         "plan_us": round(case.info["host_plan_us"], 1),
@@ -345,6 +354,7 @@ def gpu_main(args):
         "gpu_launches": 2 * args.steps,
     }
 
+    headline_pred = _predict_us(case)
     if rank == 0 and not args.quick:
         result["e2e"] = e2e_leg(case, args, dev, stream)
     del case
@@ -352,6 +362,10 @@ def gpu_main(args):
 
     if not args.quick:
         extras = extra_legs(args, dev, stream, peaks, peak_src, traffic, rank)
+        if "cost_model" in extras and headline_pred is not None:
+            m = attn_ms * 1e3
+            extras["cost_model"]["batched_decode"] = {"predicted_us": headline_pred, "measured_us": round(m, 1),
+                                                      "rel_err": round(headline_pred / m - 1.0, 4)}
         result.update(extras)
     if world > 1:
         dist.barrier()
@@ -399,9 +413,15 @@ def e2e_leg(case, args, dev, stream):
     h2d = q_h.numel() * 2 + kn_h.numel() * 2 + vn_h.numel() * 2 + slot_h.numel() * 8
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
 
+    dsplit, psplit, grid = case.info["decode_split"], case.info["prefill_split"], case.info["grid"]
+
     def step():
-        plan = msa.msa_plan_create(case.dims, table, lens, indptr, ranges, 0)
+        # the split factors the session's plan was chosen with, reused: a
+        # planner call per step stays as cheap as the default one
+        plan = msa.msa_plan_create_ex(case.dims, table, lens, indptr, ranges, grid, dsplit, psplit)
         nbytes = msa.msa_plan_workspace_bytes(plan)
+        if nbytes > ws.numel():
+            raise RuntimeError("per-step plan larger than the session's workspace")
         msa.msa_plan_upload(plan, ws, nbytes, stream)
         q_d.copy_(q_h, non_blocking=True)
         kn_d.copy_(kn_h, non_blocking=True)
@@ -430,7 +450,31 @@ def e2e_leg(case, args, dev, stream):
     val = (case.decode_bytes() + case.append_bytes) / dt / 1e9
     return {"value": round(val, 1), "unit": "GB/s", "ms_per_step": round(dt * 1e3, 4),
             "h2d_bytes_per_step": int(h2d + plan_bytes), "d2h_bytes_per_step": int(d2h),
-            "note": "plan built from host block tables and uploaded every step"}
+            "note": "plan built from host block tables (msa_plan_create_ex with the session's split factors) "
+                    "and uploaded every step"}
+
+
+def _plan_opts():
+    """Plans made by msa_plan_create_ex with the adaptive-chunking chooser
+    (latency-model constants fitted on this GPU), or the default plan when
+    no fit is stored."""
+    from kv_cache_segment_gb300 import costfit
+    params = costfit.load_params()
+    return {"choose_with": params} if params is not None else {}
+
+
+def _planner_note(case):
+    return {"decode_split": case.info["decode_split"], "prefill_split": case.info["prefill_split"],
+            "chosen_by": "latency model (msa_plan_create_ex)" if _plan_opts() else "defaults"}
+
+
+def _predict_us(case):
+    """msa_plan_estimate of the case's plan under the fitted constants, or None."""
+    from kv_cache_segment_gb300 import costfit, msa
+    params = costfit.load_params()
+    if params is None:
+        return None
+    return round(msa.msa_plan_estimate(case.sess.plan, params)["time_us"], 1)
 
 
 def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
@@ -445,7 +489,7 @@ def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
     over = {}
     for idx, key in ((3, "hole_recompute"), (4, "long_context"), (5, "mixed_batch"), (2, "batched_decode")):
         wl = W.config(idx, seed=1000 + idx + 1000 * rank)
-        case = Case(wl, dev)
+        case = Case(wl, dev, plan_opts=_plan_opts())
         if key != "batched_decode":
             step_ms, attn_ms = time_case(case, steps, warm, stream)
             fl, by = case.flops(), case.decode_bytes()
@@ -460,11 +504,19 @@ def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
             lb = by / (peaks["hbm_gbs"] * 1e9) + fl / (peaks["bf16_tflops"] * 1e12)
             ent["roofline_frac_additive"] = round(lb / (attn_ms * 1e-3), 4)
             ent["traffic"] = traffic.get(key)
+            ent["predicted_us"] = _predict_us(case)
+            ent["planner"] = _planner_note(case)
+            if _plan_opts():
+                # the same launch with the default split factors
+                case.replan()
+                _, def_ms = time_case(case, steps, warm, stream, with_append=False)
+                ent["default_plan_attention_ms"] = round(def_ms, 4)
+                case.replan(**_plan_opts())
             if key in ("long_context", "mixed_batch"):
                 # graded per-kind rates: the same sequences, layout and tiling
                 # with only the decode rows, then only the prefill rows
                 for kind in ("decode", "prefill"):
-                    sub = Case(W.restrict_rows(wl, kind), dev)
+                    sub = Case(W.restrict_rows(wl, kind), dev, plan_opts=_plan_opts())
                     _, sub_ms = time_case(sub, steps, warm, stream, with_append=False)
                     if kind == "decode":
                         gbs = sub.decode_bytes() / (sub_ms * 1e-3) / 1e9
@@ -483,7 +535,7 @@ def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
             _, seg_ms = time_case(case, steps, warm, stream, with_append=False)
             del case
             torch.cuda.empty_cache()
-            cont = Case(wl, dev, contiguous=True)
+            cont = Case(wl, dev, contiguous=True, plan_opts=_plan_opts())
             _, con_ms = time_case(cont, steps, warm, stream, with_append=False)
             over[key] = {"segmented_ms": round(seg_ms, 4), "contiguous_ms": round(con_ms, 4),
                          "ratio": round(seg_ms / con_ms, 4)}
@@ -491,6 +543,17 @@ def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
         else:
             del case
         torch.cuda.empty_cache()
+    # expected-latency model (msa_plan_estimate, constants fitted on this
+    # GPU) against the measured launches
+    from kv_cache_segment_gb300 import costfit
+    params = costfit.load_params()
+    if params is not None:
+        cm = {}
+        for key, ent in lines.items():
+            if "predicted_us" in ent:
+                cm[key] = {"predicted_us": ent.pop("predicted_us"), "measured_us": round(ent["attention_ms"] * 1e3, 1)}
+                cm[key]["rel_err"] = round(cm[key]["predicted_us"] / cm[key]["measured_us"] - 1.0, 4)
+        out["cost_model"] = cm
     hr = lines["hole_recompute"]
     out["prefill"] = {"workload": "hole_recompute: 16 seqs x (8192 cached, 25% evicted in holes of 2-32 blocks, "
                                   "recomputed) + 512-token turn, 32/8 heads, D=128",
@@ -595,7 +658,7 @@ def profile_main(args):
         wl = W.config(5)
     else:
         wl = W.long_context(seed=1004, num_seqs=1)
-    case = Case(wl, dev)
+    case = Case(wl, dev, plan_opts=_plan_opts())
     stream = torch.cuda.current_stream(dev)
     for _ in range(5):
         case.append(stream)
