@@ -477,6 +477,152 @@ def _predict_us(case):
     return round(msa.msa_plan_estimate(case.sess.plan, params)["time_us"], 1)
 
 
+def gather_leg(case, steps, warm, stream):
+    """The path MSA replaces (AsymCache explainer, "核心方法 1"): gather the
+    batch's scattered K/V into one contiguous, block-aligned buffer
+    (msa_gather_kv), then attention over that buffer with one segment per
+    sequence; against msa_attention on the segmented layout.  Device time per
+    step, CUDA events on the launching stream."""
+    import dataclasses
+    import torch
+    from kv_cache_segment_gb300 import msa
+    from kv_cache_segment_gb300.runner import MsaSession
+    wl = case.wl
+    nb = [-(-int(L) // 16) for L in wl.seq_lens]
+    base = np.concatenate([[0], np.cumsum(nb)]).astype(np.int64)
+    rows = int(base[-1]) * 16
+    src = np.full(rows, -1, np.int64)
+    seg_slots = wl.slot_mapping()
+    ind = wl.kv_indptr
+    table = np.full((wl.num_seqs, max(1, max(nb) if nb else 1)), -1, np.int32)
+    for s in range(wl.num_seqs):
+        L = int(wl.seq_lens[s])
+        src[base[s] * 16: base[s] * 16 + L] = seg_slots[ind[s]:ind[s] + L]
+        table[s, :nb[s]] = base[s] + np.arange(nb[s])
+    cont = dataclasses.replace(wl, block_table=table, pool_blocks=max(1, int(base[-1])),
+                               runs_drawn=[[(0, int(base[s]), nb[s])] for s in range(wl.num_seqs)],
+                               name=wl.name + "/gathered")
+    sess = MsaSession.from_workload(cont, device=case.dev, **_plan_opts())
+    shape = (max(rows, 1), wl.num_kv_heads, wl.head_dim)
+    kg = torch.empty(shape, dtype=torch.bfloat16, device=case.dev)
+    vg = torch.empty(shape, dtype=torch.bfloat16, device=case.dev)
+    src_d = torch.from_numpy(src).to(case.dev)
+    err = torch.zeros(1, dtype=torch.int32, device=case.dev)
+
+    def gather():
+        msa.msa_gather_kv(case.kp, case.vp, case.kp.shape[0], src_d, rows, kg, vg, case.dims, err, stream)
+
+    def attend():
+        msa.msa_attention(case.q, kg, vg, rows, sess.plan, case.out, msa.MSA_OUT_BF16, case.lse, stream)
+
+    def timed(fns):
+        for _ in range(warm):
+            for f in fns:
+                f()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            for f in fns:
+                f()
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / steps
+
+    g_ms = timed([gather])
+    a_ms = timed([attend])
+    ga_ms = timed([gather, attend])
+    m_ms = timed([lambda: case.attention(stream)])
+    rc, word = sess.check_device()
+    if rc != 0 or int(err.item()) != 0:
+        raise RuntimeError(f"gather leg: device error {word:#x} / {int(err.item())}")
+    sess.close()
+    return {"msa_ms": round(m_ms, 4), "gather_ms": round(g_ms, 4), "contiguous_attention_ms": round(a_ms, 4),
+            "gather_plus_attention_ms": round(ga_ms, 4), "msa_speedup": round(ga_ms / m_ms, 3),
+            "gathered_bytes": int(rows * wl.num_kv_heads * wl.head_dim * 2 * 2)}
+
+
+def eviction_workloads(seed=1100, num_seqs=16, blocks=512, evict=128, hq=32, hkv=8, d=128):
+    """Synthetic hit probabilities and the eviction choices of three weightings
+    of the kernel-aware score (msa_select_evictions): hit probability only,
+    recompute cost only, both; and the expected-cost mode, the set with the
+    least expected recompute time (lowest hit probability x cost).  Per policy the recompute workload that
+    follows when every evicted block is needed again: live segments where
+    they were, each evicted hole recomputed into fresh blocks, queries = the
+    evicted positions and the decode row.
+
+    Hit probabilities per block (seeded): attention-sink blocks at the start
+    (0.9), a recency ramp over the last blocks (0.85 e^-(age/32)), and a
+    sparse background (Beta(0.5, 4)); clipped to [0, 1]."""
+    from kv_cache_segment_gb300 import costfit, msa
+    from kv_cache_segment_gb300 import workloads as W
+    params = costfit.load_params() or dict(launch_us=0.0, dec_item_us=0.0, dec_gbs=6400.0, dec_cta_gbs=60.0,
+                                           pre_item_us=30.0, pre_tile_us=0.8, box_us=0.0, merge_us=8.0)
+    rng = np.random.default_rng(seed)
+    L = blocks * 16
+    dims = msa.make_dims(hq, hkv, d)
+    hits = []
+    for _ in range(num_seqs):
+        b = np.arange(blocks)
+        p = 0.9 * (b < 4) + 0.85 * np.exp(-(blocks - 1 - b) / 32.0) + rng.beta(0.5, 4.0, blocks)
+        hits.append(np.clip(p, 0.0, 1.0).astype(np.float32))
+    out = {}
+    policies = (("hit_only", (1.0, 0.0)), ("cost_only", (0.0, 1.0)), ("hit_and_cost", (1.0, 1.0)),
+                ("expected_cost_optimum", None))
+    for name, weights in policies:
+        alpha, beta = weights if weights else (None, None)
+        runs, ranges = [], []
+        exp_hits = exp_flops = exp_us = 0.0
+        for s in range(num_seqs):
+            if weights:
+                ev, cost = msa.msa_select_evictions(dims, L, hits[s], alpha, beta, params, evict)
+            else:  # the set with the least expected recompute time
+                ev, cost = msa.msa_select_evictions(dims, L, hits[s], 0.0, 0.0, params, evict,
+                                                    mode=msa.MSA_EVICT_EXPECTED_COST)
+            gone = np.zeros(blocks, bool)
+            gone[ev] = True
+            exp_hits += float(hits[s][ev].sum())
+            exp_us += float((hits[s][ev] * cost[ev]).sum())
+            keys = np.array([sum(range(16 * b + 1, 16 * b + 17)) for b in ev], np.float64)
+            exp_flops += float((hits[s][ev] * 4.0 * d * hq * keys).sum())
+            sizes, rr = [], []
+            b = 0
+            while b < blocks:  # alternate live segments and holes, in logical order
+                e = b
+                while e < blocks and gone[e] == gone[b]:
+                    e += 1
+                sizes.append(e - b)
+                if gone[b]:
+                    rr.append((16 * b, 16 * e))
+                b = e
+            rr.append((L, L + 1))
+            runs.append(sizes)
+            ranges.append(rr)
+        wl = W.custom([L] * num_seqs, runs, ranges, hq=hq, hkv=hkv, d=d, seed=seed, name=f"eviction/{name}")
+        out[name] = {"wl": wl, "alpha": alpha, "beta": beta, "expected_hit_blocks": round(exp_hits, 2),
+                     "expected_recompute_gflop": round(exp_flops / 1e9, 3),
+                     "model_expected_recompute_us": round(exp_us, 1),
+                     "segments_after_recompute": int(sum(len(r) for r in runs))}
+    return out
+
+
+def eviction_leg(dev, stream, steps, warm):
+    import torch
+    res = {}
+    for name, ent in eviction_workloads().items():
+        wl = ent.pop("wl")
+        case = Case(wl, dev, plan_opts=_plan_opts())
+        step_ms, attn_ms = time_case(case, steps, warm, stream)
+        ent["all_hit_recompute"] = {"step_ms": round(step_ms, 4), "attention_ms": round(attn_ms, 4),
+                                    "prefill_tflop": round(case.flops() / 1e12, 3),
+                                    "predicted_us": _predict_us(case)}
+        res[name] = ent
+        del case
+        torch.cuda.empty_cache()
+    return res
+
+
 def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
     """Prefill/recompute TFLOP/s (hole recompute + new turn), long context,
     mixed batch, and segmented vs contiguous layouts."""
@@ -487,6 +633,7 @@ def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
     out = {}
     lines = {}
     over = {}
+    gathers = {}
     for idx, key in ((3, "hole_recompute"), (4, "long_context"), (5, "mixed_batch"), (2, "batched_decode")):
         wl = W.config(idx, seed=1000 + idx + 1000 * rank)
         case = Case(wl, dev, plan_opts=_plan_opts())
@@ -532,6 +679,8 @@ def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
                     torch.cuda.empty_cache()
             lines[key] = ent
         if key in ("hole_recompute", "batched_decode", "long_context"):
+            gathers[key] = gather_leg(case, steps, warm, stream)
+            torch.cuda.empty_cache()
             _, seg_ms = time_case(case, steps, warm, stream, with_append=False)
             del case
             torch.cuda.empty_cache()
@@ -565,6 +714,8 @@ def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
                                    "traffic": hr.get("traffic")}}
     out["workloads"] = lines
     out["segmentation_overhead"] = over
+    out["gather_then_attention"] = gathers
+    out["eviction_policies"] = eviction_leg(dev, stream, steps, warm)
     return out
 
 

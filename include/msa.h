@@ -225,6 +225,44 @@ typedef struct {
 int msa_plan_estimate(msa_plan_t plan, const msa_cost_params* params, msa_cost_estimate* est);
 
 /*
+ * Kernel-aware eviction choice for one sequence (AsymCache explainer,
+ * "核心方法 2": evict the blocks whose score is lowest, the score weighing
+ * the block's future hit probability against its position-aware recompute
+ * cost, with weights alpha and beta set from the batch and the hardware).
+ * For the sequence's n_blocks = ceil(seq_len / 16) cached blocks:
+ *
+ *   cost_us(b) = pre_tile_us * Hq * (sum over b's positions p of
+ *                min(p + 1, seq_len)) / (128 * 128)
+ *     the attention work of recomputing block b's rows (4*D*Hq*sum min(p+1,
+ *     L) flops: each row attends to every earlier key) in units of one
+ *     128x128 tile of one head, at the latency model's prefill rate;
+ *   score(b)   = alpha * hit_prob[b] + beta * cost_us(b) / max_b cost_us(b)
+ *
+ * With mode MSA_EVICT_EXPECTED_COST the score is instead
+ *   score(b)   = hit_prob[b] * cost_us(b)
+ * the block's expected recompute time (alpha and beta unused): for a fixed
+ * number of evictions, the lowest such scores give the least expected
+ * recompute time, which the pages' linear score only approximates.
+ * The n_evict blocks of lowest score are written to evicted[0 .. n_evict)
+ * in ascending block order; of equal scores the lower block index goes
+ * first.  Later blocks cost more to recompute (the pages also call tail
+ * blocks cheap; the attention arithmetic says the opposite, and this follows
+ * the arithmetic).
+ *   hit_prob   host float [n_blocks], each in [0, 1]
+ *   params     latency-model constants (pre_tile_us is used)
+ *   evicted    host int32 [n_evict]
+ *   cost_us    host double [n_blocks] or NULL: receives cost_us(b)
+ * Returns MSA_ERR_INVALID_ARG for an unknown mode, n_evict outside [0,
+ * n_blocks], a probability outside [0, 1], or negative or non-finite
+ * weights.
+ */
+typedef enum { MSA_EVICT_LINEAR = 0, MSA_EVICT_EXPECTED_COST = 1 } msa_evict_mode;
+
+int msa_select_evictions(const msa_dims* dims, int32_t seq_len, const float* hit_prob, int32_t mode, double alpha,
+                         double beta, const msa_cost_params* params, int32_t n_evict, int32_t* evicted,
+                         double* cost_us);
+
+/*
  * msa_plan_create with options.  Work items: a group (decode rows of one kv
  * head, or a 128-row tile of one or two query heads) whose key range is
  * long is cut into parts of about (the launch's work per CTA) / split tiles;
@@ -260,13 +298,31 @@ int msa_plan_destroy(msa_plan_t plan);
  *   k_new, v_new    device bf16 [n, Hkv, D]
  *   slot_mapping    device int64 [n]: pool row (block*16 + offset) or -1
  *   k_pool, v_pool  device bf16 [pool_tokens, Hkv, D]
- * A slot >= pool_tokens is not written; the kernel records
- * MSA_ERR_BAD_BLOCK_ID in `error_word` (device int32, may be NULL) instead.
+ * A slot >= pool_tokens is not written; the kernel ORs MSA_DEVERR_SLOT into
+ * `error_word` (device int32, may be NULL) instead.
  * Duplicate slots in one call race (one of the rows wins).
  */
 int msa_append_kv(const void* k_new, const void* v_new, const int64_t* slot_mapping, int32_t n,
                   void* k_pool, void* v_pool, int64_t pool_tokens, const msa_dims* dims,
                   int32_t* error_word, msa_stream_t stream);
+
+/*
+ * Gather K/V rows out of the paged pools (the transpose of msa_append_kv):
+ * for t in [0, n), if 0 <= slot_mapping[t] < pool_tokens,
+ *     k_out[t] = k_pool[slot_mapping[t]],  v_out[t] = v_pool[slot_mapping[t]]
+ * (rows of Hkv*D bf16); slot -1 leaves row t untouched.  This is the first
+ * half of the "gather + attention" path that MSA makes unnecessary
+ * (AsymCache explainer, "核心方法 1"); the bench times that path against
+ * msa_attention on the segmented layout.
+ *   k_pool, v_pool  device bf16 [pool_tokens, Hkv, D] (16-byte aligned)
+ *   slot_mapping    device int64 [n]
+ *   k_out, v_out    device bf16 [n, Hkv, D] (16-byte aligned, caller-owned)
+ * A slot >= pool_tokens is skipped; the kernel ORs MSA_DEVERR_SLOT into
+ * `error_word` (device int32, may be NULL).
+ */
+int msa_gather_kv(const void* k_pool, const void* v_pool, int64_t pool_tokens, const int64_t* slot_mapping,
+                  int32_t n, void* k_out, void* v_out, const msa_dims* dims, int32_t* error_word,
+                  msa_stream_t stream);
 
 /*
  * Attention of every query row of the plan, one persistent launch.
@@ -323,6 +379,19 @@ int msa_attention(const void* q, const void* k_pool, const void* v_pool, int64_t
  */
 int msa_attention_no_alloc(const void* q, const void* k_pool, const void* v_pool, int64_t pool_tokens,
                            msa_plan_t plan, void* out, int32_t out_dtype, float* lse, msa_stream_t stream);
+
+/* Bits of a device error word (msa_plan_check_device's `detail`, the
+ * error_word of msa_append_kv / msa_gather_kv): a wait in a role of the
+ * attention kernel ran out of time (producer, MMA, compute), a plan index
+ * out of range, a slot past the pool, a failed TMEM allocation. */
+enum {
+    MSA_DEVERR_TIMEOUT_PRODUCER = 1 << 0,
+    MSA_DEVERR_TIMEOUT_MMA = 1 << 1,
+    MSA_DEVERR_TIMEOUT_COMPUTE = 1 << 2,
+    MSA_DEVERR_BAD_INDEX = 1 << 3,
+    MSA_DEVERR_SLOT = 1 << 4,
+    MSA_DEVERR_TMEM_ALLOC = 1 << 5
+};
 
 /* Synchronise `stream`, read the workspace's error word and return
  * MSA_ERR_DEVICE_CHECK if a kernel recorded an error (then clear it), else

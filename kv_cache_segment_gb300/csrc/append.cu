@@ -60,4 +60,52 @@ int launch_append_kv(const void* k_new, const void* v_new, const int64_t* slot, 
     return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
+// The transpose of the scatter: k_out[t] = k_pool[slot[t]] (and V).  It is
+// the first half of the "gather + attention" path that MSA replaces
+// (AsymCache explainer, "核心方法 1": without MSA, a cache whose live blocks
+// are scattered goes through a gather into one contiguous buffer before a
+// contiguous attention kernel); the bench times that path against MSA.
+__global__ void __launch_bounds__(256) gather_kv_kernel(const uint4* __restrict__ k_pool,
+                                                        const uint4* __restrict__ v_pool, int64_t pool_tokens,
+                                                        const int64_t* __restrict__ slot, int32_t n,
+                                                        uint4* __restrict__ k_out, uint4* __restrict__ v_out,
+                                                        int32_t row_chunks, int32_t* error_word) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < n; t += warps) {
+        const int64_t s = slot[t];
+        if (s < 0) continue;
+        if (s >= pool_tokens) {
+            if (lane == 0 && error_word) atomicOr(error_word, kErrAppendSlot);
+            continue;
+        }
+        const uint4* ks = k_pool + s * row_chunks;
+        const uint4* vs = v_pool + s * row_chunks;
+        uint4* kd = k_out + t * row_chunks;
+        uint4* vd = v_out + t * row_chunks;
+        for (int c = lane; c < row_chunks; c += 32) {
+            const uint4 a = __ldcs(ks + c);
+            const uint4 b = __ldcs(vs + c);
+            kd[c] = a;
+            vd[c] = b;
+        }
+    }
+}
+
+int launch_gather_kv(const void* k_pool, const void* v_pool, int64_t pool_tokens, const int64_t* slot, int32_t n,
+                     void* k_out, void* v_out, int32_t row_elems, int32_t* error_word, msa_stream_t stream) {
+    static int sms = 0;
+    if (sms == 0) sms = device_sm_count();
+    if (sms <= 0) return MSA_ERR_CUDA;
+    const int32_t row_chunks = row_elems * 2 / 16;
+    const int warps_per_block = 8;
+    int64_t blocks = ((int64_t)n + warps_per_block - 1) / warps_per_block;
+    const int64_t cap = (int64_t)sms * 8;
+    if (blocks > cap) blocks = cap;
+    gather_kv_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(k_pool), static_cast<const uint4*>(v_pool), pool_tokens, slot, n,
+        static_cast<uint4*>(k_out), static_cast<uint4*>(v_out), row_chunks, error_word);
+    return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
 }  // namespace msa

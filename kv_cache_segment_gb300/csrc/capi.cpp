@@ -20,6 +20,11 @@ int device_sm_count() {
 
 }  // namespace msa
 
+static_assert(msa::kErrTimeoutProducer == MSA_DEVERR_TIMEOUT_PRODUCER && msa::kErrTimeoutMma == MSA_DEVERR_TIMEOUT_MMA &&
+                  msa::kErrTimeoutCompute == MSA_DEVERR_TIMEOUT_COMPUTE && msa::kErrBadIndex == MSA_DEVERR_BAD_INDEX &&
+                  msa::kErrAppendSlot == MSA_DEVERR_SLOT && msa::kErrTmemAlloc == MSA_DEVERR_TMEM_ALLOC,
+              "device error bits must match msa.h");
+
 extern "C" {
 
 int msa_plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks_per_seq,
@@ -123,6 +128,20 @@ int msa_append_kv(const void* k_new, const void* v_new, const int64_t* slot_mapp
     for (const void* p : {k_new, v_new, (const void*)k_pool, (const void*)v_pool})
         if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return MSA_ERR_INVALID_ARG;
     return msa::launch_append_kv(k_new, v_new, slot_mapping, n, k_pool, v_pool, pool_tokens,
+                                 dims->num_kv_heads * dims->head_dim, error_word, stream);
+}
+
+int msa_gather_kv(const void* k_pool, const void* v_pool, int64_t pool_tokens, const int64_t* slot_mapping,
+                  int32_t n, void* k_out, void* v_out, const msa_dims* dims, int32_t* error_word,
+                  msa_stream_t stream) {
+    if (!dims || n < 0 || pool_tokens < 0) return MSA_ERR_INVALID_ARG;
+    if (dims->num_kv_heads <= 0 || (dims->head_dim != 64 && dims->head_dim != 128))
+        return MSA_ERR_UNSUPPORTED_DIMS;
+    if (n == 0) return MSA_OK;
+    if (!k_out || !v_out || !slot_mapping || !k_pool || !v_pool) return MSA_ERR_INVALID_ARG;
+    for (const void* p : {(const void*)k_out, (const void*)v_out, k_pool, v_pool})
+        if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return MSA_ERR_INVALID_ARG;
+    return msa::launch_gather_kv(k_pool, v_pool, pool_tokens, slot_mapping, n, k_out, v_out,
                                  dims->num_kv_heads * dims->head_dim, error_word, stream);
 }
 

@@ -215,3 +215,41 @@ int msa_plan_estimate(msa_plan_t plan, const msa_cost_params* c, msa_cost_estima
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- eviction --
+
+extern "C" int msa_select_evictions(const msa_dims* dims, int32_t seq_len, const float* hit_prob, int32_t mode,
+                                    double alpha, double beta, const msa_cost_params* params, int32_t n_evict,
+                                    int32_t* evicted, double* cost_us) {
+    if (!dims || !params || seq_len < 0) return MSA_ERR_INVALID_ARG;
+    if (mode != MSA_EVICT_LINEAR && mode != MSA_EVICT_EXPECTED_COST) return MSA_ERR_INVALID_ARG;
+    if (!(alpha >= 0.0) || !(beta >= 0.0) || !std::isfinite(alpha) || !std::isfinite(beta)) return MSA_ERR_INVALID_ARG;
+    if (!(params->pre_tile_us >= 0.0) || !std::isfinite(params->pre_tile_us)) return MSA_ERR_INVALID_ARG;
+    const int32_t nb = (seq_len + kBlock - 1) / kBlock;
+    if (n_evict < 0 || n_evict > nb) return MSA_ERR_INVALID_ARG;
+    if (nb > 0 && !hit_prob) return MSA_ERR_INVALID_ARG;
+    if (n_evict > 0 && !evicted) return MSA_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < nb; ++b)
+        if (!(hit_prob[b] >= 0.0f && hit_prob[b] <= 1.0f)) return MSA_ERR_INVALID_ARG;
+    std::vector<double> cost(nb);
+    double cmax = 0.0;
+    for (int32_t b = 0; b < nb; ++b) {
+        const int64_t p0 = (int64_t)b * kBlock, p1 = std::min<int64_t>(p0 + kBlock, seq_len);
+        // sum over p in [p0, p1) of min(p + 1, seq_len) = p + 1 (p < seq_len)
+        const double keys = (double)((p0 + 1 + p1) * (p1 - p0) / 2);
+        cost[b] = params->pre_tile_us * dims->num_q_heads * keys / (double)(msa::kTileKeys * msa::kTileRows);
+        cmax = std::max(cmax, cost[b]);
+        if (cost_us) cost_us[b] = cost[b];
+    }
+    std::vector<std::pair<double, int32_t>> sc(nb);
+    for (int32_t b = 0; b < nb; ++b)
+        sc[b] = {mode == MSA_EVICT_EXPECTED_COST ? (double)hit_prob[b] * cost[b]
+                                                 : alpha * (double)hit_prob[b] + (cmax > 0.0 ? beta * cost[b] / cmax : 0.0),
+                 b};
+    std::stable_sort(sc.begin(), sc.end(), [](const auto& x, const auto& y) { return x.first < y.first; });
+    std::vector<int32_t> out(n_evict);
+    for (int32_t i = 0; i < n_evict; ++i) out[i] = sc[i].second;
+    std::sort(out.begin(), out.end());
+    for (int32_t i = 0; i < n_evict; ++i) evicted[i] = out[i];
+    return MSA_OK;
+}

@@ -75,7 +75,8 @@ struct WsLayout {
     size_t total;
 };
 
-// Error word codes written by kernels (bit flags, OR-ed).
+// Error word codes written by kernels (bit flags, OR-ed); the public names
+// are the MSA_DEVERR_* constants of msa.h.
 enum DeviceError : int32_t {
     kErrTimeoutProducer = 1 << 0,
     kErrTimeoutMma = 1 << 1,

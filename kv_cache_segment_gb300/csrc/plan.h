@@ -73,6 +73,8 @@ int device_sm_count();
 int launch_append_kv(const void* k_new, const void* v_new, const int64_t* slot, int32_t n,
                      void* k_pool, void* v_pool, int64_t pool_tokens, int32_t row_elems,
                      int32_t* error_word, msa_stream_t stream);
+int launch_gather_kv(const void* k_pool, const void* v_pool, int64_t pool_tokens, const int64_t* slot, int32_t n,
+                     void* k_out, void* v_out, int32_t row_elems, int32_t* error_word, msa_stream_t stream);
 int launch_attention(const msa_plan_s* P, const void* q, const void* k_pool, const void* v_pool,
                      int64_t pool_tokens, void* out, int32_t out_dtype, float* lse, msa_stream_t stream);
 // the same launch with an explicit device workspace holding the plan image

@@ -29,6 +29,14 @@ MSA_ERR_DEVICE_CHECK = -8
 MSA_ERR_NOT_UPLOADED = -9
 MSA_OUT_BF16 = 0
 MSA_OUT_FP32 = 1
+MSA_EVICT_LINEAR = 0
+MSA_EVICT_EXPECTED_COST = 1
+MSA_DEVERR_TIMEOUT_PRODUCER = 1 << 0
+MSA_DEVERR_TIMEOUT_MMA = 1 << 1
+MSA_DEVERR_TIMEOUT_COMPUTE = 1 << 2
+MSA_DEVERR_BAD_INDEX = 1 << 3
+MSA_DEVERR_SLOT = 1 << 4
+MSA_DEVERR_TMEM_ALLOC = 1 << 5
 
 
 class MsaError(RuntimeError):
@@ -104,7 +112,10 @@ def load(path: str = LIB_PATH):
         "msa_plan_estimate": ([vp, ctypes.POINTER(msa_cost_params), ctypes.POINTER(msa_cost_estimate)],
                               ctypes.c_int),
         "msa_plan_destroy": ([vp], ctypes.c_int),
+        "msa_select_evictions": ([ctypes.POINTER(msa_dims), i32, vp, i32, ctypes.c_double, ctypes.c_double,
+                                  ctypes.POINTER(msa_cost_params), i32, vp, vp], ctypes.c_int),
         "msa_append_kv": ([vp, vp, vp, i32, vp, vp, i64, ctypes.POINTER(msa_dims), vp, vp], ctypes.c_int),
+        "msa_gather_kv": ([vp, vp, i64, vp, i32, vp, vp, ctypes.POINTER(msa_dims), vp, vp], ctypes.c_int),
         "msa_attention": ([vp, vp, vp, i64, vp, vp, i32, vp, vp], ctypes.c_int),
         "msa_attention_no_alloc": ([vp, vp, vp, i64, vp, vp, i32, vp, vp], ctypes.c_int),
         "msa_plan_check_device": ([vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
@@ -249,6 +260,22 @@ def msa_plan_estimate(plan, params) -> dict:
     return {name: getattr(e, name) for name, _ in msa_cost_estimate._fields_}
 
 
+def msa_select_evictions(dims: msa_dims, seq_len: int, hit_prob, alpha: float, beta: float, params, n_evict: int,
+                         mode: int = 0):
+    """(evicted block indices ascending, per-block recompute cost in us) for
+    one sequence; params: dict of msa_cost_params names (see include/msa.h)."""
+    lib = load()
+    hp = np.ascontiguousarray(hit_prob, np.float32)
+    nb = -(-int(seq_len) // 16)
+    ev = np.zeros(max(int(n_evict), 1), np.int32)
+    cost = np.zeros(max(nb, 1), np.float64)
+    c = msa_cost_params(*[float(params[k]) for k in COST_PARAM_NAMES])
+    _check(lib.msa_select_evictions(ctypes.byref(dims), int(seq_len), hp.ctypes.data if hp.size else None,
+                                    int(mode), float(alpha), float(beta), ctypes.byref(c), int(n_evict),
+                                    ev.ctypes.data, cost.ctypes.data), "msa_select_evictions")
+    return ev[: int(n_evict)], cost[:nb]
+
+
 def msa_plan_destroy(plan):
     if plan:
         load().msa_plan_destroy(plan)
@@ -259,6 +286,12 @@ def msa_append_kv(k_new, v_new, slot_mapping, n: int, k_pool, v_pool, pool_token
     _check(load().msa_append_kv(_p(k_new), _p(v_new), _p(slot_mapping), int(n), _p(k_pool), _p(v_pool),
                                 int(pool_tokens), ctypes.byref(dims), _p(error_word), _stream(stream)),
            "msa_append_kv")
+
+
+def msa_gather_kv(k_pool, v_pool, pool_tokens: int, slot_mapping, n: int, k_out, v_out, dims: msa_dims,
+                  error_word=None, stream=None):
+    _check(load().msa_gather_kv(_p(k_pool), _p(v_pool), int(pool_tokens), _p(slot_mapping), int(n), _p(k_out),
+                                _p(v_out), ctypes.byref(dims), _p(error_word), _stream(stream)), "msa_gather_kv")
 
 
 def msa_attention(q, k_pool, v_pool, pool_tokens: int, plan, out, out_dtype: int = MSA_OUT_BF16, lse=None,

@@ -68,6 +68,44 @@ def test_append_kv_slot_past_pool_is_reported_not_written():
     assert kp.float().sum().item() == 256
 
 
+@pytest.mark.parametrize("hkv,d", [(8, 128), (2, 64)])
+def test_gather_kv_bit_exact(hkv, d):
+    """k_out[t] = k_pool[slot[t]] (and V) for slot >= 0; rows with slot -1
+    keep what they held; against numpy indexing of the same bits."""
+    g = torch.Generator().manual_seed(9)
+    pool_tokens, n = 5000, 1500
+    kp = torch.randn((pool_tokens, hkv, d), generator=g).to(torch.bfloat16).cuda()
+    vp = torch.randn((pool_tokens, hkv, d), generator=g).to(torch.bfloat16).cuda()
+    slot = torch.randint(0, pool_tokens, (n,), generator=g, dtype=torch.int64)
+    slot[::5] = -1
+    ko = torch.full((n, hkv, d), 3.0, dtype=torch.bfloat16, device="cuda")
+    vo = torch.full((n, hkv, d), -3.0, dtype=torch.bfloat16, device="cuda")
+    want_k, want_v = _bits(ko).copy(), _bits(vo).copy()
+    keep = slot.numpy() >= 0
+    want_k[keep] = _bits(kp)[slot.numpy()[keep]]
+    want_v[keep] = _bits(vp)[slot.numpy()[keep]]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dims = msa.make_dims(hkv, hkv, d)
+    msa.msa_gather_kv(kp, vp, pool_tokens, slot.cuda(), n, ko, vo, dims, err, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(ko), want_k) and np.array_equal(_bits(vo), want_v)
+    assert int(err.item()) == 0
+    sel = slot.cuda().clamp(min=0)
+    assert torch.equal(kp.index_select(0, sel)[keep], ko[keep])
+
+
+def test_gather_kv_slot_past_pool_is_reported_not_read():
+    kp = torch.ones((64, 2, 64), dtype=torch.bfloat16, device="cuda")
+    ko = torch.zeros((3, 2, 64), dtype=torch.bfloat16, device="cuda")
+    slot = torch.tensor([1, 64, 5], dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    msa.msa_gather_kv(kp, kp, 64, slot, 3, ko, ko.clone(), msa.make_dims(2, 2, 64), err,
+                      torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert int(err.item()) == msa.MSA_DEVERR_SLOT
+    assert ko[0].float().sum().item() == 128 and ko[1].float().sum().item() == 0 and ko[2].float().sum().item() == 128
+
+
 # ------------------------------------------------------- attention, small --
 
 @pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
