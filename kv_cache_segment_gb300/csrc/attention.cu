@@ -346,7 +346,10 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
     const uint32_t lQ = (uint32_t)dQ;
     const uint32_t lK = (uint32_t)ptx::smem_desc(ptx::smem_u32(smem + C::kOffK), 16, 1024, 2);
     const uint32_t lV = (uint32_t)ptx::smem_desc(ptx::smem_u32(smem + C::kOffV), C::kPanelBytes, 1024, 2);
-    uint32_t kv_cnt = 0, q_cnt = 0, pf[2] = {0u, 0u}, oc[2] = {0u, 0u}, n_taken = 0;
+    // P-ready phases per head; O-done phases (one per item: the items of a
+    // plan all have the same number of heads, so both heads' barriers move
+    // together or only head 0's is used)
+    uint32_t kv_cnt = 0, q_cnt = 0, pf0 = 0, pf1 = 0, oc = 0, n_taken = 0;
 
     for (;;) {
         const int ii = take_item_w(p, ctl, n_taken, kErrTimeoutMma, lane);
@@ -372,11 +375,11 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
                 // rows that see fewer than 128 keys add a second pass with the
                 // bf16 residual of P (interleaved per 16-key step)
                 if (j >= 1) {
-                    if (!wait_bar_w(p, ctl, &ctl->p_full[k], pf[k] & 1, kErrTimeoutMma)) return;
-                    ++pf[k];
+                    if (!wait_bar_w(p, ctl, &ctl->p_full[k], (k ? pf1 : pf0) & 1, kErrTimeoutMma)) return;
+                    if (k) ++pf1; else ++pf0;
                     if (k == 0 && !wait_bar_w(p, ctl, &ctl->v_full[stp], (kp / C::kStages) & 1, kErrTimeoutMma))
                         return;
-                    if (jj == 0 && !wait_bar_w(p, ctl, &ctl->o_empty[k], (oc[k] & 1) ^ 1, kErrTimeoutMma)) return;
+                    if (jj == 0 && !wait_bar_w(p, ctl, &ctl->o_empty[k], (oc & 1) ^ 1, kErrTimeoutMma)) return;
                     ptx::tc_fence_after();
                     const uint32_t vl = lV + (uint32_t)((stp * C::kTileBytes) >> 4);
                     const uint32_t to = tbase + C::kTmemO + k * D, tp = tbase + k * 128;
@@ -421,7 +424,7 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
                 ptx::tc_commit_e(&ctl->v_empty[stp]);
                 if (jj == T - 1) {
                     ptx::tc_commit_e(&ctl->o_full);
-                    for (int k = 0; k < nh; ++k) ++oc[k];
+                    ++oc;
                 }
             }
             if (j < T) {
