@@ -393,9 +393,12 @@ def reduce_over_ranks(elapsed_ms, nbytes, device=None):
 
 
 def e2e_leg(case, args, dev, stream):
-    """Same metric through the C ABI from host buffers: per step the plan is
-    built from host arrays and uploaded, q and the new K/V go up from pinned
-    memory, out and lse come back to pinned memory."""
+    """Same metric through the C ABI from host buffers.  Every step: the plan
+    is built from the host block tables and uploaded, q and the new K/V go
+    up from pinned memory, append + attention run, out and lse come back to
+    pinned memory and the host waits for them.  As a serving loop would, the
+    host builds step i+1's plan while the GPU runs step i (two workspaces
+    taking turns), so planning overlaps device work instead of adding to it."""
     import torch
     from kv_cache_segment_gb300 import msa
     wl = case.wl
@@ -407,51 +410,57 @@ def e2e_leg(case, args, dev, stream):
     lse_h = torch.empty(case.lse.shape, dtype=case.lse.dtype).pin_memory()
     q_d = torch.empty_like(case.q)
     kn_d, vn_d, slot_d = torch.empty_like(case.k_new), torch.empty_like(case.v_new), torch.empty_like(case.slot)
-    ws = case.sess.workspace
+    ws = [case.sess.workspace, torch.empty_like(case.sess.workspace)]
     table, lens = wl.block_table, wl.seq_lens
     indptr, ranges = wl.q_range_indptr, wl.q_ranges_flat
     h2d = q_h.numel() * 2 + kn_h.numel() * 2 + vn_h.numel() * 2 + slot_h.numel() * 8
     d2h = out_h.numel() * 2 + lse_h.numel() * 4
-
     dsplit, psplit, grid = case.info["decode_split"], case.info["prefill_split"], case.info["grid"]
 
-    def step():
+    def make_plan(i):
         # the split factors the session's plan was chosen with, reused: a
         # planner call per step stays as cheap as the default one
         plan = msa.msa_plan_create_ex(case.dims, table, lens, indptr, ranges, grid, dsplit, psplit)
         nbytes = msa.msa_plan_workspace_bytes(plan)
-        if nbytes > ws.numel():
+        if nbytes > ws[i % 2].numel():
             raise RuntimeError("per-step plan larger than the session's workspace")
-        msa.msa_plan_upload(plan, ws, nbytes, stream)
-        q_d.copy_(q_h, non_blocking=True)
-        kn_d.copy_(kn_h, non_blocking=True)
-        vn_d.copy_(vn_h, non_blocking=True)
-        slot_d.copy_(slot_h, non_blocking=True)
-        msa.msa_append_kv(kn_d, vn_d, slot_d, len(slot_d), case.kp, case.vp, case.kp.shape[0], case.dims, case.err,
-                          stream)
-        msa.msa_attention(q_d, case.kp, case.vp, case.kp.shape[0], plan, case.out, msa.MSA_OUT_BF16, case.lse,
-                          stream)
-        out_h.copy_(case.out, non_blocking=True)
-        lse_h.copy_(case.lse, non_blocking=True)
-        stream.synchronize()
-        msa.msa_plan_destroy(plan)
+        msa.msa_plan_upload(plan, ws[i % 2], nbytes, stream)
+        return plan, nbytes
+
+    def run(n_steps):
+        plan, nbytes = make_plan(0)
+        for i in range(n_steps):
+            q_d.copy_(q_h, non_blocking=True)
+            kn_d.copy_(kn_h, non_blocking=True)
+            vn_d.copy_(vn_h, non_blocking=True)
+            slot_d.copy_(slot_h, non_blocking=True)
+            msa.msa_append_kv(kn_d, vn_d, slot_d, len(slot_d), case.kp, case.vp, case.kp.shape[0], case.dims,
+                              case.err, stream)
+            msa.msa_attention(q_d, case.kp, case.vp, case.kp.shape[0], plan, case.out, msa.MSA_OUT_BF16, case.lse,
+                              stream)
+            out_h.copy_(case.out, non_blocking=True)
+            lse_h.copy_(case.lse, non_blocking=True)
+            nxt = make_plan(i + 1) if i + 1 < n_steps else None  # overlaps step i on the GPU
+            stream.synchronize()  # step i's results are in host memory
+            msa.msa_plan_destroy(plan)
+            if nxt is not None:
+                plan, nbytes = nxt
         return nbytes
 
-    for _ in range(max(3, args.warmup)):
-        step()
+    run(max(3, args.warmup))
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        plan_bytes = step()
+    plan_bytes = run(args.steps)
     dt = (time.perf_counter() - t0) / args.steps
-    # restore the session's own plan in the shared workspace
-    msa.msa_plan_upload(case.sess.plan, ws, case.sess.ws_bytes, stream)
+    # restore the session's own plan in its workspace
+    msa.msa_plan_upload(case.sess.plan, ws[0], case.sess.ws_bytes, stream)
     torch.cuda.synchronize()
     val = (case.decode_bytes() + case.append_bytes) / dt / 1e9
     return {"value": round(val, 1), "unit": "GB/s", "ms_per_step": round(dt * 1e3, 4),
             "h2d_bytes_per_step": int(h2d + plan_bytes), "d2h_bytes_per_step": int(d2h),
-            "note": "plan built from host block tables (msa_plan_create_ex with the session's split factors) "
-                    "and uploaded every step"}
+            "note": "per step: plan from host block tables (msa_plan_create_ex with the session's split factors, "
+                    "built while the previous step runs) uploaded, inputs up from pinned memory, append + "
+                    "attention, out + lse back to pinned memory, host waits"}
 
 
 def _plan_opts():
