@@ -33,12 +33,14 @@ def compare(out, lse, ref_out, ref_lse, what=""):
     return {"out_max_abs": float(err.max()), "out_max_rel": rel, "lse_max_abs": float(lerr.max())}
 
 
-def run_gpu(wl, k_log, v_log, q, out_fp32=False, num_sms=0, fill=float("nan")):
-    """Pools from the logical K/V (other rows = `fill`), then plan+attention."""
+def run_gpu(wl, k_log, v_log, q, out_fp32=False, num_sms=0, fill=float("nan"), **plan_opts):
+    """Pools from the logical K/V (other rows = `fill`), then plan+attention;
+    plan_opts go to msa_plan_create_ex (decode_split, prefill_split,
+    choose_with)."""
     dev = torch.device("cuda")
     kl, vl, qd = k_log.to(dev), v_log.to(dev), q.to(dev)
     kp, vp = W.make_pool(wl, kl, vl, fill=fill)
-    sess = MsaSession.from_workload(wl, num_sms=num_sms)
+    sess = MsaSession.from_workload(wl, num_sms=num_sms, **plan_opts)
     lse = torch.empty((wl.num_q_rows, wl.num_q_heads), dtype=torch.float32, device=dev)
     out = sess.attention(qd, kp, vp, lse=lse, out_fp32=out_fp32)
     rc, word = sess.check_device()

@@ -128,6 +128,25 @@ def test_split_groups_merge(idx):
     compare(out, lse, ro, rl, wl.name + "/split")
 
 
+@pytest.mark.parametrize("idx", [2, 3, 5])
+@pytest.mark.parametrize("opts", [dict(decode_split=1.0, prefill_split=1.0), dict(decode_split=12.0, prefill_split=16.0),
+                                  "chooser"], ids=["coarse", "fine", "chooser"])
+def test_plan_options_match_oracle(idx, opts):
+    """Plans from msa_plan_create_ex (the bench's): few large items, many
+    small split ones, and the latency model's choice."""
+    from kv_cache_segment_gb300 import costfit
+    wl = W.small_config(idx)
+    k, v, q = W.make_values(wl)
+    if opts == "chooser":
+        params = costfit.load_params()
+        if params is None:
+            pytest.skip("no fitted latency-model constants")
+        opts = dict(choose_with=params)
+    out, lse, info = run_gpu(wl, k, v, q, num_sms=40, **opts)
+    ro, rl = oracle_ref(wl, k, v, q)
+    compare(out, lse, ro, rl, f"{wl.name}/{opts}")
+
+
 def test_fp32_output():
     wl = W.small_config(3)
     k, v, q = W.make_values(wl)
