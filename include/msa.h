@@ -307,6 +307,20 @@ int msa_append_kv(const void* k_new, const void* v_new, const int64_t* slot_mapp
                   int32_t* error_word, msa_stream_t stream);
 
 /*
+ * Self-check of the bounded waits (for tests; the paper has no counterpart).
+ * Every wait in the attention kernel gives up after a time limit, records a
+ * bit in the error word, raises the CTA's abort flag (so the CTA's other
+ * waiters leave at once) and returns, leaving the context usable.  This
+ * launches one CTA that does exactly that on an mbarrier nothing arrives
+ * at: a first waiter gives up after limit_ns (1 ns .. 10 s) and ORs
+ * MSA_DEVERR_TIMEOUT_COMPUTE into device_words[0]; a second waiter, with a
+ * limit 64 times longer, must leave through the abort flag and sets
+ * device_words[1] = 1.  device_words: device int32 [2], zeroed by the
+ * caller.
+ */
+int msa_selftest_wait_timeout(uint64_t limit_ns, int32_t* device_words, msa_stream_t stream);
+
+/*
  * Gather K/V rows out of the paged pools (the transpose of msa_append_kv):
  * for t in [0, n), if 0 <= slot_mapping[t] < pool_tokens,
  *     k_out[t] = k_pool[slot_mapping[t]],  v_out[t] = v_pool[slot_mapping[t]]

@@ -13,6 +13,7 @@
 
 #include "msa_internal.h"
 #include "plan.h"
+#include "ptx.cuh"
 
 namespace msa {
 
@@ -105,6 +106,39 @@ int launch_gather_kv(const void* k_pool, const void* v_pool, int64_t pool_tokens
     gather_kv_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4*>(k_pool), static_cast<const uint4*>(v_pool), pool_tokens, slot, n,
         static_cast<uint4*>(k_out), static_cast<uint4*>(v_out), row_chunks, error_word);
+    return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+// Self-check of the bounded waits every role of the attention kernel uses:
+// warp 0 waits on an mbarrier that nothing arrives at, gives up after
+// limit_ns, records the timeout bit and sets the CTA's abort flag, as a
+// role of the attention kernel does; warp 1 waits on the same barrier with
+// a far longer limit and must leave on the abort flag.  word[0] = error
+// bits, word[1] = 1 if warp 1 left through the abort path.
+__global__ void __launch_bounds__(64) selftest_wait_kernel(uint64_t limit_ns, int32_t* word) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5;
+    if (warp == 0) {
+        const bool ok = ptx::mbar_wait(&bar, 0, &abort_flag, limit_ns);
+        if (!ok && threadIdx.x == 0) {
+            atomicOr(word, kErrTimeoutCompute);
+            *reinterpret_cast<volatile int*>(&abort_flag) = 1;
+        }
+    } else {
+        const bool ok = ptx::mbar_wait(&bar, 0, &abort_flag, limit_ns * 64);
+        if (!ok && threadIdx.x == 32) word[1] = *reinterpret_cast<volatile int*>(&abort_flag) ? 1 : 0;
+    }
+}
+
+int launch_selftest_wait(uint64_t limit_ns, int32_t* word, msa_stream_t stream) {
+    selftest_wait_kernel<<<1, 64, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns, word);
     return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 

@@ -131,6 +131,11 @@ int msa_append_kv(const void* k_new, const void* v_new, const int64_t* slot_mapp
                                  dims->num_kv_heads * dims->head_dim, error_word, stream);
 }
 
+int msa_selftest_wait_timeout(uint64_t limit_ns, int32_t* device_words, msa_stream_t stream) {
+    if (!device_words || limit_ns == 0 || limit_ns > 10000000000ull) return MSA_ERR_INVALID_ARG;
+    return msa::launch_selftest_wait(limit_ns, device_words, stream);
+}
+
 int msa_gather_kv(const void* k_pool, const void* v_pool, int64_t pool_tokens, const int64_t* slot_mapping,
                   int32_t n, void* k_out, void* v_out, const msa_dims* dims, int32_t* error_word,
                   msa_stream_t stream) {

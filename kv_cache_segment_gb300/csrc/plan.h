@@ -73,6 +73,7 @@ int device_sm_count();
 int launch_append_kv(const void* k_new, const void* v_new, const int64_t* slot, int32_t n,
                      void* k_pool, void* v_pool, int64_t pool_tokens, int32_t row_elems,
                      int32_t* error_word, msa_stream_t stream);
+int launch_selftest_wait(uint64_t limit_ns, int32_t* word, msa_stream_t stream);
 int launch_gather_kv(const void* k_pool, const void* v_pool, int64_t pool_tokens, const int64_t* slot, int32_t n,
                      void* k_out, void* v_out, int32_t row_elems, int32_t* error_word, msa_stream_t stream);
 int launch_attention(const msa_plan_s* P, const void* q, const void* k_pool, const void* v_pool,

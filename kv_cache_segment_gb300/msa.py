@@ -115,6 +115,7 @@ def load(path: str = LIB_PATH):
         "msa_select_evictions": ([ctypes.POINTER(msa_dims), i32, vp, i32, ctypes.c_double, ctypes.c_double,
                                   ctypes.POINTER(msa_cost_params), i32, vp, vp], ctypes.c_int),
         "msa_append_kv": ([vp, vp, vp, i32, vp, vp, i64, ctypes.POINTER(msa_dims), vp, vp], ctypes.c_int),
+        "msa_selftest_wait_timeout": ([ctypes.c_uint64, vp, vp], ctypes.c_int),
         "msa_gather_kv": ([vp, vp, i64, vp, i32, vp, vp, ctypes.POINTER(msa_dims), vp, vp], ctypes.c_int),
         "msa_attention": ([vp, vp, vp, i64, vp, vp, i32, vp, vp], ctypes.c_int),
         "msa_attention_no_alloc": ([vp, vp, vp, i64, vp, vp, i32, vp, vp], ctypes.c_int),
@@ -286,6 +287,11 @@ def msa_append_kv(k_new, v_new, slot_mapping, n: int, k_pool, v_pool, pool_token
     _check(load().msa_append_kv(_p(k_new), _p(v_new), _p(slot_mapping), int(n), _p(k_pool), _p(v_pool),
                                 int(pool_tokens), ctypes.byref(dims), _p(error_word), _stream(stream)),
            "msa_append_kv")
+
+
+def msa_selftest_wait_timeout(limit_ns: int, device_words, stream=None):
+    _check(load().msa_selftest_wait_timeout(int(limit_ns), _p(device_words), _stream(stream)),
+           "msa_selftest_wait_timeout")
 
 
 def msa_gather_kv(k_pool, v_pool, pool_tokens: int, slot_mapping, n: int, k_out, v_out, dims: msa_dims,

@@ -274,3 +274,24 @@ def test_misaligned_pointers_are_rejected_before_launch():
         assert e.value.status == msa.MSA_ERR_INVALID_ARG
     finally:
         sess.close()
+
+
+def test_bounded_wait_runs_out_and_the_context_survives():
+    """A wait on a barrier nothing arrives at gives up after its limit, the
+    error bit reaches the host, a second waiter leaves on the abort flag, and
+    the device keeps working (an attention call right after is exact)."""
+    import time
+    words = torch.zeros(2, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    msa.msa_selftest_wait_timeout(50_000_000, words, torch.cuda.current_stream())  # 50 ms
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert words[0].item() == msa.MSA_DEVERR_TIMEOUT_COMPUTE
+    assert words[1].item() == 1
+    assert 0.045 < dt < 2.0
+    wl = W.small_config(1)
+    k, v, q = W.make_values(wl)
+    out, lse, _ = run_gpu(wl, k, v, q)
+    ro, rl = oracle_ref(wl, k, v, q)
+    compare(out, lse, ro, rl, "after a timed-out wait")
