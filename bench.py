@@ -51,13 +51,25 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_sha(path):
+    """First 12 hex digits of the sha1 of a source file's code: comments
+    removed and whitespace runs folded, so that a capture stays valid across
+    edits of comments only."""
+    import hashlib
+    import re
+    src = open(path, encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    src = re.sub(r"\s+", " ", src)
+    return hashlib.sha1(src.encode()).hexdigest()[:12]
+
+
 def load_traffic():
     """Per-launch DRAM bytes from the committed ncu summaries (profiles/*.txt
     lines `traffic <workload> <bytes> <source-sha>`), kept only while the
     kernel source is unchanged."""
-    import hashlib
     src = os.path.join(ROOT, "kv_cache_segment_gb300", "csrc", "attention.cu")
-    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()[:12] if os.path.exists(src) else ""
+    sha = code_sha(src) if os.path.exists(src) else ""
     out = {}
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):

@@ -15,19 +15,26 @@
 // group that was split for SM balance write (output, lse) partials and the
 // last one to finish merges them by log-sum-exp.
 //
-// CTA roles (10 warps; 6 when the launch has decode items only):
-//   warp 0      TMA producer: the Q tiles of a prefill item and the K/V
-//               tiles into a ring of shared-memory stages.
-//   warp 1      owns TMEM; one lane issues tcgen05.mma.  Per KV tile j, in
-//               this order: PV0(j-1), S0(j), PV1(j-1), S1(j), where
-//               Sk = Qk K^T lands in TMEM buffer k and PVk accumulates
-//               O_k += P_k V with P_k read from TMEM (it overwrites S_k; the
-//               tensor core runs one thread's MMAs in issue order).
-//   warps 2..5  warpgroup 0: softmax of Q tile 0 (thread = row = TMEM lane),
+// CTA roles, launch with prefill items (12 warps):
+//   warp 0      K producer: takes items from the work queue, loads the Q
+//               tiles of prefill items and the K tiles (TMA) into a ring of
+//               shared-memory stages, records each tile's key range.
+//   warp 1      owns TMEM; runs the MMA issue loop converged, one elected
+//               lane issuing tcgen05.mma.  Per KV tile j, in this order:
+//               PV0(j-1), S0(j), PV1(j-1), S1(j), where Sk = Qk K^T lands in
+//               TMEM buffer k and PVk accumulates O_k += P_k V with P_k read
+//               from TMEM (it overwrites S_k; the tensor core runs one
+//               thread's MMAs in issue order).
+//   warp 2      V producer: the V tiles, on a ring of their own.
+//   warp 3      merge warp: finishes decode items (combines the compute
+//               warps' states, writes out / partials, cross-CTA merge).
+//   warps 4..7  warpgroup 0: softmax of Q tile 0 (thread = row = TMEM lane)
 //               and the decode math (mma.sync, 32 keys per warp per tile).
-//   warps 6..9  warpgroup 1: softmax of Q tile 1.
+//   warps 8..11 warpgroup 1: softmax of Q tile 1.
 // Each softmax warpgroup has the other's PV + S (about 1024 tensor cycles) to
 // produce its P before the tensor core needs it.
+// Launch with decode items only (7 warps): K producer, V producer, the four
+// decode warps, the merge warp.
 #include <cuda.h>
 #include <type_traits>
 #include <cuda_bf16.h>
