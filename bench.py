@@ -598,7 +598,7 @@ def eviction_workloads(seed=1100, num_seqs=16, blocks=512, evict=128, hq=32, hkv
     from kv_cache_segment_gb300 import costfit, msa
     from kv_cache_segment_gb300 import workloads as W
     params = costfit.load_params() or dict(launch_us=0.0, dec_item_us=0.0, dec_gbs=6400.0, dec_cta_gbs=60.0,
-                                           pre_item_us=30.0, pre_tile_us=0.8, box_us=0.0, merge_us=8.0)
+                                           pre_item_us=30.0, pre_tile_us=0.8, box_us=0.0, dec_merge_us=8.0, pre_merge_us=20.0)
     rng = np.random.default_rng(seed)
     L = blocks * 16
     dims = msa.make_dims(hq, hkv, d)

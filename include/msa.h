@@ -181,7 +181,9 @@ int msa_plan_get_order(msa_plan_t plan, int32_t* order, int32_t* n_items);
  * Each work item runs two phases on the CTA that takes it:
  *   fixed phase (time):
  *     decode : dec_item_us            prefill: pre_item_us + pre_tile_us * tiles * heads
- *     + box_us * extra_boxes + merge_us (if its group is split into parts)
+ *     + box_us * extra_boxes + dec_merge_us / pre_merge_us (if its group is
+ *       split into parts: a decode part's partial is 16 rows, a prefill
+ *       part's 128 rows x 1 or 2 heads, and the last part merges them all)
  *   stream phase (decode items only, bytes): tiles * 128 keys * D * 2 B * 2
  *     (K and V); every CTA in a stream phase progresses at
  *     min(dec_cta_gbs, dec_gbs / number of CTAs in a stream phase), so the
@@ -204,7 +206,8 @@ typedef struct {
     double pre_item_us;
     double pre_tile_us;
     double box_us;
-    double merge_us;
+    double dec_merge_us;
+    double pre_merge_us;
 } msa_cost_params;
 
 typedef struct {

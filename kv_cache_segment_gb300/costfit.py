@@ -14,7 +14,7 @@ segment counts; hole recompute; long-context chunks; mixed batches) at
 different seeds and sizes for the two sets, each planned with three
 different split factors (msa_plan_create_ex).  Each plan is timed as the median of
 `--reps` launches of msa_attention alone (CUDA events on the launching
-stream, after warm-up launches).  The eight parameters are fitted by
+stream, after warm-up launches).  The nine parameters are fitted by
 bounded least squares on log(predicted / measured).
 """
 from __future__ import annotations
@@ -53,6 +53,9 @@ def training_set():
         s.append((f"holes{i}", W.hole_recompute(seed=2020 + i, num_seqs=n, cached_blocks=cb, evict_blocks=ev)))
     for i, (length, runs, chunk) in enumerate([(16384, 1, 512), (65536, 64, 2048), (32768, 16, 1024)]):
         s.append((f"long{i}", W.long_context(seed=2030 + i, num_seqs=1, length=length, n_runs=runs, chunk=chunk)))
+    # launches the size of the bench's prefill workloads
+    s.append(("holes_big", W.hole_recompute(seed=2025, num_seqs=16, cached_blocks=512, evict_blocks=128)))
+    s.append(("long_big", W.long_context(seed=2035, num_seqs=2, length=98304, n_runs=48, chunk=2048)))
     for i, (nd, npf, chunk) in enumerate([(16, 1, 512), (64, 4, 2048), (128, 2, 1024)]):
         s.append((f"mixed{i}", W.mixed_batch(seed=2040 + i, num_decode=nd, num_prefill=npf, chunk=chunk)))
     return s
@@ -115,7 +118,7 @@ def fit(records, x0=None):
     """records: [(plan, measured_us)] -> params dict (least squares on logs)."""
     from scipy.optimize import least_squares
     names = msa.COST_PARAM_NAMES
-    x0 = np.asarray(x0 if x0 is not None else [5.0, 2.0, 6400.0, 80.0, 5.0, 1.0, 0.02, 5.0], float)
+    x0 = np.asarray(x0 if x0 is not None else [5.0, 2.0, 6400.0, 80.0, 5.0, 1.0, 0.02, 5.0, 20.0], float)
 
     def resid(x):
         p = dict(zip(names, x))

@@ -70,8 +70,8 @@ struct BoxCounts {
 };
 
 bool params_ok(const msa_cost_params* c) {
-    const double prm[8] = {c->launch_us, c->dec_item_us, c->dec_gbs, c->dec_cta_gbs,
-                           c->pre_item_us, c->pre_tile_us, c->box_us, c->merge_us};
+    const double prm[9] = {c->launch_us, c->dec_item_us, c->dec_gbs, c->dec_cta_gbs, c->pre_item_us,
+                           c->pre_tile_us, c->box_us, c->dec_merge_us, c->pre_merge_us};
     for (double v : prm)
         if (!(v >= 0.0) || !std::isfinite(v)) return false;
     return true;
@@ -98,7 +98,8 @@ int estimate(const msa_plan_s* P, const msa_cost_params* c, const BoxCounts& box
             f = c->pre_item_us + c->pre_tile_us * (double)(tiles * g.pad);
             out.prefill_tile_heads += tiles * g.pad;
         }
-        f += c->box_us * (double)boxes + (split ? c->merge_us : 0.0);
+        f += c->box_us * (double)boxes +
+             (split ? (it.kind == msa::kDecode ? c->dec_merge_us : c->pre_merge_us) : 0.0);
         fixed[i] = f;
         out.extra_boxes += boxes;
         out.n_split_items += split ? 1 : 0;

@@ -67,7 +67,8 @@ class msa_cost_params(ctypes.Structure):
     _fields_ = [("launch_us", ctypes.c_double), ("dec_item_us", ctypes.c_double),
                 ("dec_gbs", ctypes.c_double), ("dec_cta_gbs", ctypes.c_double),
                 ("pre_item_us", ctypes.c_double), ("pre_tile_us", ctypes.c_double),
-                ("box_us", ctypes.c_double), ("merge_us", ctypes.c_double)]
+                ("box_us", ctypes.c_double), ("dec_merge_us", ctypes.c_double),
+                ("pre_merge_us", ctypes.c_double)]
 
 
 class msa_cost_estimate(ctypes.Structure):

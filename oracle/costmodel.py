@@ -8,7 +8,8 @@ queue:
 
   fixed phase (us)   dec_item                                 (decode)
                    | pre_item + pre_tile * tiles * heads      (prefill)
-                     + box * extra_boxes + merge * [group split into parts]
+                     + box * extra_boxes
+                     + dec_merge | pre_merge   [group split into parts]
   stream phase (B)   decode only: tiles * 128 * D * 2 * 2 (K and V, bf16),
                      at min(dec_cta, dec / n_streaming) GB/s per CTA
   tiles        128-key windows [kb + 128 i, min(kb + 128 (i+1), ke))
@@ -84,7 +85,8 @@ def estimate(items, order, block_table, seq_lens, grid, params, head_dim):
             f = params["pre_item_us"] + params["pre_tile_us"] * tiles * heads
             b = 0.0
             out["prefill_tile_heads"] += tiles * heads
-        f += params["box_us"] * extra + (params["merge_us"] if split else 0.0)
+        merge = params["dec_merge_us"] if kind == 0 else params["pre_merge_us"]
+        f += params["box_us"] * extra + (merge if split else 0.0)
         out["extra_boxes"] += extra
         out["n_split_items"] += 1 if split else 0
         out["stream_bytes"] += int(b)

@@ -9,7 +9,7 @@ import oracle.costmodel as OC
 from kv_cache_segment_gb300 import msa, workloads as W
 
 PARAMS = dict(launch_us=6.5, dec_item_us=2.25, dec_gbs=6400.0, dec_cta_gbs=96.0, pre_item_us=3.5,
-              pre_tile_us=0.875, box_us=0.0625, merge_us=1.75)
+              pre_tile_us=0.875, box_us=0.0625, dec_merge_us=1.75, pre_merge_us=6.5)
 
 
 def _plan(wl, num_sms=152):
@@ -128,8 +128,8 @@ def test_estimate_rejects_null():
 
 # ------------------------------------------------- adaptive chunking (create_ex)
 
-FITTED = dict(launch_us=17.3, dec_item_us=0.0, dec_gbs=7565.0, dec_cta_gbs=59.4, pre_item_us=30.1, pre_tile_us=0.787,
-              box_us=0.0, merge_us=8.43)
+FITTED = dict(launch_us=18.6, dec_item_us=4.55, dec_gbs=8121.0, dec_cta_gbs=52.8, pre_item_us=6.08, pre_tile_us=0.878,
+              box_us=0.0, dec_merge_us=0.79, pre_merge_us=48.7)
 DEC_CANDIDATES = (1.0, 1.5, 2.0, 3.0, 4.0)
 PRE_CANDIDATES = (1.0, 2.0, 4.0)
 

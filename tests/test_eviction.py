@@ -7,7 +7,7 @@ import oracle.eviction as OE
 from kv_cache_segment_gb300 import msa
 
 PARAMS = dict(launch_us=17.3, dec_item_us=0.0, dec_gbs=7565.0, dec_cta_gbs=59.4, pre_item_us=30.1, pre_tile_us=0.787,
-              box_us=0.0, merge_us=8.43)
+              box_us=0.0, dec_merge_us=8.43, pre_merge_us=20.0)
 
 
 def _dims(hq=32, hkv=8, d=128):
