@@ -295,3 +295,24 @@ def test_bounded_wait_runs_out_and_the_context_survives():
     out, lse, _ = run_gpu(wl, k, v, q)
     ro, rl = oracle_ref(wl, k, v, q)
     compare(out, lse, ro, rl, "after a timed-out wait")
+
+
+@pytest.mark.parametrize("name", ["decode", "holes", "mixed", "long"])
+def test_latency_model_predicts_measured_launches(name):
+    """The shipped latency-model constants predict the measured launch time
+    of medium workloads it was not fitted on within 25 %."""
+    from kv_cache_segment_gb300 import costfit
+    params = costfit.load_params()
+    if params is None:
+        pytest.skip("no fitted latency-model constants")
+    wl = {"decode": lambda: W.batched_decode(seed=4001, num_seqs=40, len_range=(2048, 12288), max_seg=6,
+                                             pool_tokens=1 << 20),
+          "holes": lambda: W.hole_recompute(seed=4002, num_seqs=6, cached_blocks=448, evict_blocks=96),
+          "mixed": lambda: W.mixed_batch(seed=4003, num_decode=48, num_prefill=2, chunk=1536),
+          "long": lambda: W.long_context(seed=4004, num_seqs=1, length=40960, n_runs=24, chunk=1024)}[name]()
+    us, sess = costfit.measure(wl, torch.device("cuda"), reps=9, splits=((0.0, 0.0),))[0]
+    try:
+        pred = msa.msa_plan_estimate(sess.plan, params)["time_us"]
+    finally:
+        sess.close()
+    assert abs(pred / us - 1.0) < 0.25, (name, pred, us)
