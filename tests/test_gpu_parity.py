@@ -204,6 +204,66 @@ def test_edge_cases(case):
         assert torch.all(out[0].float() == 0) and torch.all(torch.isneginf(lse[0]))
 
 
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 128), (6, 2, 128), (10, 2, 128), (6, 2, 64)])
+@pytest.mark.parametrize("opts", [dict(), dict(decode_split=12.0, prefill_split=16.0)])
+def test_odd_gqa_ratios(hq, hkv, d, opts):
+    """G = Hq/Hkv odd: prefill items carry one query head (the second softmax
+    warpgroup idles), and a decode item packs floor(16 / G) rows.  Sequence 0
+    has two full 128-row tiles and a ragged prefill tail; sequence 1 has 3
+    decode rows; sequence 2 has 4 rows, which is a decode item for G <= 4
+    and a 4-row prefill tile for G = 5.  The second plan splits groups, so
+    one-head prefill parts go through the cross-CTA merge."""
+    wl = W.custom([700, 260, 90], [[4, 30, 10], [5, 12], [6]], [[(0, 300), (650, 701)], [(258, 261)], [(87, 91)]],
+                  hq=hq, hkv=hkv, d=d, seed=11)
+    k, v, q = W.make_values(wl)
+    out, lse, info = run_gpu(wl, k, v, q, **opts)
+    assert info["num_prefill_items"] > 0 and info["num_decode_items"] > 0
+    ro, rl = oracle_ref(wl, k, v, q)
+    compare(out, lse, ro, rl, f"G={hq // hkv} d={d}")
+
+
+@pytest.mark.parametrize("shape", ["rising", "falling", "spikes"])
+def test_running_max_moves(shape):
+    """Scores far from N(0,1): keys whose scores rise along the sequence (the
+    running max moves up by more than the lazy-rescale threshold many times,
+    so O is rescaled in TMEM and in registers), fall (the first keys dominate
+    and later probabilities underflow), or carry a few large outliers.  q is
+    made positive and K[t] = a(t) + 0.25 N(0,1), so the score of key t is
+    about a(t) * 0.8 * sqrt(D) = 9 a(t); a(t) stays <= 3.5 (lse up to ~40),
+    where fp32 accumulation in the MMA still meets the lse bound."""
+    wl = W.custom([1500, 700], [[20, 44, 30], [10, 34]], [[(0, 260), (1490, 1501)], [(600, 700), (700, 701)]],
+                  hq=8, hkv=2, seed=13)
+    k, v, q = W.make_values(wl)
+    g = torch.Generator().manual_seed(5)
+    T = k.shape[0]
+    t = torch.zeros(T)
+    for s in range(wl.num_seqs):
+        a, b = int(wl.kv_indptr[s]), int(wl.kv_indptr[s + 1])
+        t[a:b] = torch.linspace(0.0, 1.0, b - a)
+    if shape == "rising":
+        amp = 3.5 * t
+    elif shape == "falling":
+        amp = 3.5 * (1.0 - t)
+    else:
+        amp = torch.zeros(T)
+        amp[torch.randint(0, T, (40,), generator=g)] = 3.5
+    k = (amp[:, None, None] + 0.25 * torch.randn(k.shape, generator=g)).to(torch.bfloat16)
+    q = q.float().abs().to(torch.bfloat16)
+    out, lse, _ = run_gpu(wl, k, v, q)
+    ro, rl = oracle_ref(wl, k, v, q)
+    assert np.nanmax(rl) > 20.0  # the scores really are large
+    extra = None
+    if shape == "spikes":
+        # A row whose weight sits on two or three outlier keys (p = 0.6 / 0.4)
+        # sees the bf16 rounding of P un-averaged: the PV product then
+        # carries up to 2^-8 * sum_j p_j |V_j,d| (bf16 unit roundoff; the
+        # residual pass only covers rows with fewer than 128 keys).  The
+        # oracle gives that sum exactly: the same softmax applied to |V|.
+        wabs, _ = oracle_ref(wl, k, v.abs(), q)
+        extra = 2.0 ** -8 * wabs
+    compare(out, lse, ro, rl, shape, extra=extra)
+
+
 def test_repeat_calls_are_identical():
     """Merge counters reset themselves: back-to-back calls give the same bits."""
     wl = W.small_config(2)
