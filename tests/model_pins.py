@@ -1,0 +1,189 @@
+"""Closed-form pins of the plain latency-model and eviction oracles
+(oracle/costmodel.py, oracle/eviction.py).  Each pin takes the oracle module
+as an argument (the real one, or a copy with a planted mistake) and checks it
+against values worked out by hand here, on hand-built work lists: nothing in
+these pins calls the library.
+
+The model (MSA paper abstract; AsymCache explainer, "核心方法 2/3"): a work
+item costs a fixed phase (decode: dec_item; prefill: pre_item + pre_tile x
+tiles x heads; plus box x extra TMA boxes and, for a part of a split group, a
+merge constant) and, for decode, a stream of tiles x 128 x D x 2 B x 2 (K and
+V) bytes at min(per-CTA rate, shared rate / streaming CTAs); CTAs take items
+in queue order as they free up.  The eviction score: alpha x hit + beta x
+cost / max cost, lowest first, ties to the lower block; or hit x cost.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+
+PARAMS = dict(launch_us=6.5, dec_item_us=2.25, dec_gbs=6400.0, dec_cta_gbs=96.0, pre_item_us=3.5,
+              pre_tile_us=0.875, box_us=0.0625, dec_merge_us=1.75, pre_merge_us=6.5)
+TILE_BYTES = 2 * 128 * 128 * 2  # K and V of one 128-key tile, D = 128, bf16
+
+
+def _item(kind, seq, heads, row0, kb, ke, part=0, head=0, nrows=1):
+    return (kind, seq, head, heads, row0, nrows, kb, ke, part)
+
+
+def _close(a, b, rel=1e-12):
+    return math.isclose(a, b, rel_tol=rel, abs_tol=1e-12)
+
+
+# ------------------------------------------------------------ latency model --
+
+def pin_one_cta_mixed_items(oc):
+    """One CTA runs a decode item (3 tiles), a prefill item (2 tiles x 2
+    heads) and the two parts of a split decode group (2 tiles each) back to
+    back: makespan = sum of fixed phases + all streamed bytes at min(per-CTA,
+    shared) rate; time = launch + makespan."""
+    tables = {0: list(range(0, 24)), 1: list(range(100, 116)), 2: list(range(200, 232))}
+    lens = {0: 384, 1: 256, 2: 512}
+    items = [_item(0, 0, 4, 0, 0, 384), _item(1, 1, 2, 1, 0, 256, nrows=128),
+             _item(0, 2, 4, 129, 0, 256, part=0), _item(0, 2, 4, 129, 256, 512, part=1)]
+    p = PARAMS
+    fixed = (p["dec_item_us"] + (p["pre_item_us"] + p["pre_tile_us"] * 2 * 2)
+             + 2 * (p["dec_item_us"] + p["dec_merge_us"]))
+    stream = 7 * TILE_BYTES / (min(p["dec_cta_gbs"], p["dec_gbs"]) * 1e3)
+    r = oc.estimate(items, [0, 1, 2, 3], tables, lens, 1, p, 128)
+    assert r["n_items"] == 4 and r["n_split_items"] == 2
+    assert r["decode_tiles"] == 7 and r["prefill_tile_heads"] == 4 and r["extra_boxes"] == 0
+    assert r["stream_bytes"] == 7 * TILE_BYTES
+    assert _close(r["fixed_us"], fixed)
+    assert _close(r["makespan_us"], fixed + stream)
+    assert _close(r["time_us"], p["launch_us"] + fixed + stream)
+
+
+def pin_split_prefill_pays_its_merge(oc):
+    """Two parts of a split prefill group (one head, 1 tile each) on two CTAs:
+    each is pre_item + pre_tile + pre_merge, in parallel."""
+    items = [_item(1, 0, 1, 0, 0, 128, part=0, nrows=128), _item(1, 0, 1, 0, 128, 256, part=1, nrows=128)]
+    p = PARAMS
+    r = oc.estimate(items, [0, 1], {0: list(range(16))}, {0: 256}, 2, p, 128)
+    assert _close(r["makespan_us"], p["pre_item_us"] + p["pre_tile_us"] + p["pre_merge_us"])
+    assert r["n_split_items"] == 2 and r["stream_bytes"] == 0
+
+
+def pin_queue_order(oc):
+    """Two CTAs, four prefill items of 4, 1, 2 and 6 tiles (one head) in that
+    order: CTA 1 frees first and takes the third item, CTA 0 the fourth."""
+    p = PARAMS
+    cost = [p["pre_item_us"] + p["pre_tile_us"] * t for t in (4, 1, 2, 6)]
+    items = [_item(1, s, 1, 0, 0, 128 * t, nrows=128) for s, t in enumerate((4, 1, 2, 6))]
+    tables = {s: list(range(1000 * s, 1000 * s + 48)) for s in range(4)}
+    lens = {s: 768 for s in range(4)}
+    r = oc.estimate(items, [0, 1, 2, 3], tables, lens, 2, p, 128)
+    want = max(cost[1] + cost[2], cost[0] + cost[3])
+    assert _close(r["makespan_us"], want)
+
+
+def pin_shared_bandwidth(oc):
+    """Two CTAs stream at once with a shared rate below twice the per-CTA
+    rate: each gets half of it."""
+    p = dict(PARAMS, dec_gbs=100.0, dec_cta_gbs=96.0, box_us=0.0)
+    items = [_item(0, s, 4, 0, 0, 384) for s in range(2)]
+    tables = {0: list(range(24)), 1: list(range(100, 124))}
+    r = oc.estimate(items, [0, 1], tables, {0: 384, 1: 384}, 2, p, 128)
+    assert _close(r["makespan_us"], p["dec_item_us"] + 3 * TILE_BYTES / (50.0 * 1e3))
+
+
+def pin_equal_items_in_rounds(oc):
+    """N equal decode items (3 tiles) on C CTAs: rounds of k = min(C, left)
+    items, each a fixed phase plus the stream at min(per-CTA, shared / k)."""
+    for n, c, dec in ((6, 4, 6400.0), (20, 3, 6400.0), (9, 4, 150.0)):
+        p = dict(PARAMS, box_us=0.0, dec_gbs=dec)
+        items = [_item(0, s, 4, s, 0, 384) for s in range(n)]
+        tables = {s: list(range(30 * s, 30 * s + 24)) for s in range(n)}
+        r = oc.estimate(items, list(range(n)), tables, {s: 384 for s in range(n)}, c, p, 128)
+        want, left = 0.0, n
+        while left > 0:
+            k = min(c, left)
+            want += p["dec_item_us"] + 3 * TILE_BYTES / (min(p["dec_cta_gbs"], dec / k) * 1e3)
+            left -= k
+        assert _close(r["makespan_us"], want), (n, c, dec)
+
+
+def pin_tma_boxes(oc):
+    """Every block its own segment (physical blocks 0, 2, 4, ...): a full
+    128-key tile needs 8 boxes (7 extra); the 40-key last tile 3 (2 extra).
+    One segment: only the partial last tile takes one box per 16-key block."""
+    L = 2 * 128 + 40
+    nb = -(-L // 16)
+    r = oc.estimate([_item(0, 0, 4, 0, 0, L)], [0], {0: [2 * b for b in range(nb)]}, {0: L}, 1, PARAMS, 128)
+    assert r["extra_boxes"] == 2 * 7 + 2
+    assert _close(r["fixed_us"], PARAMS["dec_item_us"] + PARAMS["box_us"] * 16)
+    r1 = oc.estimate([_item(0, 0, 4, 0, 0, L)], [0], {0: list(range(nb))}, {0: L}, 1, PARAMS, 128)
+    assert r1["extra_boxes"] == 2
+
+
+def pin_recompute_flops(oc):
+    """4 D Hq sum_{p=a}^{b-1} min(p+1, L) by the arithmetic-series formula."""
+    for a, b, L in ((0, 37, 400), (100, 228, 400), (380, 401, 400)):
+        hi = min(b, L)
+        s = hi * (hi + 1) // 2 - a * (a + 1) // 2 + (L if b == L + 1 else 0)
+        assert oc.hole_recompute_flops(128, 8, a, b, L) == 4.0 * 128 * 8 * s
+
+
+COST_PINS = [pin_one_cta_mixed_items, pin_split_prefill_pays_its_merge, pin_queue_order, pin_shared_bandwidth,
+             pin_equal_items_in_rounds, pin_tma_boxes, pin_recompute_flops]
+
+
+# ------------------------------------------------------------------ eviction --
+
+def pin_block_cost(oe):
+    """cost(b) = pre_tile * Hq * sum_{p in block b} (p + 1) / 128^2."""
+    L, hq, pt = 1000, 32, 0.875
+    cost = oe.recompute_cost_us(L, hq, pt)
+    assert len(cost) == 63
+    for b in (0, 10, 62):
+        lo, hi = 16 * b, min(16 * b + 16, L)
+        assert math.isclose(cost[b], pt * hq * ((hi * (hi + 1) - lo * (lo + 1)) // 2) / 16384, rel_tol=1e-15)
+
+
+def pin_hit_only(oe):
+    """alpha alone: the blocks least likely to be hit go first."""
+    hit = np.linspace(1.0, 0.0, 40)
+    ev, _ = oe.select_evictions(40 * 16, 32, hit, 1.0, 0.0, 0.875, 10)
+    assert ev == list(range(30, 40))
+
+
+def pin_cost_only(oe):
+    """beta alone: recompute work grows with position, the first blocks go."""
+    ev, cost = oe.select_evictions(40 * 16 + 5, 32, np.full(41, 0.5), 0.0, 1.0, 0.875, 7)
+    assert ev == list(range(7))
+    assert all(b > a for a, b in zip(cost[:-2], cost[1:-1]))
+
+
+def pin_cost_on_the_keep_side(oe):
+    """Equal hit probability except block 5 (slightly more likely to be hit):
+    with the cost term added, the cheap early blocks still go before it, and
+    a block dearer to recompute is kept over a cheaper one of equal hit."""
+    hit = np.full(20, 0.5)
+    hit[5] = 0.52
+    ev, _ = oe.select_evictions(20 * 16, 32, hit, 1.0, 0.01, 0.875, 5)
+    assert ev == [0, 1, 2, 3, 4]
+    ev, _ = oe.select_evictions(20 * 16, 32, hit, 1.0, 0.01, 0.875, 6)
+    assert ev == [0, 1, 2, 3, 4, 6]
+
+
+def pin_ties_to_lower_block(oe):
+    ev, _ = oe.select_evictions(20 * 16, 32, np.full(20, 0.3), 1.0, 0.0, 0.875, 5)
+    assert ev == [0, 1, 2, 3, 4]
+
+
+def pin_expected_cost_optimum(oe):
+    """Brute force: no other n blocks have a lower sum of hit x cost."""
+    rng = np.random.default_rng(3)
+    L = 9 * 16 - 3
+    hit = rng.random(9)
+    for n in range(10):
+        ev, cost = oe.select_evictions(L, 32, hit, 0.0, 0.0, 0.875, n, expected_cost=True)
+        got = sum(hit[i] * cost[i] for i in ev)
+        best = min(sum(hit[i] * cost[i] for i in c) for c in itertools.combinations(range(9), n))
+        assert math.isclose(got, best, rel_tol=1e-12, abs_tol=1e-12) and len(ev) == n
+
+
+EVICTION_PINS = [pin_block_cost, pin_hit_only, pin_cost_only, pin_cost_on_the_keep_side, pin_ties_to_lower_block,
+                 pin_expected_cost_optimum]
