@@ -409,34 +409,58 @@ def e2e_leg(case, args, dev, stream):
     is built from the host block tables and uploaded, q and the new K/V go
     up from pinned memory, append + attention run, out and lse come back to
     pinned memory and the host reads them.  As a serving loop would, the
-    steps are pipelined two deep: the host builds and issues step i+1
-    (plan, copies, kernels) before it waits for step i's results, with two
-    sets of device and pinned buffers and two workspaces taking turns."""
+    steps are pipelined two deep (the host builds and issues step i+1 before
+    it waits for step i's results) with two sets of device buffers and
+    workspaces taking turns, and the copies run on two copy streams: step
+    i+1's inputs go up while step i computes, and step i's results come back
+    while step i+1 computes.  Events order each buffer set's uses: a set's
+    inputs are overwritten only after the attention two steps back has read
+    them, and its output only after the copy of that step's results is done.
+    The inputs of a step travel as one packed pinned buffer (q | K new | V
+    new | slots) and the results as one (out | lse)."""
     import torch
     from kv_cache_segment_gb300 import msa
     wl = case.wl
-    q_h = case.q.cpu().pin_memory()
-    kn_h = case.k_new.cpu().pin_memory()
-    vn_h = case.v_new.cpu().pin_memory()
-    slot_h = case.slot.cpu().pin_memory()
+    parts_in = [case.q, case.k_new, case.v_new, case.slot]
+    parts_out = [case.out, case.lse]
+
+    def layout(parts):
+        offs, o = [], 0
+        for t in parts:
+            offs.append(o)
+            o += -(-t.numel() * t.element_size() // 16) * 16  # 16-byte aligned pieces
+        return offs, o
+
+    in_off, in_bytes = layout(parts_in)
+    out_off, out_bytes = layout(parts_out)
+
+    def views(buf, parts, offs):
+        return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(parts, offs)]
+
+    in_h = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    for v, t in zip(views(in_h, parts_in, in_off), parts_in):
+        v.copy_(t.cpu())
     two = lambda f: [f(), f()]  # noqa: E731
-    out_h = two(lambda: torch.empty(case.out.shape, dtype=case.out.dtype).pin_memory())
-    lse_h = two(lambda: torch.empty(case.lse.shape, dtype=case.lse.dtype).pin_memory())
-    q_d = two(lambda: torch.empty_like(case.q))
-    kn_d, vn_d = two(lambda: torch.empty_like(case.k_new)), two(lambda: torch.empty_like(case.v_new))
-    slot_d = two(lambda: torch.empty_like(case.slot))
-    out_d, lse_d = two(lambda: torch.empty_like(case.out)), two(lambda: torch.empty_like(case.lse))
+    in_d = two(lambda: torch.empty(in_bytes, dtype=torch.uint8, device=dev))
+    out_d = two(lambda: torch.empty(out_bytes, dtype=torch.uint8, device=dev))
+    out_h = two(lambda: torch.empty(out_bytes, dtype=torch.uint8).pin_memory())
+    vin = [views(b, parts_in, in_off) for b in in_d]    # [q, k_new, v_new, slot] per set
+    vout = [views(b, parts_out, out_off) for b in out_d]  # [out, lse] per set
+    lse_h = [views(b, parts_out, out_off)[1] for b in out_h]
     ws = [case.sess.workspace, torch.empty_like(case.sess.workspace)]
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in, ev_attn, ev_out = two(torch.cuda.Event), two(torch.cuda.Event), two(torch.cuda.Event)
     table, lens = wl.block_table, wl.seq_lens
     indptr, ranges = wl.q_range_indptr, wl.q_ranges_flat
-    h2d = q_h.numel() * 2 + kn_h.numel() * 2 + vn_h.numel() * 2 + slot_h.numel() * 8
-    d2h = out_h[0].numel() * 2 + lse_h[0].numel() * 4
+    n_new = len(case.slot)
     dsplit, psplit, grid = case.info["decode_split"], case.info["prefill_split"], case.info["grid"]
     check = [0.0]
+    host_s = [0.0]
 
     def issue(i):
         """Plan, upload and launch step i on buffer set i % 2; returns (plan,
-        plan bytes, done event)."""
+        plan bytes)."""
+        t0 = time.perf_counter()
         b = i % 2
         # the split factors the session's plan was chosen with, reused: a
         # planner call per step stays as cheap as the default one
@@ -444,24 +468,28 @@ def e2e_leg(case, args, dev, stream):
         nbytes = msa.msa_plan_workspace_bytes(plan)
         if nbytes > ws[b].numel():
             raise RuntimeError("per-step plan larger than the session's workspace")
-        msa.msa_plan_upload(plan, ws[b], nbytes, stream)
-        q_d[b].copy_(q_h, non_blocking=True)
-        kn_d[b].copy_(kn_h, non_blocking=True)
-        vn_d[b].copy_(vn_h, non_blocking=True)
-        slot_d[b].copy_(slot_h, non_blocking=True)
-        msa.msa_append_kv(kn_d[b], vn_d[b], slot_d[b], len(slot_d[b]), case.kp, case.vp, case.kp.shape[0],
-                          case.dims, case.err, stream)
-        msa.msa_attention(q_d[b], case.kp, case.vp, case.kp.shape[0], plan, out_d[b], msa.MSA_OUT_BF16, lse_d[b],
-                          stream)
-        out_h[b].copy_(out_d[b], non_blocking=True)
-        lse_h[b].copy_(lse_d[b], non_blocking=True)
-        ev = torch.cuda.Event()
-        ev.record(stream)
-        return plan, nbytes, ev
+        h2d_s.wait_event(ev_attn[b])  # set b's inputs and workspace were read by step i-2
+        msa.msa_plan_upload(plan, ws[b], nbytes, h2d_s)
+        with torch.cuda.stream(h2d_s):
+            in_d[b].copy_(in_h, non_blocking=True)
+        ev_in[b].record(h2d_s)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])  # step i-2's results have left set b's output
+        q_d, kn_d, vn_d, slot_d = vin[b]
+        o_d, l_d = vout[b]
+        msa.msa_append_kv(kn_d, vn_d, slot_d, n_new, case.kp, case.vp, case.kp.shape[0], case.dims, case.err, stream)
+        msa.msa_attention(q_d, case.kp, case.vp, case.kp.shape[0], plan, o_d, msa.MSA_OUT_BF16, l_d, stream)
+        ev_attn[b].record(stream)
+        d2h_s.wait_event(ev_attn[b])
+        with torch.cuda.stream(d2h_s):
+            out_h[b].copy_(out_d[b], non_blocking=True)
+        ev_out[b].record(d2h_s)
+        host_s[0] += time.perf_counter() - t0
+        return plan, nbytes
 
     def finish(i, step):
-        plan, _, ev = step
-        ev.synchronize()  # step i's results are in host memory
+        plan, _ = step
+        ev_out[i % 2].synchronize()  # step i's results are in host memory
         check[0] += float(lse_h[i % 2][0, 0])  # the host reads them
         msa.msa_plan_destroy(plan)
 
@@ -477,21 +505,37 @@ def e2e_leg(case, args, dev, stream):
 
     run(max(3, args.warmup))
     torch.cuda.synchronize()
+    host_s[0] = 0.0
     t0 = time.perf_counter()
     plan_bytes = run(args.steps)
     dt = (time.perf_counter() - t0) / args.steps
+    torch.cuda.synchronize()
     # restore the session's own plan in its workspace
     msa.msa_plan_upload(case.sess.plan, ws[0], case.sess.ws_bytes, stream)
     torch.cuda.synchronize()
     if not math.isfinite(check[0]):
         raise RuntimeError("e2e leg read a non-finite lse")
+    # the last step's results, read back through the pipeline, are the bits
+    # the device-timed path computes with the same plan (the kernel is
+    # deterministic for a plan; the appended rows are the same every step)
+    case.append(stream)
+    case.attention(stream)
+    torch.cuda.synchronize()
+    o_h, l_h = views(out_h[(args.steps - 1) % 2], parts_out, out_off)
+    if not (torch.equal(o_h.view(torch.int16), case.out.cpu().view(torch.int16))
+            and torch.equal(l_h, case.lse.cpu())):
+        raise RuntimeError("e2e leg results differ from the device path's")
     val = (case.decode_bytes() + case.append_bytes) / dt / 1e9
+    h2d = sum(t.numel() * t.element_size() for t in parts_in)
+    d2h = sum(t.numel() * t.element_size() for t in parts_out)
     return {"value": round(val, 1), "unit": "GB/s", "ms_per_step": round(dt * 1e3, 4),
             "h2d_bytes_per_step": int(h2d + plan_bytes), "d2h_bytes_per_step": int(d2h),
+            "host_issue_us_per_step": round(host_s[0] / args.steps * 1e6, 1),
             "note": "per step: plan from host block tables (msa_plan_create_ex with the session's split factors) "
                     "uploaded, inputs up from pinned memory, append + attention, out + lse back to pinned "
                     "memory and read by the host; steps pipelined two deep (step i+1 issued before step i "
-                    "is waited for)"}
+                    "is waited for), copies on two copy streams overlapping the neighbouring steps' kernels; the last "
+                    "step's out and lse equal the device path's bit for bit"}
 
 
 def _plan_opts():
