@@ -292,14 +292,23 @@ def _sample_rows(wl, rng, per_seq=2):
     return np.unique(np.asarray(rows, np.int64))
 
 
+@pytest.mark.parametrize("plan", ["default", "chooser"])
 @pytest.mark.parametrize("idx", [2, 3, 4, 5])
-def test_full_size_configs_sampled(idx):
-    """The full workloads in the bench's launch configuration, checked on
-    sampled rows (first/last row of every sequence plus random ones)."""
+def test_full_size_configs_sampled(idx, plan):
+    """The full workloads, checked on sampled rows (first/last row of every
+    sequence plus random ones), under the default plan and under the plan
+    the bench times (split factors chosen by the latency model)."""
+    from kv_cache_segment_gb300 import costfit
+    opts = {}
+    if plan == "chooser":
+        params = costfit.load_params()
+        if params is None:
+            pytest.skip("no fitted latency-model constants")
+        opts = dict(choose_with=params)
     wl = W.config(idx)
     dev = torch.device("cuda")
     k, v, q = W.make_values(wl, device=dev)
-    out, lse, _ = run_gpu(wl, k, v, q)
+    out, lse, _ = run_gpu(wl, k, v, q, **opts)
     rng = np.random.default_rng(idx)
     rows = _sample_rows(wl, rng, per_seq=4 if idx != 4 else 6)
     if idx == 3:
