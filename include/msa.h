@@ -272,10 +272,12 @@ int msa_select_evictions(const msa_dims* dims, int32_t seq_len, const float* hit
  * each part is an item, and the parts are merged by log-sum-exp.  Parts
  * balance the CTAs but each costs a partial write, a merge share and a
  * pipeline start.  Adaptive chunking (AsymCache explainer, "核心方法 3"):
- * with choose_with set, the planner tries decode_split in {1, 1.5, 2, 3, 4,
- * 6}, then prefill_split in {1, 2, 4, 8}, and keeps the plan with the lowest
- * msa_plan_estimate time under those parameters.  msa_plan_info reports the
- * factors used.
+ * with choose_with set, the planner tries decode_split in {1, 1.5, 2, 3, 4}
+ * (prefill_split held at its given or default value), then, with the best
+ * of those, prefill_split in {1, 2, 4}, and keeps the plan with the lowest
+ * msa_plan_estimate time under those parameters (a factor is searched only
+ * when the plan has items of that kind).  msa_plan_info reports the factors
+ * used.
  */
 typedef struct {
     int32_t num_sms;        /* CTAs of the launch; 0 = the current device's SMs   */
@@ -298,10 +300,12 @@ int msa_plan_destroy(msa_plan_t plan);
  *                               v_pool[slot_mapping[t]] = v_new[t]
  * A bit copy.  Rows with slot -1 are skipped.
  *
- *   k_new, v_new    device bf16 [n, Hkv, D]
+ *   k_new, v_new    device bf16 [n, Hkv, D] (16-byte aligned)
  *   slot_mapping    device int64 [n]: pool row (block*16 + offset) or -1
- *   k_pool, v_pool  device bf16 [pool_tokens, Hkv, D]
- * A slot >= pool_tokens is not written; the kernel ORs MSA_DEVERR_SLOT into
+ *   k_pool, v_pool  device bf16 [pool_tokens, Hkv, D] (16-byte aligned)
+ * Rows move as 16-byte words: a misaligned k_new, v_new or pool pointer
+ * returns MSA_ERR_INVALID_ARG before anything is launched; n == 0 is a
+ * no-op.  A slot >= pool_tokens is not written; the kernel ORs MSA_DEVERR_SLOT into
  * `error_word` (device int32, may be NULL) instead.
  * Duplicate slots in one call race (one of the rows wins).
  */
