@@ -351,7 +351,9 @@ int msa_gather_kv(const void* k_pool, const void* v_pool, int64_t pool_tokens, c
  *   q            device bf16 [n_q, Hq, D], rows in the plan's packed order
  *                (16-byte aligned)
  *   k_pool, v_pool  device bf16 [pool_tokens, Hkv, D] (16-byte aligned)
- *   pool_tokens  rows in each pool; must cover every block the plan reads
+ *   pool_tokens  rows in each pool: below the highest row the plan reads
+ *                returns MSA_ERR_BAD_BLOCK_ID, above 2^31 - 1 (the TMA's
+ *                32-bit row coordinate) MSA_ERR_INVALID_ARG
  *   plan         an uploaded plan
  *   out          device [n_q, Hq, D], bf16 or fp32 per out_dtype (16-byte
  *                aligned); a misaligned q, pool or out pointer returns
