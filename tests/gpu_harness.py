@@ -59,3 +59,38 @@ def run_gpu(wl, k_log, v_log, q, out_fp32=False, num_sms=0, fill=float("nan"), *
 def oracle_ref(wl, k_log, v_log, q, rows=None):
     return oracle.dense_attention(wl.kv_indptr, k_log, v_log, wl.q_indptr, wl.q_pos, q, wl.num_q_heads,
                                   wl.num_kv_heads, wl.scale, rows=rows)
+
+
+def random_workload(seed):
+    """A small seeded workload with its shape drawn too: D in {64, 128},
+    Hkv in {1, 2, 4}, G = Hq/Hkv in {1, 2, 3, 4, 5, 8, 16} (at most 64 query
+    heads), 1-5 sequences of 0-1500 cached tokens in 1-8 segments, 1-3
+    disjoint query ranges per sequence (decode rows at p = L included; about
+    a third of the sequences decode-only, 1 to 16/G trailing rows), and
+    a plan option set (default, fine split, coarse).  N(0, 1) values as
+    everywhere else."""
+    rng = np.random.default_rng(10_000 + seed)
+    d = int(rng.choice([64, 128]))
+    hkv = int(rng.choice([1, 2, 4]))
+    g = int(rng.choice([G for G in (1, 2, 3, 4, 5, 8, 16) if hkv * G <= 64]))
+    n = int(rng.integers(1, 6))
+    lens, runs, ranges = [], [], []
+    for _ in range(n):
+        L = int(rng.integers(0, 1501)) if rng.random() > 0.1 else 0
+        nb = -(-L // 16)
+        lens.append(L)
+        runs.append(W._cut_sizes(rng, nb, int(rng.integers(1, 9))) if nb else [])
+        # 1-3 sorted disjoint ranges inside [0, L + 1); the last often ends at L + 1 (decode)
+        k = int(rng.integers(1, 4))
+        cuts = np.sort(rng.choice(np.arange(0, L + 2), size=min(2 * k, L + 2), replace=False))
+        rs = [(int(a), int(b)) for a, b in zip(cuts[0::2], cuts[1::2]) if b > a]
+        rs = [(a, min(b, a + 300)) for a, b in rs]
+        if rng.random() < 0.6 and (not rs or rs[-1][1] <= L):
+            rs.append((L, L + 1))
+        if rng.random() < 0.35:  # decode-only: the last 1 .. 16/G rows (the GQA-packed path)
+            t = int(rng.integers(1, 16 // g + 1))
+            rs = [(max(0, L + 1 - t), L + 1)]
+        ranges.append(rs or [(L, L + 1)])
+    opts = [dict(), dict(decode_split=12.0, prefill_split=16.0), dict(decode_split=1.0, prefill_split=1.0)][seed % 3]
+    wl = W.custom(lens, runs, ranges, hq=hkv * g, hkv=hkv, d=d, seed=20_000 + seed)
+    return wl, opts

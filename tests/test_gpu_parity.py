@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_harness import compare, oracle_ref, run_gpu
+from gpu_harness import compare, oracle_ref, random_workload, run_gpu
 from kv_cache_segment_gb300 import msa, workloads as W
 from kv_cache_segment_gb300.runner import MsaSession, append_kv
 
@@ -262,6 +262,17 @@ def test_running_max_moves(shape):
         wabs, _ = oracle_ref(wl, k, v.abs(), q)
         extra = 2.0 ** -8 * wabs
     compare(out, lse, ro, rl, shape, extra=extra)
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_random_workloads_match_oracle(seed):
+    """Seeded random shapes, layouts, query ranges and split options
+    (gpu_harness.random_workload) against the oracle."""
+    wl, opts = random_workload(seed)
+    k, v, q = W.make_values(wl)
+    out, lse, _ = run_gpu(wl, k, v, q, **opts)
+    ro, rl = oracle_ref(wl, k, v, q)
+    compare(out, lse, ro, rl, f"random {seed}: {wl.num_q_heads}/{wl.num_kv_heads} heads, D={wl.head_dim}, {opts}")
 
 
 def test_repeat_calls_are_identical():
