@@ -6,7 +6,6 @@ marshals arguments; all work runs in libmsa.
 """
 from __future__ import annotations
 
-import numpy as np
 
 from . import msa
 

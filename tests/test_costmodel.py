@@ -2,7 +2,6 @@
 Python restatement in oracle/costmodel.py, and both against closed forms."""
 import math
 
-import numpy as np
 import pytest
 
 import oracle.costmodel as OC

@@ -2,7 +2,6 @@
 
 Tolerance (bf16 in, fp32 accumulate): every out element within
 2e-3 + 1e-2*|ref|, lse within 1e-4 absolute; pool scatter bit-exact."""
-import math
 
 import numpy as np
 import pytest

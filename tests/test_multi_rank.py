@@ -4,7 +4,6 @@ collective; only the final timing reduction crosses ranks."""
 import os
 import socket
 
-import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
