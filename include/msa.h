@@ -290,6 +290,11 @@ int msa_plan_create_ex(const msa_dims* dims, int32_t num_seqs, int32_t max_block
                        const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_range_indptr,
                        const int32_t* q_ranges, const msa_plan_options* opts, msa_plan_t* out);
 
+/* Free a plan (NULL is a no-op).  The host memory of up to two destroyed
+ * plans is kept per calling thread and reused by that thread's next
+ * msa_plan_create(_ex): a loop that plans every step then works in memory
+ * it has already touched.  The workspace is the caller's and is not
+ * touched. */
 int msa_plan_destroy(msa_plan_t plan);
 
 /*

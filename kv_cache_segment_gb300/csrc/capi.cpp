@@ -20,9 +20,12 @@ int device_sm_count() {
 
 }  // namespace msa
 
-static_assert(msa::kErrTimeoutProducer == MSA_DEVERR_TIMEOUT_PRODUCER && msa::kErrTimeoutMma == MSA_DEVERR_TIMEOUT_MMA &&
-                  msa::kErrTimeoutCompute == MSA_DEVERR_TIMEOUT_COMPUTE && msa::kErrBadIndex == MSA_DEVERR_BAD_INDEX &&
-                  msa::kErrAppendSlot == MSA_DEVERR_SLOT && msa::kErrTmemAlloc == MSA_DEVERR_TMEM_ALLOC,
+constexpr bool same_bit(int a, int b) { return a == b; }
+static_assert(same_bit(msa::kErrTimeoutProducer, MSA_DEVERR_TIMEOUT_PRODUCER) &&
+                  same_bit(msa::kErrTimeoutMma, MSA_DEVERR_TIMEOUT_MMA) &&
+                  same_bit(msa::kErrTimeoutCompute, MSA_DEVERR_TIMEOUT_COMPUTE) &&
+                  same_bit(msa::kErrBadIndex, MSA_DEVERR_BAD_INDEX) && same_bit(msa::kErrAppendSlot, MSA_DEVERR_SLOT) &&
+                  same_bit(msa::kErrTmemAlloc, MSA_DEVERR_TMEM_ALLOC),
               "device error bits must match msa.h");
 
 extern "C" {
@@ -113,7 +116,7 @@ int msa_plan_get_items(msa_plan_t plan, int32_t* items, int32_t* n_items) {
 }
 
 int msa_plan_destroy(msa_plan_t plan) {
-    delete plan;
+    msa::plan_release(plan);
     return MSA_OK;
 }
 

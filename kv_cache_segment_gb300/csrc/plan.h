@@ -33,7 +33,34 @@ struct msa_plan_s {
     void* workspace = nullptr;   // set by msa_plan_upload
     size_t workspace_bytes = 0;
     msa_plan_info info{};
+
+    // Back to the state of a new plan, keeping the vectors' storage (see
+    // plan_release).  Every field above must be reset here.
+    void reset() {
+        dims = msa_dims{};
+        num_seqs = 0;
+        G = 1;
+        dec_rows = 16;
+        grid = 1;
+        max_pool_row = 0;
+        n_dec_slots = n_pre_slots = 0;
+        seq_lens.clear();
+        run_indptr.clear();
+        runs.clear();
+        row_indptr.clear();
+        pos.clear();
+        groups.clear();
+        items.clear();
+        order.clear();
+        lay = msa::WsLayout{};
+        image.clear();
+        workspace = nullptr;
+        workspace_bytes = 0;
+        info = msa_plan_info{};
+    }
 };
+// A field added to msa_plan_s must also be reset in reset().
+static_assert(sizeof(msa_plan_s) == 504, "msa_plan_s changed: update reset()");
 
 namespace msa {
 
@@ -44,6 +71,13 @@ namespace msa {
 // item a pipeline start and an epilogue.
 constexpr double kDefaultDecodeSplit = 3.0;
 constexpr double kDefaultPrefillSplit = 4.0;
+
+// Plans are recycled per thread: plan_release keeps a destroyed plan (its
+// vectors emptied but their storage kept) for the next plan_alloc on the
+// same thread, so a loop that plans every step reuses memory it has already
+// touched instead of faulting in fresh pages.
+msa_plan_s* plan_alloc();
+void plan_release(msa_plan_s* P);
 
 // An output group before its key range is cut into work items.
 struct Pending {

@@ -38,6 +38,14 @@ static int validate_dims(const msa_dims* d) {
     return MSA_OK;
 }
 
+namespace {
+constexpr size_t kRecycledPlans = 2;
+thread_local std::vector<std::unique_ptr<msa_plan_s>> t_recycled;
+// scratch of plan_create / split_items, kept per thread for the same reason
+thread_local std::vector<Pending> t_pend;
+thread_local std::vector<double> t_cost;
+}  // namespace
+
 // Number of KV tiles the kernels walk over keys [kb, ke): 128-key windows
 // of the logical key range starting at kb (a window may span segments).
 static int64_t count_tiles(int32_t kb, int32_t ke) {
@@ -74,7 +82,11 @@ void split_items(msa_plan_s* P, const std::vector<Pending>& pend, double dec_spl
     const double per_cta = total / P->grid;
     const int64_t min_tiles[2] = {4, 8};
 
-    std::vector<double> cost;
+    std::vector<double>& cost = t_cost;
+    cost.clear();
+    P->groups.reserve(pend.size());
+    P->items.reserve(pend.size() * 2);
+    cost.reserve(pend.size() * 2);
     for (size_t gi = 0; gi < pend.size(); ++gi) {
         const Pending& pd = pend[gi];
         const int32_t kind = pd.g.kind;
@@ -126,6 +138,26 @@ void split_items(msa_plan_s* P, const std::vector<Pending>& pend, double dec_spl
     std::stable_sort(P->order.begin(), P->order.end(), [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
 }
 
+
+msa_plan_s* plan_alloc() {
+    if (!t_recycled.empty()) {
+        msa_plan_s* P = t_recycled.back().release();
+        t_recycled.pop_back();
+        return P;
+    }
+    return new (std::nothrow) msa_plan_s();
+}
+
+void plan_release(msa_plan_s* P) {
+    if (!P) return;
+    if (t_recycled.size() >= kRecycledPlans) {
+        delete P;
+        return;
+    }
+    P->reset();
+    t_recycled.emplace_back(P);
+}
+
 int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
                 const int32_t* table, const int32_t* seq_lens, const int32_t* q_range_indptr,
                 const int32_t* q_ranges, int32_t num_sms, const msa_plan_options* opts, msa_plan_s** out) {
@@ -145,9 +177,9 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
         if (num_sms <= 0) return MSA_ERR_CUDA;
     }
 
-    msa_plan_s* P = new (std::nothrow) msa_plan_s();
+    msa_plan_s* P = plan_alloc();
     if (!P) return MSA_ERR_INVALID_ARG;
-    std::unique_ptr<msa_plan_s> guard(P);
+    std::unique_ptr<msa_plan_s, void (*)(msa_plan_s*)> guard(P, plan_release);
     P->dims = *dims;
     P->num_seqs = num_seqs;
     P->G = dims->num_q_heads / dims->num_kv_heads;
@@ -189,18 +221,27 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
         if (q_range_indptr[0] != 0) return MSA_ERR_BAD_Q_RANGE;
         if (q_range_indptr[num_seqs] > 0 && !q_ranges) return MSA_ERR_INVALID_ARG;
     }
-    P->row_indptr.assign(1, 0);
+    // validate the ranges and count the rows, then lay the positions out
+    int64_t n_rows = 0;
     for (int32_t s = 0; s < num_seqs; ++s) {
         const int32_t a = q_range_indptr[s], b = q_range_indptr[s + 1];
         if (b < a) return MSA_ERR_BAD_Q_RANGE;
         int64_t prev_end = 0;
         for (int32_t i = a; i < b; ++i) {
             const int32_t st = q_ranges[2 * i], en = q_ranges[2 * i + 1];
-            if (st < 0 || en <= st || en > seq_lens[s] + 1 || st < prev_end) return MSA_ERR_BAD_Q_RANGE;
+            if (st < 0 || en <= st || (int64_t)en > (int64_t)seq_lens[s] + 1 || st < prev_end)
+                return MSA_ERR_BAD_Q_RANGE;
             prev_end = en;
-            if ((int64_t)P->pos.size() + (en - st) > (int64_t)INT32_MAX / 2) return MSA_ERR_INVALID_ARG;
-            for (int32_t p = st; p < en; ++p) P->pos.push_back(p);
+            n_rows += en - st;
+            if (n_rows > (int64_t)INT32_MAX / 2) return MSA_ERR_INVALID_ARG;
         }
+    }
+    P->row_indptr.assign(1, 0);
+    P->row_indptr.reserve((size_t)num_seqs + 1);
+    P->pos.reserve((size_t)n_rows);
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        for (int32_t i = q_range_indptr[s]; i < q_range_indptr[s + 1]; ++i)
+            for (int32_t p = q_ranges[2 * i]; p < q_ranges[2 * i + 1]; ++p) P->pos.push_back(p);
         P->row_indptr.push_back((int32_t)P->pos.size());
     }
     const int32_t n_q = (int32_t)P->pos.size();
@@ -208,7 +249,16 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
     // ---- output groups ----------------------------------------------------
     // A sequence's trailing rows go to the GQA-packed decode path when they
     // number at most kDecRows / G; everything else is cut into 128-row tiles.
-    std::vector<Pending> pend;
+    std::vector<Pending>& pend = t_pend;
+    pend.clear();
+    {
+        size_t n_groups = 0;  // capacity hint: at most one decode group per kv head plus the 128-row tiles
+        for (int32_t s = 0; s < num_seqs; ++s) {
+            const int32_t n = P->row_indptr[s + 1] - P->row_indptr[s];
+            n_groups += (size_t)(n / kTileRows + 2) * (size_t)std::max(Hkv, Hq);
+        }
+        pend.reserve(n_groups);
+    }
     double prefill_flops = 0.0;
     int64_t dec_kv = 0, dec_qo = 0;
     int32_t dec_rows_total = 0, pre_rows_total = 0;

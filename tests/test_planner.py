@@ -224,3 +224,34 @@ def test_restricted_rows_partition_the_plan(idx):
     full, di, pi = infos
     assert di["decode_kv_bytes"] == full["decode_kv_bytes"] and di["prefill_flops"] == 0
     assert pi["decode_kv_bytes"] == 0 and pi["prefill_flops"] == pytest.approx(full["prefill_flops"], rel=1e-12)
+
+
+def _plan_state(plan, n_seqs):
+    info = msa.msa_plan_get_info(plan)
+    info.pop("host_plan_us")
+    return (info, msa.msa_plan_workspace_bytes(plan), msa.msa_plan_get_items(plan).tolist(),
+            msa.msa_plan_get_order(plan).tolist(), [msa.msa_plan_get_runs(plan, s).tolist() for s in range(n_seqs)])
+
+
+def test_recycled_plans_equal_fresh_ones():
+    """msa_plan_destroy keeps freed plans' storage for the next create on the
+    thread: a plan built on recycled storage (after a large plan, a small
+    one, and a create that failed part-way) equals one built before."""
+    small = W.small_config(5)
+    want = []
+    for wl in (small, W.small_config(3)):
+        p = _plan(wl)
+        want.append(_plan_state(p, wl.num_seqs))
+        msa.msa_plan_destroy(p)
+    big = _plan(W.config(3))
+    big2 = _plan(W.config(5))
+    msa.msa_plan_destroy(big)
+    msa.msa_plan_destroy(big2)
+    dims = msa.make_dims(8, 2, 128)
+    with pytest.raises(msa.MsaError):  # fails after its runs were built
+        msa.msa_plan_create(dims, np.array([[0, 1]], np.int32), np.array([20], np.int32), np.array([0, 1], np.int32),
+                            np.array([5, 3], np.int32), NSM)
+    for wl, w in zip((small, W.small_config(3)), want):
+        p = _plan(wl)
+        assert _plan_state(p, wl.num_seqs) == w
+        msa.msa_plan_destroy(p)
