@@ -863,8 +863,12 @@ def reference_main(args):
             vals.append(r)
     value = float(np.mean([r["value"] for r in vals]))
     cores = vals[-1]["cores"]
+    # a full step of the workload (its algorithmic K/V + q/out/lse bytes) at the oracle's rate
+    kv = sum(int(wl.seq_lens[s]) for s in range(wl.num_seqs))
+    step_bytes = kv * wl.num_kv_heads * wl.head_dim * 4 + wl.num_q_rows * wl.num_q_heads * (wl.head_dim * 4 + 4)
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(step_bytes / (value * 1e9) * 1e3, 1), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "batched_decode: 32 seqs x 1 decode row, 32/8 heads, D=128, block 16, "
                                    "L~U{2048..16384}, 1-8 segments/seq in a 4M-token pool"},
