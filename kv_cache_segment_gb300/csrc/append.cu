@@ -47,8 +47,7 @@ __global__ void __launch_bounds__(256) append_kv_kernel(const uint4* __restrict_
 int launch_append_kv(const void* k_new, const void* v_new, const int64_t* slot, int32_t n, void* k_pool,
                      void* v_pool, int64_t pool_tokens, int32_t row_elems, int32_t* error_word,
                      msa_stream_t stream) {
-    static int sms = 0;
-    if (sms == 0) sms = device_sm_count();
+    static const int sms = device_sm_count();  // grid cap only (thread-safe static)
     if (sms <= 0) return MSA_ERR_CUDA;
     const int32_t row_chunks = row_elems * 2 / 16;  // 16-byte chunks per token row
     const int warps_per_block = 8;
@@ -95,8 +94,7 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(const uint4* __restrict_
 
 int launch_gather_kv(const void* k_pool, const void* v_pool, int64_t pool_tokens, const int64_t* slot, int32_t n,
                      void* k_out, void* v_out, int32_t row_elems, int32_t* error_word, msa_stream_t stream) {
-    static int sms = 0;
-    if (sms == 0) sms = device_sm_count();
+    static const int sms = device_sm_count();  // grid cap only (thread-safe static)
     if (sms <= 0) return MSA_ERR_CUDA;
     const int32_t row_chunks = row_elems * 2 / 16;
     const int warps_per_block = 8;

@@ -36,6 +36,7 @@
 // Launch with decode items only (7 warps): K producer, V producer, the four
 // decode warps, the merge warp.
 #include <cuda.h>
+#include <atomic>
 #include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -1270,16 +1271,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder, looked up once (thread-safe static).
 static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    static const EncodeTiledFn fn = [] {
         void* ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
+            return reinterpret_cast<EncodeTiledFn>(ptr);
+        return EncodeTiledFn(nullptr);
+    }();
     return fn;
 }
 
@@ -1297,28 +1299,41 @@ static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Launch attributes of one kernel instantiation on the current device (a
+// function attribute belongs to the device it was set on): done once per
+// device, bit d of `done` marking device d.
+template <int D, bool DEC>
+static int configure_current_device() {
+    using C = Cfg<D, DEC>;
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MSA_ERR_CUDA;
+    const uint64_t bit = uint64_t(1) << dev;
+    if (done.load(std::memory_order_acquire) & bit) return MSA_OK;
+    if (cudaFuncSetAttribute(msa_attention_kernel<D, DEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
+        cudaSuccess)
+        return MSA_ERR_CUDA;
+    if (!DEC) {
+        // The register split only balances if the kernel launches with
+        // exactly kRegsLaunch registers per thread; otherwise a growing
+        // warpgroup would wait for registers that never come.  Refuse.
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, msa_attention_kernel<D, DEC>) != cudaSuccess ||
+            fa.numRegs != C::kRegsLaunch) {
+            fprintf(stderr, "libmsa: attention kernel has %d registers per thread, expected %d\n", fa.numRegs,
+                    C::kRegsLaunch);
+            return MSA_ERR_CUDA;
+        }
+    }
+    done.fetch_or(bit, std::memory_order_release);
+    return MSA_OK;
+}
+
 template <int D, bool DEC>
 static int launch_d(const msa_plan_s* P, const AttnParams& prm, const CUtensorMap* maps, cudaStream_t st) {
     using C = Cfg<D, DEC>;
-    static bool configured = false;
-    if (!configured) {
-        if (cudaFuncSetAttribute(msa_attention_kernel<D, DEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmem) != cudaSuccess)
-            return MSA_ERR_CUDA;
-        if (!DEC) {
-            // The register split only balances if the kernel launches with
-            // exactly kRegsLaunch registers per thread; otherwise a growing
-            // warpgroup would wait for registers that never come.  Refuse.
-            cudaFuncAttributes fa;
-            if (cudaFuncGetAttributes(&fa, msa_attention_kernel<D, DEC>) != cudaSuccess ||
-                fa.numRegs != C::kRegsLaunch) {
-                fprintf(stderr, "libmsa: attention kernel has %d registers per thread, expected %d\n", fa.numRegs,
-                        C::kRegsLaunch);
-                return MSA_ERR_CUDA;
-            }
-        }
-        configured = true;
-    }
+    const int rc = configure_current_device<D, DEC>();
+    if (rc != MSA_OK) return rc;
     msa_attention_kernel<D, DEC>
         <<<P->grid, C::kThreads, C::kSmem, st>>>(prm, maps[0], maps[1], maps[2], maps[3], maps[4]);
     return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
