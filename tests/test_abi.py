@@ -78,3 +78,24 @@ def test_argument_checks_return_before_any_device_work():
         assert lib.msa_attention(A, A, A, 64, plan, A, 0, None, None) == msa.MSA_ERR_NOT_UPLOADED
     finally:
         msa.msa_plan_destroy(plan)
+
+
+def test_tensor_checks_of_the_python_wrapper():
+    """runner.check_tensor, which MsaSession.attention and append_kv apply to
+    every tensor before a pointer crosses the ABI."""
+    import pytest
+    import torch
+    from kv_cache_segment_gb300.runner import check_tensor
+    t = torch.zeros((5, 4, 64), dtype=torch.bfloat16)
+    check_tensor(t, "t", (torch.bfloat16,), (5, 4, 64))
+    check_tensor(t, "t", (torch.bfloat16,), (None, 4, 64))
+    with pytest.raises(TypeError):
+        check_tensor(t.float(), "t", (torch.bfloat16,), (5, 4, 64))
+    with pytest.raises(ValueError):
+        check_tensor(t, "t", (torch.bfloat16,), (5, 4, 128))
+    with pytest.raises(ValueError):
+        check_tensor(t, "t", (torch.bfloat16,), (5, 4))
+    with pytest.raises(ValueError):
+        check_tensor(t.transpose(0, 1), "t", (torch.bfloat16,), (4, 5, 64))
+    with pytest.raises(ValueError):
+        check_tensor(t, "t", (torch.bfloat16,), (5, 4, 64), torch.device("meta"))

@@ -355,6 +355,36 @@ def test_misaligned_pointers_are_rejected_before_launch():
         sess.close()
 
 
+def test_wrong_tensors_are_refused_before_launch():
+    """MsaSession.attention / append_kv check dtype, shape, contiguity and
+    device of every tensor: a mis-shaped lse would otherwise be written past
+    its end."""
+    wl = W.small_config(2)
+    k, v, q = W.make_values(wl)
+    dev = torch.device("cuda")
+    kp, vp = W.make_pool(wl, k.to(dev), v.to(dev))
+    sess = MsaSession.from_workload(wl)
+    try:
+        qd = q.to(dev)
+        n_q, hq = qd.shape[0], qd.shape[1]
+        with pytest.raises(TypeError):
+            sess.attention(qd.half(), kp, vp)
+        with pytest.raises(ValueError):
+            sess.attention(qd, kp, vp, lse=torch.empty((n_q - 1, hq), dtype=torch.float32, device=dev))
+        with pytest.raises(ValueError):
+            sess.attention(qd[:-1], kp, vp)
+        with pytest.raises(ValueError):
+            sess.attention(qd, kp.transpose(1, 2).contiguous().transpose(1, 2), vp)
+        with pytest.raises(ValueError):
+            sess.attention(qd, kp, vp[:-1])
+        with pytest.raises(ValueError):
+            append_kv(kp[:4], vp[:4], torch.zeros(3, dtype=torch.int64, device=dev), kp, vp, sess.dims)
+        torch.cuda.synchronize()
+        assert sess.check_device()[0] == 0
+    finally:
+        sess.close()
+
+
 def test_bounded_wait_runs_out_and_the_context_survives():
     """A wait on a barrier nothing arrives at gives up after its limit, the
     error bit reaches the host, a second waiter leaves on the abort flag, and
