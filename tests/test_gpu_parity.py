@@ -274,6 +274,54 @@ def test_random_workloads_match_oracle(seed):
     compare(out, lse, ro, rl, f"random {seed}: {wl.num_q_heads}/{wl.num_kv_heads} heads, D={wl.head_dim}, {opts}")
 
 
+@pytest.mark.parametrize("idx", [3, 5])
+def test_cuda_graph_replay_equals_eager(idx):
+    """append + attention captured once in a CUDA graph and replayed: the
+    calls neither synchronise nor allocate, and the kernel resets its own
+    queue and merge counters, so every replay gives the eager call's bits
+    (split groups included: many CTAs force them)."""
+    wl = W.small_config(idx)
+    k, v, q = W.make_values(wl)
+    dev = torch.device("cuda")
+    kp, vp = W.make_pool(wl, k.to(dev), v.to(dev))
+    sess = MsaSession.from_workload(wl, num_sms=1000)
+    try:
+        assert sess.info["num_items"] > sess.info["num_groups"]
+        qd = q.to(dev)
+        # re-append the first 8 cached rows of sequence 0 (same values: the result is unchanged)
+        assert int(wl.seq_lens[0]) >= 8
+        s0 = int(wl.kv_indptr[0])
+        rows = torch.arange(8)
+        slot = torch.as_tensor([int(wl.block_table[0][r // 16]) * 16 + r % 16 for r in rows.tolist()],
+                               dtype=torch.int64, device=dev)
+        kn, vn = k[s0:s0 + 8].to(dev).contiguous(), v[s0:s0 + 8].to(dev).contiguous()
+        out = torch.empty((wl.num_q_rows, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((wl.num_q_rows, wl.num_q_heads), dtype=torch.float32, device=dev)
+        side = torch.cuda.Stream()
+        sess.stream = side
+        with torch.cuda.stream(side):
+            append_kv(kn, vn, slot, kp, vp, sess.dims, stream=side)
+            sess.attention(qd, kp, vp, out=out, lse=lse)
+        side.synchronize()
+        want_o, want_l = out.clone(), lse.clone()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            append_kv(kn, vn, slot, kp, vp, sess.dims, stream=side)
+            sess.attention(qd, kp, vp, out=out, lse=lse)
+        for _ in range(3):
+            out.zero_()
+            lse.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(out.view(torch.int16), want_o.view(torch.int16))
+            assert torch.equal(lse, want_l)
+        assert sess.check_device()[0] == 0
+        ro, rl = oracle_ref(wl, k, v, q)
+        compare(out, lse, ro, rl, "graph replay")
+    finally:
+        sess.close()
+
+
 def test_repeat_calls_are_identical():
     """Merge counters reset themselves: back-to-back calls give the same bits."""
     wl = W.small_config(2)
