@@ -800,7 +800,34 @@ def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
     out["segmentation_overhead"] = over
     out["gather_then_attention"] = gathers
     out["eviction_policies"] = eviction_leg(dev, stream, steps, warm)
+    out["decode_shapes"] = decode_shapes_leg(dev, stream, peaks, steps, warm, rank)
     return out
+
+
+# Batched decode (the headline's length and segment draws) at other GQA
+# ratios and head dimensions: (Hq, Hkv, D, sequences, pool tokens).  Each is
+# sized so that the launch runs ~0.35-0.7 ms: a ~0.12 ms launch loses ~15-20 %
+# to its fixed start and tail, which says nothing about the streaming rate.
+DECODE_SHAPES = ((32, 32, 128, 32, 1 << 21), (64, 4, 128, 128, 1 << 23), (32, 8, 64, 128, 1 << 23),
+                 (8, 8, 64, 128, 1 << 23))
+
+
+def decode_shapes_leg(dev, stream, peaks, steps, warm, rank):
+    """Decode HBM rate of the kernel across G = Hq/Hkv in {1, 16} and D = 64."""
+    import torch
+    from kv_cache_segment_gb300 import workloads as W
+    res = []
+    for hq, hkv, d, n, pool in DECODE_SHAPES:
+        wl = W.batched_decode(seed=1002 + 1000 * rank, num_seqs=n, hq=hq, hkv=hkv, d=d, pool_tokens=pool)
+        case = Case(wl, dev, plan_opts=_plan_opts())
+        _, ms = time_case(case, steps, warm, stream, with_append=False)
+        gbs = case.decode_bytes() / (ms * 1e-3) / 1e9
+        res.append({"hq": hq, "hkv": hkv, "head_dim": d, "G": hq // hkv, "seqs": n, "attention_ms": round(ms, 4),
+                    "decode_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+                    "items": int(case.info["num_items"])})
+        del case
+        torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------- CPU legs --
