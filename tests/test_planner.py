@@ -255,3 +255,23 @@ def test_recycled_plans_equal_fresh_ones():
         p = _plan(wl)
         assert _plan_state(p, wl.num_seqs) == w
         msa.msa_plan_destroy(p)
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_random_workloads_coverage(seed):
+    """The GPU parity test's seeded random shapes (GQA ratios 1-16, D 64/128,
+    empty sequences, 1-8 segments, 1-3 query ranges, split options): runs
+    equal the drawn layout and every (row, head, visible key) is covered
+    exactly once, under the split factors the GPU test uses."""
+    from gpu_harness import random_workload
+    wl, opts = random_workload(seed)
+    dims = msa.make_dims(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, 16, wl.scale)
+    plan = msa.msa_plan_create_ex(dims, wl.block_table, wl.seq_lens, wl.q_range_indptr, wl.q_ranges_flat, NSM,
+                                  opts.get("decode_split", 0.0), opts.get("prefill_split", 0.0))
+    try:
+        for s in range(wl.num_seqs):
+            got = msa.msa_plan_get_runs(plan, s)
+            assert [tuple(int(x) for x in g) for g in got] == [tuple(r) for r in wl.runs_drawn[s]]
+        _check_coverage(wl, plan)
+    finally:
+        msa.msa_plan_destroy(plan)
