@@ -162,9 +162,10 @@ int msa_plan_get_info(msa_plan_t plan, msa_plan_info* info);
 
 /* Host copy of the work list, for tests: items[9*i + 0..8] =
  * (kind 0=decode 1=prefill, seq, head (kv head for decode, first query
- * head for prefill), query heads covered (G for decode, 1 or 2 consecutive
- * heads for prefill), first packed row, number of rows, key begin, key end,
- * part).  With items == NULL only *n_items is written. */
+ * head for prefill), query heads covered (G for decode; for prefill 2
+ * consecutive heads over at most 128 rows, or, when Hq/Hkv is odd, 1 head
+ * over at most 256 rows), first packed row, number of rows, key begin, key
+ * end, part).  With items == NULL only *n_items is written. */
 int msa_plan_get_items(msa_plan_t plan, int32_t* items, int32_t* n_items);
 
 /* The plan's processing order: order[q] = index (into the msa_plan_get_items
@@ -180,7 +181,7 @@ int msa_plan_get_order(msa_plan_t plan, int32_t* order, int32_t* n_items);
  *
  * Each work item runs two phases on the CTA that takes it:
  *   fixed phase (time):
- *     decode : dec_item_us            prefill: pre_item_us + pre_tile_us * tiles * heads
+ *     decode : dec_item_us            prefill: pre_item_us + pre_tile_us * tiles * qtiles
  *     + box_us * extra_boxes + dec_merge_us / pre_merge_us (if its group is
  *       split into parts: a decode part's partial is 16 rows, a prefill
  *       part's 128 rows x 1 or 2 heads, and the last part merges them all)
@@ -188,8 +189,9 @@ int msa_plan_get_order(msa_plan_t plan, int32_t* order, int32_t* n_items);
  *     (K and V); every CTA in a stream phase progresses at
  *     min(dec_cta_gbs, dec_gbs / number of CTAs in a stream phase), so the
  *     CTAs share HBM and the last ones run faster.
- * tiles = 128-key windows the item walks; heads = 1 or 2 query heads of a
- * prefill item; extra_boxes = TMA boxes beyond one per tile (a tile that is
+ * tiles = 128-key windows the item walks; qtiles = the prefill item's query
+ * tiles of 128 rows x one head (1 or 2: two heads of one kv head, or for an
+ * odd Hq/Hkv one head over two consecutive row tiles); extra_boxes = TMA boxes beyond one per tile (a tile that is
  * not a full 128-key window inside one segment is fetched one 16-key block
  * at a time).  Items are handed out in the plan's order to `grid` CTAs, a
  * CTA taking the next one when it becomes free (several freed at once take
@@ -217,7 +219,7 @@ typedef struct {
     int64_t n_items;
     int64_t n_split_items;   /* items of groups split into several parts      */
     int64_t decode_tiles;    /* sum over decode items of their tiles          */
-    int64_t prefill_tile_heads; /* sum over prefill items of tiles * heads    */
+    int64_t prefill_tile_heads; /* sum over prefill items of tiles * qtiles   */
     int64_t extra_boxes;     /* see above                                     */
     int64_t stream_bytes;    /* sum of the decode items' stream phases        */
     int64_t decode_kv_bytes; /* as msa_plan_info                              */
@@ -370,7 +372,8 @@ int msa_gather_kv(const void* k_pool, const void* v_pool, int64_t pool_tokens, c
  * Decode rows (a sequence's trailing rows when they number at most 16/G)
  * are served GQA-packed: one work item reads a K/V chunk of one kv head
  * once for all G query heads.  Other rows go in tiles of 128 rows per
- * query head on the tensor cores.  Items whose sequence was split for SM
+ * query head on the tensor cores, two tiles sharing each K/V chunk (two
+ * heads of a kv head, or for odd Hq/Hkv two row tiles of one head).  Items whose sequence was split for SM
  * balance write partial (output, lse) pairs to the workspace; the last item
  * of a group to finish merges them by log-sum-exp and writes out/lse.
  * A kernel that hits an internal time limit or a bad index records a code

@@ -153,6 +153,20 @@ __device__ __forceinline__ bool wait_bar(const AttnParams& p, Ctl* ctl, uint64_t
     return false;
 }
 
+// Query tile k (0 or 1) of a prefill group: for G even the two tiles are
+// two query heads of one kv head over the same rows; for odd G they are two
+// consecutive 128-row tiles of one head.  Either way both share the group's
+// K/V tiles, so the two softmax warpgroups alternate on the tensor core.
+__device__ __forceinline__ int qtile_head(const AttnParams& p, const Group& g, int k) {
+    return g.head + ((p.G & 1) ? 0 : k);
+}
+__device__ __forceinline__ int qtile_row0(const AttnParams& p, const Group& g, int k) {
+    return g.row0 + ((p.G & 1) ? k * kTileRows : 0);
+}
+__device__ __forceinline__ int qtile_rows(const AttnParams& p, const Group& g, int k) {
+    return (p.G & 1) ? min(kTileRows, g.nrows - k * kTileRows) : g.nrows;
+}
+
 // Sum of the two bf16 values packed in w, as fp32 (exact).
 __device__ __forceinline__ float bf16x2_sum(uint32_t w) {
     return __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
@@ -257,13 +271,13 @@ __device__ void producer(const AttnParams& p, uint8_t* smem, Ctl* ctl, const CUt
         if (!DEC && it.kind == kPrefill) {
             kvh = g.head / p.G;
             if (KSIDE) {
-                const int nh = g.pad;  // query heads of the item: 1 or 2 (consecutive, same kv head)
+                const int nh = g.pad;  // query tiles of the item: 1 or 2 (see qtile_head)
                 if (!wait_bar(p, ctl, &ctl->q_empty, (q_cnt & 1) ^ 1, code)) goto drain;
                 ptx::mbar_arrive_expect_tx(&ctl->q_full, nh * C::kTileBytes);
                 for (int k = 0; k < nh; ++k)
                     for (int pn = 0; pn < C::kPanels; ++pn)
                         ptx::tma_load_3d(smem + C::kOffQ + k * C::kTileBytes + pn * C::kPanelBytes, tmQ, pn * 64,
-                                         g.head + k, g.row0, &ctl->q_full);
+                                         qtile_head(p, g, k), qtile_row0(p, g, k), &ctl->q_full);
                 ++q_cnt;
             }
         }
@@ -354,10 +368,9 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
     const uint32_t lQ = (uint32_t)dQ;
     const uint32_t lK = (uint32_t)ptx::smem_desc(ptx::smem_u32(smem + C::kOffK), 16, 1024, 2);
     const uint32_t lV = (uint32_t)ptx::smem_desc(ptx::smem_u32(smem + C::kOffV), C::kPanelBytes, 1024, 2);
-    // P-ready phases per head; O-done phases (one per item: the items of a
-    // plan all have the same number of heads, so both heads' barriers move
-    // together or only head 0's is used)
-    uint32_t kv_cnt = 0, q_cnt = 0, pf0 = 0, pf1 = 0, oc = 0, n_taken = 0;
+    // P-ready phases per query tile; O-free phases per query tile (tile 1's
+    // barrier only moves in items that have a second tile)
+    uint32_t kv_cnt = 0, q_cnt = 0, pf0 = 0, pf1 = 0, oc0 = 0, oc1 = 0, n_taken = 0;
 
     for (;;) {
         const int ii = take_item_w(p, ctl, n_taken, kErrTimeoutMma, lane);
@@ -387,7 +400,9 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
                     if (k) ++pf1; else ++pf0;
                     if (k == 0 && !wait_bar_w(p, ctl, &ctl->v_full[stp], (kp / C::kStages) & 1, kErrTimeoutMma))
                         return;
-                    if (jj == 0 && !wait_bar_w(p, ctl, &ctl->o_empty[k], (oc & 1) ^ 1, kErrTimeoutMma)) return;
+                    if (jj == 0 &&
+                        !wait_bar_w(p, ctl, &ctl->o_empty[k], ((k ? oc1 : oc0) & 1) ^ 1, kErrTimeoutMma))
+                        return;
                     ptx::tc_fence_after();
                     const uint32_t vl = lV + (uint32_t)((stp * C::kTileBytes) >> 4);
                     const uint32_t to = tbase + C::kTmemO + k * D, tp = tbase + k * 128;
@@ -432,7 +447,8 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
                 ptx::tc_commit_e(&ctl->v_empty[stp]);
                 if (jj == T - 1) {
                     ptx::tc_commit_e(&ctl->o_full);
-                    ++oc;
+                    ++oc0;
+                    if (nh == 2) ++oc1;
                 }
             }
             if (j < T) {
@@ -875,10 +891,11 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
     using C = Cfg<D, DEC>;
     const int quarter = warp & 3;
     const int ri = quarter * 32 + lane;  // tile row = TMEM lane
-    const bool valid = ri < g.nrows;
-    const int prow = valid ? p.pos[g.row0 + ri] : -1;
-    const int pmin = p.pos[g.row0];
-    const int head = g.head + k;
+    const int r0 = qtile_row0(p, g, k);  // first row of query tile k
+    const bool valid = ri < qtile_rows(p, g, k);
+    const int prow = valid ? p.pos[r0 + ri] : -1;
+    const int pmin = p.pos[g.row0];      // the group's smallest position (the MMA warp uses the same)
+    const int head = qtile_head(p, g, k);
     const uint32_t tlane = ctl->tmem_base + ((uint32_t)(quarter * 32) << 16);
     const uint32_t tS = tlane + k * 128;             // S_k, later P_k (cols 0..63) and its residual (64..127)
     const uint32_t tO = tlane + C::kTmemO + k * D;  // O_k
@@ -1043,7 +1060,7 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
     const float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
     const bool split = g.n_parts > 1;
     const int64_t slot0 = split ? ((int64_t)(g.slot + it.part) * 2 + k) * kTileRows : 0;
-    const int64_t obase = ((int64_t)(g.row0 + ri) * p.Hq + head) * D;
+    const int64_t obase = ((int64_t)(r0 + ri) * p.Hq + head) * D;
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
         float ov[32];
@@ -1076,7 +1093,7 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
     ptx::tc_fence_before();
     ptx::mbar_arrive(&ctl->o_empty[k]);
     if (!split) {
-        if (valid && p.lse) p.lse[(int64_t)(g.row0 + ri) * p.Hq + head] = lse2 * kLn2;
+        if (valid && p.lse) p.lse[(int64_t)(r0 + ri) * p.Hq + head] = lse2 * kLn2;
         return true;
     }
     // split group: this part is written; the last part to arrive merges
@@ -1120,7 +1137,7 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
 #pragma unroll
                 for (int i = 0; i < 32; ++i) store_out(p, obase + c * 32 + i, acc[i]);
             }
-            if (p.lse) p.lse[(int64_t)(g.row0 + ri) * p.Hq + head] = L > 0.f ? (mm + log2f(L)) * kLn2 : -INFINITY;
+            if (p.lse) p.lse[(int64_t)(r0 + ri) * p.Hq + head] = L > 0.f ? (mm + log2f(L)) * kLn2 : -INFINITY;
         }
         if (ri == 0) p.counters[2 * it.group + k] = 0;  // ready for the next launch
     }

@@ -27,10 +27,12 @@ struct Run {
 
 // An output group: the rows and heads one merge produces.
 //   decode : rows [row0, row0+nrows) x query heads [head*G, head*G+G), kv head = head
-//   prefill: rows [row0, row0+nrows) x query heads [head, head+pad) (pad =
-//            1 or 2 consecutive heads of one kv head)
+//   prefill: `pad` query tiles of 128 rows x one head, all of one kv head:
+//            G even: rows [row0, row0+nrows) (<= 128) x heads [head, head+pad);
+//            G odd:  head `head` x rows [row0, row0+nrows) (<= 128 * pad),
+//                    tile k = rows [row0 + 128k, ...)
 // n_parts > 1 means the key range was split; parts write partials to slots
-// [slot, slot + n_parts) (two head slots each for prefill) and the last to
+// [slot, slot + n_parts) (two tile slots each for prefill) and the last to
 // finish merges them.
 struct Group {
     int32_t kind;
@@ -40,7 +42,7 @@ struct Group {
     int32_t nrows;
     int32_t n_parts;
     int32_t slot;
-    int32_t pad;  // query heads per group (G for decode, 1 or 2 for prefill)
+    int32_t pad;  // decode: G query heads; prefill: query tiles (1 or 2)
 };
 
 // A work item: one group's keys [kb, ke), starting in run `first_run`

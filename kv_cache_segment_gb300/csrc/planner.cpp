@@ -273,13 +273,17 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
             const int32_t ke = std::min(pmax + 1, L);
             const int64_t tiles = count_tiles(0, ke);
             // decode: one group per kv head (all G query heads packed);
-            // prefill: one group per pair of query heads sharing a kv head
-            // (G even), else per query head; Group.pad = query heads per group
+            // prefill: two query tiles of 128 rows x one head that share a kv
+            // head -- a pair of query heads over <= 128 rows (G even), or one
+            // query head over two consecutive row tiles (G odd: no second
+            // head of the same kv head to pair with); Group.pad = G for
+            // decode, the number of query tiles (1 or 2) for prefill
             const int32_t hpg = kind == kDecode ? G : (G % 2 == 0 ? 2 : 1);
             const int32_t ngr = kind == kDecode ? Hkv : Hq / hpg;
+            const int32_t pad = kind == kDecode ? G : (G % 2 == 0 ? 2 : (nrows + kTileRows - 1) / kTileRows);
             for (int32_t h = 0; h < ngr; ++h) {
                 Pending pd;
-                pd.g = Group{kind, s, kind == kDecode ? h : h * hpg, row0, nrows, 1, -1, hpg};
+                pd.g = Group{kind, s, kind == kDecode ? h : h * hpg, row0, nrows, 1, -1, pad};
                 pd.ke = ke;
                 pd.tiles = tiles;
                 pend.push_back(pd);
@@ -297,12 +301,13 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
         if (n <= P->dec_rows) {
             add_groups(kDecode, r0, n);
         } else {
+            // 128-row tiles (the remainder too, unless the decode path takes
+            // it); for odd G two consecutive tiles form one group
             const int32_t full = n / kTileRows, rem = n % kTileRows;
-            for (int32_t t = 0; t < full; ++t) add_groups(kPrefill, r0 + t * kTileRows, kTileRows);
-            if (rem > 0) {
-                if (rem <= P->dec_rows) add_groups(kDecode, r0 + full * kTileRows, rem);
-                else add_groups(kPrefill, r0 + full * kTileRows, rem);
-            }
+            const int32_t pre_rows = full * kTileRows + (rem > P->dec_rows ? rem : 0);
+            const int32_t span = G % 2 == 0 ? kTileRows : 2 * kTileRows;
+            for (int32_t a = 0; a < pre_rows; a += span) add_groups(kPrefill, r0 + a, std::min(span, pre_rows - a));
+            if (rem > 0 && rem <= P->dec_rows) add_groups(kDecode, r0 + full * kTileRows, rem);
         }
     }
 

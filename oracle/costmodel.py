@@ -7,12 +7,14 @@ kernel's expected latency (MSA paper abstract; AsymCache explainer, "æ ¸å¿ƒæ–¹æ³
 queue:
 
   fixed phase (us)   dec_item                                 (decode)
-                   | pre_item + pre_tile * tiles * heads      (prefill)
+                   | pre_item + pre_tile * tiles * qtiles     (prefill)
                      + box * extra_boxes
                      + dec_merge | pre_merge   [group split into parts]
   stream phase (B)   decode only: tiles * 128 * D * 2 * 2 (K and V, bf16),
                      at min(dec_cta, dec / n_streaming) GB/s per CTA
   tiles        128-key windows [kb + 128 i, min(kb + 128 (i+1), ke))
+  qtiles       query tiles of 128 rows x one head: ceil(rows / 128) x heads
+               (two heads over <= 128 rows, or one head over <= 256 rows)
   extra_boxes  per tile, the TMA boxes beyond one: a full 128-key window
                inside one segment is one box, any other tile one box per
                16-key block of each segment piece it touches
@@ -82,9 +84,10 @@ def estimate(items, order, block_table, seq_lens, grid, params, head_dim):
             b = tile_bytes * tiles
             out["decode_tiles"] += tiles
         else:
-            f = params["pre_item_us"] + params["pre_tile_us"] * tiles * heads
+            qtiles = -(-nrows // TILE) * heads
+            f = params["pre_item_us"] + params["pre_tile_us"] * tiles * qtiles
             b = 0.0
-            out["prefill_tile_heads"] += tiles * heads
+            out["prefill_tile_heads"] += tiles * qtiles
         merge = params["dec_merge_us"] if kind == 0 else params["pre_merge_us"]
         f += params["box_us"] * extra + (merge if split else 0.0)
         out["extra_boxes"] += extra

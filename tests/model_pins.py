@@ -66,6 +66,18 @@ def pin_split_prefill_pays_its_merge(oc):
     assert r["n_split_items"] == 2 and r["stream_bytes"] == 0
 
 
+def pin_row_pair_prefill_counts_two_tiles(oc):
+    """An odd Hq/Hkv prefill item: one head over 200 rows is two query tiles
+    (128 + 72 rows) walking the same 3 key tiles: pre_item + pre_tile x 3 x 2;
+    one head over 100 rows is one tile: pre_item + pre_tile x 3."""
+    p = PARAMS
+    items = [_item(1, 0, 1, 0, 0, 384, nrows=200), _item(1, 1, 1, 0, 0, 384, nrows=100)]
+    tables = {0: list(range(24)), 1: list(range(100, 124))}
+    r = oc.estimate(items, [0, 1], tables, {0: 384, 1: 384}, 1, p, 128)
+    assert r["prefill_tile_heads"] == 3 * 2 + 3 * 1
+    assert _close(r["fixed_us"], 2 * p["pre_item_us"] + p["pre_tile_us"] * (6 + 3))
+
+
 def pin_queue_order(oc):
     """Two CTAs, four prefill items of 4, 1, 2 and 6 tiles (one head) in that
     order: CTA 1 frees first and takes the third item, CTA 0 the fourth."""
@@ -126,7 +138,8 @@ def pin_recompute_flops(oc):
         assert oc.hole_recompute_flops(128, 8, a, b, L) == 4.0 * 128 * 8 * s
 
 
-COST_PINS = [pin_one_cta_mixed_items, pin_split_prefill_pays_its_merge, pin_queue_order, pin_shared_bandwidth,
+COST_PINS = [pin_one_cta_mixed_items, pin_split_prefill_pays_its_merge, pin_row_pair_prefill_counts_two_tiles,
+             pin_queue_order, pin_shared_bandwidth,
              pin_equal_items_in_rounds, pin_tma_boxes, pin_recompute_flops]
 
 

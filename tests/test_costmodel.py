@@ -33,9 +33,15 @@ def _both(wl, params=PARAMS, num_sms=152):
 INT_KEYS = ("n_items", "n_split_items", "decode_tiles", "prefill_tile_heads", "extra_boxes", "stream_bytes")
 
 
+def _odd_g(hq, hkv):
+    return W.custom([700, 260, 90], [[4, 30, 10], [5, 12], [6]], [[(0, 300), (650, 701)], [(258, 261)], [(87, 91)]],
+                    hq=hq, hkv=hkv, seed=11)
+
+
 @pytest.mark.parametrize("wl_fn", [lambda: W.small_config(1), lambda: W.small_config(2), lambda: W.small_config(3),
-                                   lambda: W.small_config(5), lambda: W.config(2), lambda: W.config(5)],
-                         ids=["small1", "small2", "small3", "small5", "batched_decode", "mixed_batch"])
+                                   lambda: W.small_config(5), lambda: W.config(2), lambda: W.config(5),
+                                   lambda: _odd_g(6, 2), lambda: _odd_g(4, 4)],
+                         ids=["small1", "small2", "small3", "small5", "batched_decode", "mixed_batch", "G3", "G1"])
 def test_library_matches_oracle(wl_fn):
     lib, ref, _ = _both(wl_fn())
     for k in INT_KEYS:

@@ -29,7 +29,8 @@ def test_eviction_oracle_pin(pin):
 
 # (module, name, text in the module, replacement)
 MUTATIONS = [
-    ("costmodel", "prefill_heads_dropped", 'params["pre_tile_us"] * tiles * heads', 'params["pre_tile_us"] * tiles'),
+    ("costmodel", "prefill_qtiles_dropped", 'params["pre_tile_us"] * tiles * qtiles', 'params["pre_tile_us"] * tiles'),
+    ("costmodel", "qtiles_ignore_rows", "qtiles = -(-nrows // TILE) * heads", "qtiles = heads"),
     ("costmodel", "stream_k_only", "tile_bytes = 2.0 * TILE * head_dim * 2.0", "tile_bytes = TILE * head_dim * 2.0"),
     ("costmodel", "bandwidth_not_shared", 'params["dec_gbs"] / n_stream', 'params["dec_gbs"]'),
     ("costmodel", "merge_for_every_item", "(merge if split else 0.0)", "merge"),

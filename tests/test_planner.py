@@ -104,8 +104,10 @@ def _check_coverage(wl, plan, enumerate_keys=True):
             assert a[2] == b[1] and a[1] < a[2]
         if kind == 0:
             assert nrows * G <= 16
+        elif G % 2 == 0:
+            assert nh == 2 and nrows <= 128  # two heads of one kv head over one row tile
         else:
-            assert nrows <= 128
+            assert nh == 1 and nrows <= 256  # one head over one or two row tiles
     assert np.all(owner == 1)
     if enumerate_keys:
         # every visible key of every row is inside exactly one part's range
