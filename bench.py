@@ -801,7 +801,31 @@ def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
     out["gather_then_attention"] = gathers
     out["eviction_policies"] = eviction_leg(dev, stream, steps, warm)
     out["decode_shapes"] = decode_shapes_leg(dev, stream, peaks, steps, warm, rank)
+    out["prefill_shapes"] = prefill_shapes_leg(dev, stream, peaks, steps, warm, rank)
     return out
+
+
+# Hole recompute + new turn at other GQA ratios and head dims: (Hq, Hkv, D).
+PREFILL_SHAPES = ((8, 8, 128), (24, 8, 128), (32, 8, 64))
+
+
+def prefill_shapes_leg(dev, stream, peaks, steps, warm, rank):
+    """Prefill tensor rate for odd G (query tiles are row pairs of one head)
+    and D = 64."""
+    import torch
+    from kv_cache_segment_gb300 import workloads as W
+    res = []
+    for hq, hkv, d in PREFILL_SHAPES:
+        wl = W.hole_recompute(seed=1003 + 1000 * rank, hq=hq, hkv=hkv, d=d)
+        case = Case(wl, dev, plan_opts=_plan_opts())
+        _, ms = time_case(case, steps, warm, stream, with_append=False)
+        tf = case.flops() / (ms * 1e-3) / 1e12
+        res.append({"hq": hq, "hkv": hkv, "head_dim": d, "G": hq // hkv, "attention_ms": round(ms, 4),
+                    "prefill_tflops": round(tf, 1), "tensor_frac": round(tf / peaks["bf16_tflops"], 4),
+                    "items": int(case.info["num_items"])})
+        del case
+        torch.cuda.empty_cache()
+    return res
 
 
 # Batched decode (the headline's length and segment draws) at other GQA
