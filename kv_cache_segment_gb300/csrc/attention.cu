@@ -189,7 +189,11 @@ __device__ __forceinline__ bool compute_sync(const AttnParams& p, Ctl* ctl, int 
 __device__ __forceinline__ int publish_item(const AttnParams& p, Ctl* ctl, uint32_t& n) {
     const int slot = n & 3;
     if (!wait_bar(p, ctl, &ctl->item_empty[slot], ((n >> 2) & 1) ^ 1, kErrTimeoutProducer)) return -2;
-    const int q = atomicAdd(&p.sched[0], 1);
+    // A CTA's first item is position blockIdx.x of the order (no queue
+    // round trip before its first loads, and the longest items start on
+    // distinct CTAs at once); later ones come from the global counter, which
+    // hands out positions gridDim.x, gridDim.x + 1, ...
+    const int q = n == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&p.sched[0], 1);
     const int id = q < p.n_items ? p.order[q] : -1;
     ctl->ring[slot] = id;
     ptx::mbar_arrive(&ctl->item_full[slot]);
