@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmsa.so")
-SOURCES = ["capi.cpp", "planner.cpp", "costmodel.cpp", "attention.cu", "append.cu", "noalloc.cu"]
+SOURCES = ["capi.cpp", "planner.cpp", "costmodel.cpp", "tensor_maps.cpp", "attention.cu", "append.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else "nvcc")
 

@@ -1288,37 +1288,9 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
 
 // ------------------------------------------------------------ host side --
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// The driver's tensor-map encoder, looked up once (thread-safe static).
-static EncodeTiledFn encode_fn() {
-    static const EncodeTiledFn fn = [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            return reinterpret_cast<EncodeTiledFn>(ptr);
-        return EncodeTiledFn(nullptr);
-    }();
-    return fn;
-}
-
-// 3-D bf16 map over [rows, heads, D] (innermost D), box = 64 x 1 x box_rows,
-// 128-byte swizzle; rows past the end read as zero.
-static bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
+// 3-D bf16 tensor map over [rows, heads, D] with a box of 64 x 1 x box_rows
+// (tensor_maps.cpp: encoded once per thread and inputs).
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, int box_rows);
 
 // Launch attributes of one kernel instantiation on the current device (a
 // function attribute belongs to the device it was set on): done once per
