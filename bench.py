@@ -765,14 +765,18 @@ def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
         if key in ("hole_recompute", "batched_decode", "long_context"):
             gathers[key] = gather_leg(case, steps, warm, stream)
             torch.cuda.empty_cache()
-            _, seg_ms = time_case(case, steps, warm, stream, with_append=False)
-            del case
-            torch.cuda.empty_cache()
+            # the same sequences laid out as one contiguous run each, timed in
+            # alternation with the segmented layout (median of three rounds)
+            # so that both see the same state of the GPU
             cont = Case(wl, dev, contiguous=True, plan_opts=_plan_opts())
-            _, con_ms = time_case(cont, steps, warm, stream, with_append=False)
+            seg_t, con_t = [], []
+            for _ in range(3):
+                seg_t.append(time_case(case, steps, warm, stream, with_append=False)[1])
+                con_t.append(time_case(cont, steps, warm, stream, with_append=False)[1])
+            seg_ms, con_ms = float(np.median(seg_t)), float(np.median(con_t))
             over[key] = {"segmented_ms": round(seg_ms, 4), "contiguous_ms": round(con_ms, 4),
                          "ratio": round(seg_ms / con_ms, 4)}
-            del cont
+            del case, cont
         else:
             del case
         torch.cuda.empty_cache()

@@ -192,8 +192,9 @@ int msa_plan_get_order(msa_plan_t plan, int32_t* order, int32_t* n_items);
  * tiles = 128-key windows the item walks; qtiles = the prefill item's query
  * tiles of 128 rows x one head (1 or 2: two heads of one kv head, or for an
  * odd Hq/Hkv one head over two consecutive row tiles); extra_boxes = TMA boxes beyond one per tile (a tile that is
- * not a full 128-key window inside one segment is fetched one 16-key block
- * at a time).  Items are handed out in the plan's order to `grid` CTAs, a
+ * not a full 128-key window inside one segment is fetched per segment piece,
+ * a piece's whole 16-key blocks in boxes of 4, 2 and 1 blocks).  Items are
+ * handed out in the plan's order to `grid` CTAs, a
  * CTA taking the next one when it becomes free (several freed at once take
  * in CTA order), as the kernel's queue does.  The replay is event by event:
  * time_us = launch_us + the time the last CTA finishes.  Parameters fitted

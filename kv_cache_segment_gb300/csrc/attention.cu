@@ -248,7 +248,8 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c16) {
 // soon as the S MMAs of tile j have read K(j), long before PV(j) frees V(j).
 template <int D, bool DEC, bool KSIDE>
 __device__ void producer(const AttnParams& p, uint8_t* smem, Ctl* ctl, const CUtensorMap* tm128,
-                         const CUtensorMap* tm16, const CUtensorMap* tmQ) {
+                         const CUtensorMap* tm64, const CUtensorMap* tm32, const CUtensorMap* tm16,
+                         const CUtensorMap* tmQ) {
     using C = Cfg<D, DEC>;
     uint64_t* full = KSIDE ? ctl->k_full : ctl->v_full;
     uint64_t* empty = KSIDE ? ctl->k_empty : ctl->v_empty;
@@ -288,8 +289,9 @@ __device__ void producer(const AttnParams& p, uint8_t* smem, Ctl* ctl, const CUt
         {
             // KV tiles are 128-key windows of the item's logical key range.  A
             // window that lies inside one segment is one TMA rectangle; where it
-            // spans segments, each piece is fetched from its own segment, one
-            // 16-row box per block (segments are whole blocks, so every piece is).
+            // spans segments, each piece is fetched from its own segment in
+            // boxes of 64, 32 and 16 rows (segments are whole 16-row blocks, so
+            // every piece is).
             int r = it.first_run;
             int tiles = 0;
             for (int t0 = it.kb; t0 < it.ke; t0 += kTileKeys) {
@@ -325,11 +327,16 @@ __device__ void producer(const AttnParams& p, uint8_t* smem, Ctl* ctl, const CUt
                         for (int pn = 0; pn < C::kPanels; ++pn)
                             ptx::tma_load_3d(dst + pn * C::kPanelBytes, tm128, pn * 64, kvh, phys, &full[st]);
                     } else {
+                        // the piece's whole blocks, in boxes of 4, 2 or 1 blocks (64, 32, 16 rows)
                         const int nb = (pend - cur + kBlock - 1) / kBlock;
-                        for (int b = 0; b < nb; ++b)
+                        for (int b = 0; b < nb;) {
+                            const int w = nb - b >= 4 ? 4 : (nb - b >= 2 ? 2 : 1);
+                            const CUtensorMap* tm = w == 4 ? tm64 : (w == 2 ? tm32 : tm16);
                             for (int pn = 0; pn < C::kPanels; ++pn)
-                                ptx::tma_load_3d(dst + pn * C::kPanelBytes + (off + b * kBlock) * 128, tm16, pn * 64,
+                                ptx::tma_load_3d(dst + pn * C::kPanelBytes + (off + b * kBlock) * 128, tm, pn * 64,
                                                  kvh, phys + b * kBlock, &full[st]);
+                            b += w;
+                        }
                     }
                     cur = pend;
                 }
@@ -1186,7 +1193,9 @@ __device__ void compute(const AttnParams& p, uint8_t* smem, Ctl* ctl, int warp, 
 template <int D, bool DEC>
 __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
     msa_attention_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmK64, const __grid_constant__ CUtensorMap tmK32,
                          const __grid_constant__ CUtensorMap tmK16, const __grid_constant__ CUtensorMap tmV,
+                         const __grid_constant__ CUtensorMap tmV64, const __grid_constant__ CUtensorMap tmV32,
                          const __grid_constant__ CUtensorMap tmV16, const __grid_constant__ CUtensorMap tmQ) {
     using C = Cfg<D, DEC>;
     extern __shared__ uint8_t smem_raw[];
@@ -1226,8 +1235,12 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
     }
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmK);
+        ptx::prefetch_tmap(&tmK64);
+        ptx::prefetch_tmap(&tmK32);
         ptx::prefetch_tmap(&tmK16);
         ptx::prefetch_tmap(&tmV);
+        ptx::prefetch_tmap(&tmV64);
+        ptx::prefetch_tmap(&tmV32);
         ptx::prefetch_tmap(&tmV16);
         if (!DEC) ptx::prefetch_tmap(&tmQ);
     }
@@ -1242,9 +1255,9 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
     if (warp < C::kFirstCompute) {
         if constexpr (!DEC) ptx::setmaxnreg_dec<C::kRegsLow>();
         if (warp == 0) {
-            if (lane == 0) producer<D, DEC, true>(p, smem, ctl, &tmK, &tmK16, &tmQ);
+            if (lane == 0) producer<D, DEC, true>(p, smem, ctl, &tmK, &tmK64, &tmK32, &tmK16, &tmQ);
         } else if (warp == C::kVWarp) {
-            if (lane == 0) producer<D, DEC, false>(p, smem, ctl, &tmV, &tmV16, &tmQ);
+            if (lane == 0) producer<D, DEC, false>(p, smem, ctl, &tmV, &tmV64, &tmV32, &tmV16, &tmQ);
         } else if (warp == 1) {
             if constexpr (!DEC) {
                 if (p.has_prefill) {
@@ -1328,7 +1341,8 @@ static int launch_d(const msa_plan_s* P, const AttnParams& prm, const CUtensorMa
     const int rc = configure_current_device<D, DEC>();
     if (rc != MSA_OK) return rc;
     msa_attention_kernel<D, DEC>
-        <<<P->grid, C::kThreads, C::kSmem, st>>>(prm, maps[0], maps[1], maps[2], maps[3], maps[4]);
+        <<<P->grid, C::kThreads, C::kSmem, st>>>(prm, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5],
+                                                  maps[6], maps[7], maps[8]);
     return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
@@ -1341,13 +1355,16 @@ int launch_attention_ws(const msa_plan_s* P, void* workspace, const void* q, con
                         const void* v_pool, int64_t pool_tokens, void* out, int32_t out_dtype, float* lse,
                         msa_stream_t stream) {
     const int D = P->dims.head_dim, Hq = P->dims.num_q_heads, Hkv = P->dims.num_kv_heads;
-    CUtensorMap maps[5];
+    CUtensorMap maps[9];
     const int64_t nq = P->info.num_q_rows;
-    if (!make_map(&maps[0], k_pool, pool_tokens, Hkv, D, kTileKeys) ||
-        !make_map(&maps[1], k_pool, pool_tokens, Hkv, D, kBlock) ||
-        !make_map(&maps[2], v_pool, pool_tokens, Hkv, D, kTileKeys) ||
-        !make_map(&maps[3], v_pool, pool_tokens, Hkv, D, kBlock) ||
-        !make_map(&maps[4], q, nq, Hq, D, kTileRows))
+    // K and V with boxes of 128 (a whole tile), 64, 32 and 16 rows (pieces
+    // of tiles that span segments), then Q
+    const int box_rows[4] = {kTileKeys, 4 * kBlock, 2 * kBlock, kBlock};
+    for (int i = 0; i < 4; ++i)
+        if (!make_map(&maps[i], k_pool, pool_tokens, Hkv, D, box_rows[i]) ||
+            !make_map(&maps[4 + i], v_pool, pool_tokens, Hkv, D, box_rows[i]))
+            return MSA_ERR_CUDA;
+    if (!make_map(&maps[8], q, nq, Hq, D, kTileRows))
         return MSA_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const WsLayout& W = P->lay;

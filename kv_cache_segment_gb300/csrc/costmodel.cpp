@@ -23,7 +23,8 @@ using msa::kTileKeys;
 
 // TMA boxes the producer issues for the tile [t0, t1) of sequence `seq`
 // beyond one: a full 128-key window inside one segment is one rectangle; any
-// other tile is fetched per 16-key block of each segment piece.
+// other tile is fetched piece by piece (one piece per segment it touches),
+// each piece's whole 16-key blocks in boxes of 4, 2 and 1 blocks.
 int64_t tile_extra_boxes(const msa_plan_s* P, int32_t seq, int32_t t0, int32_t t1) {
     const int32_t ra = P->run_indptr[seq], rb = P->run_indptr[seq + 1];
     // first run that ends after t0 (runs are in logical order)
@@ -39,8 +40,12 @@ int64_t tile_extra_boxes(const msa_plan_s* P, int32_t seq, int32_t t0, int32_t t
         const msa::Run& R = P->runs[r];
         const int32_t pend = std::min(t1, R.log_start + R.n_tok);
         if (pend <= cur) continue;
-        if (cur == t0 && pend - cur == kTileKeys) boxes += 1;
-        else boxes += (pend - cur + kBlock - 1) / kBlock;
+        if (cur == t0 && pend - cur == kTileKeys) {
+            boxes += 1;
+        } else {
+            const int64_t nb = (pend - cur + kBlock - 1) / kBlock;
+            boxes += nb / 4 + (nb % 4) / 2 + nb % 2;
+        }
         cur = pend;
     }
     return boxes > 1 ? boxes - 1 : 0;

@@ -16,8 +16,9 @@ queue:
   qtiles       query tiles of 128 rows x one head: ceil(rows / 128) x heads
                (two heads over <= 128 rows, or one head over <= 256 rows)
   extra_boxes  per tile, the TMA boxes beyond one: a full 128-key window
-               inside one segment is one box, any other tile one box per
-               16-key block of each segment piece it touches
+               inside one segment is one box; any other tile is fetched per
+               segment piece, a piece of b whole 16-key blocks in boxes of 4,
+               2 and 1 blocks (b // 4 + (b % 4) // 2 + b % 2 boxes)
   replay       CTAs 0..grid-1 take the first items of the plan's order; when
                a CTA's phases are done it takes the next item; between
                events every CTA advances at its phase's rate
@@ -50,7 +51,8 @@ def _boxes(segs, t0, t1):
         if lo == t0 and hi - lo == TILE:
             boxes += 1
         else:
-            boxes += -(-(hi - lo) // BLOCK)
+            b = -(-(hi - lo) // BLOCK)
+            boxes += b // 4 + (b % 4) // 2 + b % 2
     return boxes
 
 

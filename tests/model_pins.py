@@ -120,14 +120,19 @@ def pin_equal_items_in_rounds(oc):
 def pin_tma_boxes(oc):
     """Every block its own segment (physical blocks 0, 2, 4, ...): a full
     128-key tile needs 8 boxes (7 extra); the 40-key last tile 3 (2 extra).
-    One segment: only the partial last tile takes one box per 16-key block."""
+    One segment: only the partial last tile (3 blocks) is cut, into a box of
+    2 blocks and one of 1 (1 extra).  Segments of 7 and 1 blocks: the first
+    tile is pieces of 7 blocks (4 + 2 + 1 blocks: 3 boxes) and 1 block."""
     L = 2 * 128 + 40
     nb = -(-L // 16)
     r = oc.estimate([_item(0, 0, 4, 0, 0, L)], [0], {0: [2 * b for b in range(nb)]}, {0: L}, 1, PARAMS, 128)
     assert r["extra_boxes"] == 2 * 7 + 2
     assert _close(r["fixed_us"], PARAMS["dec_item_us"] + PARAMS["box_us"] * 16)
     r1 = oc.estimate([_item(0, 0, 4, 0, 0, L)], [0], {0: list(range(nb))}, {0: L}, 1, PARAMS, 128)
-    assert r1["extra_boxes"] == 2
+    assert r1["extra_boxes"] == 1
+    table = list(range(7)) + [20]  # blocks 0-6 contiguous, block 7 elsewhere
+    r2 = oc.estimate([_item(0, 0, 4, 0, 0, 128)], [0], {0: table}, {0: 128}, 1, PARAMS, 128)
+    assert r2["extra_boxes"] == (3 + 1) - 1
 
 
 def pin_recompute_flops(oc):

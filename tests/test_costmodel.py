@@ -92,7 +92,8 @@ def test_equal_items_fill_ctas_in_rounds(n_seqs, ctas, dec_gbs):
 
 def test_single_block_segments_cost_seven_extra_boxes_per_full_tile():
     """Every block its own segment: a full tile touches 8 segments (8 boxes),
-    a partial last tile of n keys ceil(n/16) boxes."""
+    a partial last tile of n keys ceil(n/16) boxes; in one segment the
+    partial tile's 3 blocks take boxes of 2 and 1 blocks."""
     L = 2 * 128 + 40
     nb = -(-L // 16)
     wl = W.custom([L], [[1] * nb], [[(L, L + 1)]], hq=4, hkv=1)
@@ -101,7 +102,7 @@ def test_single_block_segments_cost_seven_extra_boxes_per_full_tile():
     assert lib["extra_boxes"] == want and ref["extra_boxes"] == want
     one = W.custom([L], [[nb]], [[(L, L + 1)]], hq=4, hkv=1)
     lib1, ref1, _ = _both(one, num_sms=1)
-    assert lib1["extra_boxes"] == ref1["extra_boxes"] == math.ceil(40 / 16) - 1  # only the partial tile
+    assert lib1["extra_boxes"] == ref1["extra_boxes"] == 2 - 1  # only the partial tile: 3 blocks = 2 + 1
 
 
 @pytest.mark.parametrize("a,b,L", [(0, 37, 400), (100, 228, 400), (380, 401, 400)])

@@ -36,7 +36,8 @@ MUTATIONS = [
     ("costmodel", "merge_for_every_item", "(merge if split else 0.0)", "merge"),
     ("costmodel", "merge_constants_swapped", 'params["dec_merge_us"] if kind == 0 else params["pre_merge_us"]',
      'params["pre_merge_us"] if kind == 0 else params["dec_merge_us"]'),
-    ("costmodel", "one_box_per_piece", "boxes += -(-(hi - lo) // BLOCK)", "boxes += 1"),
+    ("costmodel", "one_box_per_piece", "boxes += b // 4 + (b % 4) // 2 + b % 2", "boxes += 1"),
+    ("costmodel", "one_box_per_block", "boxes += b // 4 + (b % 4) // 2 + b % 2", "boxes += b"),
     ("costmodel", "queue_taken_last_first", "                    j = queue.pop(0)",
      "                    j = queue.pop()"),
     ("costmodel", "launch_left_out", 'out["time_us"] = params["launch_us"] + t', 'out["time_us"] = t'),
