@@ -10,7 +10,8 @@ this script gives that model its constants for this kernel and GPU.
 
 Training and validation workloads are synthetic, drawn with the same
 generators as the bench (decode batches of several sizes, lengths and
-segment counts; hole recompute; long-context chunks; mixed batches) at
+segment counts; hole recompute, also at odd GQA ratios; long-context
+chunks; mixed batches) at
 different seeds and sizes for the two sets, each planned with three
 different split factors (msa_plan_create_ex).  Each plan is timed as the median of
 `--reps` launches of msa_attention alone (CUDA events on the launching
@@ -53,6 +54,8 @@ def training_set():
         s.append((f"holes{i}", W.hole_recompute(seed=2020 + i, num_seqs=n, cached_blocks=cb, evict_blocks=ev)))
     for i, (length, runs, chunk) in enumerate([(16384, 1, 512), (65536, 64, 2048), (32768, 16, 1024)]):
         s.append((f"long{i}", W.long_context(seed=2030 + i, num_seqs=1, length=length, n_runs=runs, chunk=chunk)))
+    # odd Hq/Hkv: prefill items are two row tiles of one head
+    s.append(("holes_g1", W.hole_recompute(seed=2026, num_seqs=8, cached_blocks=256, evict_blocks=64, hq=8, hkv=8)))
     # launches the size of the bench's prefill workloads
     s.append(("holes_big", W.hole_recompute(seed=2025, num_seqs=16, cached_blocks=512, evict_blocks=128)))
     s.append(("long_big", W.long_context(seed=2035, num_seqs=2, length=98304, n_runs=48, chunk=2048)))
@@ -67,6 +70,7 @@ def validation_set():
         s.append(_decode(3000 + i, n, lr, seg, f"v_decode{i}"))
     for i, (n, cb, ev) in enumerate([(4, 384, 96), (12, 512, 64)]):
         s.append((f"v_holes{i}", W.hole_recompute(seed=3010 + i, num_seqs=n, cached_blocks=cb, evict_blocks=ev)))
+    s.append(("v_holes_g3", W.hole_recompute(seed=3012, num_seqs=6, cached_blocks=384, evict_blocks=96, hq=24, hkv=8)))
     s.append(("v_long", W.long_context(seed=3020, num_seqs=2, length=49152, n_runs=32, chunk=1536)))
     for i, (nd, npf, chunk) in enumerate([(32, 2, 1024), (96, 3, 2048)]):
         s.append((f"v_mixed{i}", W.mixed_batch(seed=3030 + i, num_decode=nd, num_prefill=npf, chunk=chunk)))

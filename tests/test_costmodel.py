@@ -134,8 +134,8 @@ def test_estimate_rejects_null():
 
 # ------------------------------------------------- adaptive chunking (create_ex)
 
-FITTED = dict(launch_us=18.6, dec_item_us=4.55, dec_gbs=8121.0, dec_cta_gbs=52.8, pre_item_us=6.08, pre_tile_us=0.878,
-              box_us=0.0, dec_merge_us=0.79, pre_merge_us=48.7)
+FITTED = dict(launch_us=31.0, dec_item_us=2.83, dec_gbs=7708.0, dec_cta_gbs=60.0, pre_item_us=4.58, pre_tile_us=0.884,
+              box_us=0.0062, dec_merge_us=1.49, pre_merge_us=46.2)
 DEC_CANDIDATES = (1.0, 1.5, 2.0, 3.0, 4.0)
 PRE_CANDIDATES = (1.0, 2.0, 4.0)
 
