@@ -2,11 +2,13 @@
 //
 // One launch serves every work item of a plan: decode groups (a sequence's
 // few trailing query rows, all G query heads of one kv head packed as the
-// rows of a warp-level MMA) and prefill / hole-recompute tiles (128 query
-// rows of one or two query heads that share a kv head, on the tcgen05 tensor
-// cores with TMEM accumulators).  KV tiles are 128-key windows of an item's
-// logical key range; the producer fetches each window from the physically
-// contiguous segments it overlaps, one TMA rectangle per piece (AsymCache
+// rows of a warp-level MMA) and prefill / hole-recompute items (two query
+// tiles of 128 rows x one head that share a kv head -- two heads over the
+// same rows, or for an odd Hq/Hkv one head over two consecutive row tiles --
+// on the tcgen05 tensor cores with TMEM accumulators).  KV tiles are 128-key
+// windows of an item's logical key range; the producer fetches each window
+// from the physically contiguous segments it overlaps, in TMA boxes of 128,
+// 64, 32 or 16 rows per piece (AsymCache
 // explainer, "核心方法 1. Multi-Segment Attention": attention over the
 // physically contiguous segments of the live KV; MSA summary: one kernel over
 // many disjoint segments instead of a launch per segment).  Inside an item
@@ -16,8 +18,9 @@
 // last one to finish merges them by log-sum-exp.
 //
 // CTA roles, launch with prefill items (12 warps):
-//   warp 0      K producer: takes items from the work queue, loads the Q
-//               tiles of prefill items and the K tiles (TMA) into a ring of
+//   warp 0      K producer: takes the CTA's items (the first by position,
+//               the rest from the global work queue), loads the Q tiles of
+//               prefill items and the K tiles (TMA) into a ring of
 //               shared-memory stages, records each tile's key range.
 //   warp 1      owns TMEM; runs the MMA issue loop converged, one elected
 //               lane issuing tcgen05.mma.  Per KV tile j, in this order:
