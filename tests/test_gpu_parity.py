@@ -221,6 +221,32 @@ def test_odd_gqa_ratios(hq, hkv, d, opts):
     compare(out, lse, ro, rl, f"G={hq // hkv} d={d}")
 
 
+@pytest.mark.parametrize("name", ["holes", "mixed", "long", "holes_g3"])
+@pytest.mark.parametrize("opts", [dict(), dict(decode_split=12.0, prefill_split=16.0)])
+def test_d64_prefill_workloads(name, opts):
+    """Head dim 64 (P in its own TMEM columns, S refilled while the softmax
+    works) on small hole-recompute, mixed and long-context shapes, with and
+    without split groups; rows near a sequence start take the residual pass
+    in S's columns."""
+    if name == "holes":
+        wl = W.hole_recompute(seed=41, num_seqs=2, cached_blocks=64, evict_blocks=16, hole_range=(2, 6),
+                              turn_tokens=72, hq=8, hkv=2, d=64)
+    elif name == "holes_g3":
+        wl = W.hole_recompute(seed=42, num_seqs=2, cached_blocks=48, evict_blocks=12, hole_range=(2, 5),
+                              turn_tokens=100, hq=6, hkv=2, d=64)
+    elif name == "mixed":
+        wl = W.mixed_batch(seed=43, num_decode=6, num_prefill=2, chunk=200, median=600, cap=3000, max_seg=8,
+                           hq=16, hkv=2, d=64)
+    else:
+        wl = W.long_context(seed=44, num_seqs=1, length=4096 + 40, n_runs=12, p=1.0 / 16, chunk=300,
+                            hq=8, hkv=2, d=64)
+    k, v, q = W.make_values(wl)
+    out, lse, info = run_gpu(wl, k, v, q, **opts)
+    assert info["num_prefill_items"] > 0
+    ro, rl = oracle_ref(wl, k, v, q)
+    compare(out, lse, ro, rl, f"D=64 {name} {opts}")
+
+
 @pytest.mark.parametrize("shape", ["rising", "falling", "spikes"])
 def test_running_max_moves(shape):
     """Scores far from N(0,1): keys whose scores rise along the sequence (the
