@@ -402,6 +402,27 @@ def test_full_size_configs_sampled(idx, plan):
     compare(out[torch.as_tensor(rows, device=dev)], lse[torch.as_tensor(rows, device=dev)], ro, rl, wl.name)
 
 
+def test_million_token_sequence_sampled():
+    """One sequence of 2^20 + 37 cached tokens in 40 segments (pools of 4 GiB
+    each), queried by a 100-row recompute range at its end and a decode row:
+    positions near 2^20, key ranges split over many CTAs and merged; checked
+    on sampled rows."""
+    L = (1 << 20) + 37
+    nb = -(-L // 16)
+    rng = np.random.default_rng(20)
+    cuts = np.sort(rng.choice(np.arange(1, nb), size=39, replace=False))
+    sizes = np.diff(np.concatenate([[0], cuts, [nb]])).tolist()
+    wl = W.custom([L], [sizes], [[(L - 100, L + 1)]], hq=32, hkv=8, seed=21)
+    dev = torch.device("cuda")
+    k, v, q = W.make_values(wl, device=dev)
+    out, lse, info = run_gpu(wl, k, v, q)
+    assert info["num_items"] > info["num_groups"]  # split groups, merged by the last part
+    rows = np.array([0, 1, 50, 98, 99, 100], np.int64)
+    ro, rl = oracle_ref(wl, k.cpu(), v.cpu(), q.cpu(), rows=rows)
+    sel = torch.as_tensor(rows, device=dev)
+    compare(out[sel], lse[sel], ro, rl, "2^20-token sequence")
+
+
 def test_misaligned_pointers_are_rejected_before_launch():
     """q and out must be 16-byte aligned (TMA, vector stores): a misaligned
     pointer comes back as MSA_ERR_INVALID_ARG and nothing is written."""
