@@ -1,0 +1,55 @@
+/* A plain C11 caller of libmsa (no C++, no torch): host-only calls of the
+ * ABI in include/msa.h.  Prints one line of results for the Python test to
+ * check; exits non-zero on any unexpected status. */
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "msa.h"
+
+#define CHECK(x)                                                            \
+    do {                                                                    \
+        int rc_ = (x);                                                      \
+        if (rc_ != MSA_OK) {                                                \
+            fprintf(stderr, "%s -> %s\n", #x, msa_status_string(rc_));      \
+            return 1;                                                       \
+        }                                                                   \
+    } while (0)
+
+int main(void) {
+    /* two sequences: 40 tokens in segments of blocks {0,1} and {7}; 20
+     * tokens in block {3}; queries: rows [30, 41) of seq 0, a decode row of seq 1 */
+    const msa_dims dims = {8, 2, 128, 16, 0.08838834764831845f};
+    const int32_t table[2][3] = {{10, 11, 17}, {3, 4, -1}};
+    const int32_t lens[2] = {40, 20};
+    const int32_t indptr[3] = {0, 1, 2};
+    const int32_t ranges[2][2] = {{30, 41}, {20, 21}};
+    msa_plan_t plan = NULL;
+    CHECK(msa_plan_create(&dims, 2, 3, &table[0][0], lens, indptr, &ranges[0][0], 4, &plan));
+    msa_plan_info info;
+    memset(&info, 0, sizeof info);
+    CHECK(msa_plan_get_info(plan, &info));
+    int32_t runs[3 * 8], n_runs = 0;
+    CHECK(msa_plan_get_runs(plan, 0, runs, &n_runs));
+    int32_t n_items = 0;
+    CHECK(msa_plan_get_items(plan, NULL, &n_items));
+    size_t ws = 0;
+    CHECK(msa_plan_workspace_bytes(plan, &ws));
+    const msa_cost_params prm = {10.0, 2.0, 6000.0, 50.0, 5.0, 1.0, 0.0, 1.0, 40.0};
+    msa_cost_estimate est;
+    CHECK(msa_plan_estimate(plan, &prm, &est));
+    const float hit[3] = {0.9f, 0.1f, 0.5f};
+    int32_t evicted[1] = {-1};
+    double cost[3];
+    CHECK(msa_select_evictions(&dims, 40, hit, MSA_EVICT_LINEAR, 1.0, 0.0, &prm, 1, evicted, cost));
+    /* an attention call before any upload is refused before any device work */
+    const int not_up = msa_attention((const void*)0x1000, (const void*)0x1000, (const void*)0x1000, 64, plan,
+                                     (void*)0x1000, MSA_OUT_BF16, NULL, NULL);
+    CHECK(msa_plan_destroy(plan));
+    printf("rows %d runs %d run0 %d %d %d run1 %d %d %d items %d ws_ok %d est_items %lld evict %d cost_rising %d "
+           "not_uploaded %s cost %.17g %.17g %.17g\n",
+           info.num_q_rows, n_runs, runs[0], runs[1], runs[2], runs[3], runs[4], runs[5], n_items, ws > 0,
+           (long long)est.n_items, evicted[0], cost[1] > cost[0], msa_status_string(not_up), cost[0], cost[1],
+           cost[2]);
+    return 0;
+}
