@@ -348,6 +348,41 @@ def test_cuda_graph_replay_equals_eager(idx):
         sess.close()
 
 
+def test_two_sessions_on_two_streams_at_once():
+    """Plans with their own workspaces launched on two streams without
+    ordering between them (a decode batch and a hole-recompute batch, split
+    groups in both): each result equals the same plan run alone, bit for bit.
+    The kernel keeps no state outside its plan's workspace."""
+    dev = torch.device("cuda")
+    runs = []
+    for idx in (2, 3):
+        wl = W.small_config(idx)
+        k, v, q = W.make_values(wl)
+        kp, vp = W.make_pool(wl, k.to(dev), v.to(dev))
+        sess = MsaSession.from_workload(wl, num_sms=1000)
+        runs.append((wl, sess, q.to(dev), kp, vp, k, v, q))
+    try:
+        alone = []
+        for wl, sess, qd, kp, vp, *_ in runs:
+            alone.append(sess.attention(qd, kp, vp).clone())
+        torch.cuda.synchronize()
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        outs = [[], []]
+        for _ in range(4):
+            for i, (wl, sess, qd, kp, vp, *_rest) in enumerate(runs):
+                sess.stream = streams[i]
+                with torch.cuda.stream(streams[i]):
+                    outs[i].append(sess.attention(qd, kp, vp))
+        torch.cuda.synchronize()
+        for i, (wl, sess, qd, kp, vp, k, v, q) in enumerate(runs):
+            assert sess.check_device()[0] == 0
+            for o in outs[i]:
+                assert torch.equal(o.view(torch.int16), alone[i].view(torch.int16))
+    finally:
+        for r in runs:
+            r[1].close()
+
+
 def test_repeat_calls_are_identical():
     """Merge counters reset themselves: back-to-back calls give the same bits."""
     wl = W.small_config(2)
