@@ -97,7 +97,7 @@ def load(path: str = LIB_PATH):
         return _lib
     if not os.path.exists(path):
         raise ImportError(f"{path} not found: build it with `python -m kv_cache_segment_gb300.build` "
-                          "(or __graft_entry__.build()); there is no fallback implementation")
+                          "; there is no fallback implementation")
     lib = ctypes.CDLL(path)
     vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     sigs = {
