@@ -96,8 +96,8 @@ def load(path: str = LIB_PATH):
     if _lib is not None:
         return _lib
     if not os.path.exists(path):
-        raise ImportError(f"{path} not found: build it with `python -m kv_cache_segment_gb300.build` "
-                          "; there is no fallback implementation")
+        raise ImportError(f"{path} not found: build it with `python -m kv_cache_segment_gb300.build`; "
+                          "there is no fallback implementation")
     lib = ctypes.CDLL(path)
     vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     sigs = {
