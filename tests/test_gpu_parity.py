@@ -155,6 +155,37 @@ def test_fp32_output():
     compare(out, lse, ro, rl, "fp32 out")
 
 
+@pytest.mark.parametrize("idx", [3, 5])
+def test_fp32_output_through_split_merges(idx):
+    """fp32 out with split groups (many CTAs): the last-arriver merges write
+    fp32 rows, within tolerance of the oracle."""
+    wl = W.small_config(idx)
+    k, v, q = W.make_values(wl)
+    out, lse, info = run_gpu(wl, k, v, q, out_fp32=True, num_sms=1000)
+    assert out.dtype == torch.float32 and info["num_items"] > info["num_groups"]
+    ro, rl = oracle_ref(wl, k, v, q)
+    compare(out, lse, ro, rl, "fp32 out, split")
+
+
+def test_lse_null_gives_the_same_out():
+    """lse is optional (NULL): out is bit-identical to a call that asks for it."""
+    wl = W.small_config(5)
+    k, v, q = W.make_values(wl)
+    dev = torch.device("cuda")
+    kp, vp = W.make_pool(wl, k.to(dev), v.to(dev))
+    sess = MsaSession.from_workload(wl, num_sms=400)
+    try:
+        qd = q.to(dev)
+        lse = torch.empty((wl.num_q_rows, wl.num_q_heads), dtype=torch.float32, device=dev)
+        a = sess.attention(qd, kp, vp, lse=lse).clone()
+        b = sess.attention(qd, kp, vp)
+        torch.cuda.synchronize()
+        assert sess.check_device()[0] == 0
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    finally:
+        sess.close()
+
+
 def test_segmented_equals_contiguous_layout():
     """Losslessness: the same logical K/V laid out as one segment or as many
     gives the same result (both within tolerance of the oracle and of each
