@@ -217,3 +217,30 @@ def test_bad_cost_params_are_rejected():
             msa.msa_plan_estimate(plan, dict(FITTED, pre_tile_us=float("nan")))
     finally:
         msa.msa_plan_destroy(plan)
+
+
+def test_fit_recovers_known_constants():
+    """costfit.fit on launch times generated by the model itself from known
+    constants (several workloads x split plans) finds constants that predict
+    those times to 1e-3; the ones the plans constrain well come back to 2 %."""
+    from kv_cache_segment_gb300 import costfit
+    truth = dict(launch_us=20.0, dec_item_us=3.0, dec_gbs=7000.0, dec_cta_gbs=55.0, pre_item_us=5.0,
+                 pre_tile_us=0.9, box_us=0.01, dec_merge_us=1.5, pre_merge_us=40.0)
+    plans = []
+    for wl in (W.small_config(2), W.small_config(3), W.small_config(5), W.config(2),
+               W.batched_decode(seed=9, num_seqs=64, len_range=(512, 4096), pool_tokens=1 << 20)):
+        dims = msa.make_dims(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, 16, wl.scale)
+        for ds, ps in ((1.0, 1.0), (3.0, 4.0), (8.0, 8.0)):
+            for sms in (152, 40):
+                plans.append(msa.msa_plan_create_ex(dims, wl.block_table, wl.seq_lens, wl.q_range_indptr,
+                                                    wl.q_ranges_flat, sms, ds, ps))
+    try:
+        records = [(p, msa.msa_plan_estimate(p, truth)["time_us"]) for p in plans]
+        got = costfit.fit(records)
+        err = costfit.errors(records, got)
+        assert err["max_abs_rel_err"] < 1e-3, err
+        for k in ("launch_us", "pre_tile_us", "dec_gbs"):
+            assert got[k] == pytest.approx(truth[k], rel=0.02), (k, got[k])
+    finally:
+        for p in plans:
+            msa.msa_plan_destroy(p)
