@@ -631,10 +631,17 @@ def eviction_workloads(seed=1100, num_seqs=16, blocks=512, evict=128, hq=32, hkv
     """Synthetic hit probabilities and the eviction choices of three weightings
     of the kernel-aware score (msa_select_evictions): hit probability only,
     recompute cost only, both; and the expected-cost mode, the set with the
-    least expected recompute time (lowest hit probability x cost).  Per policy the recompute workload that
-    follows when every evicted block is needed again: live segments where
-    they were, each evicted hole recomputed into fresh blocks, queries = the
-    evicted positions and the decode row.
+    least expected recompute time (lowest hit probability x cost).  Those use
+    the hole reading of the recompute cost (only the evicted block is
+    rebuilt); two more policies, cost only and hit and cost, use the prefix
+    reading (a block is usable only with its whole prefix, so evicting b
+    leaves b .. end to rebuild).  Per policy the recompute workload that
+    follows when every evicted block is needed again: hole reading: live
+    segments where they were, each evicted hole recomputed into fresh
+    blocks, queries = the evicted positions and the decode row; prefix
+    reading: the live prefix before the first evicted block, everything from
+    there to the end recomputed into one fresh run, queries = those positions
+    and the decode row.
 
     Hit probabilities per block (seeded): attention-sink blocks at the start
     (0.9), a recency ramp over the last blocks (0.85 e^-(age/32)), and a
@@ -652,24 +659,36 @@ def eviction_workloads(seed=1100, num_seqs=16, blocks=512, evict=128, hq=32, hkv
         p = 0.9 * (b < 4) + 0.85 * np.exp(-(blocks - 1 - b) / 32.0) + rng.beta(0.5, 4.0, blocks)
         hits.append(np.clip(p, 0.0, 1.0).astype(np.float32))
     out = {}
-    policies = (("hit_only", (1.0, 0.0)), ("cost_only", (0.0, 1.0)), ("hit_and_cost", (1.0, 1.0)),
-                ("expected_cost_optimum", None))
-    for name, weights in policies:
+    policies = (("hit_only", (1.0, 0.0), False), ("cost_only", (0.0, 1.0), False),
+                ("hit_and_cost", (1.0, 1.0), False), ("expected_cost_optimum", None, False),
+                ("prefix_cost_only", (0.0, 1.0), True), ("prefix_hit_and_cost", (1.0, 1.0), True))
+    for name, weights, prefix in policies:
         alpha, beta = weights if weights else (None, None)
         runs, ranges = [], []
-        exp_hits = exp_flops = exp_us = 0.0
+        exp_hits = exp_flops = exp_us = all_flops = 0.0
+        first = []
         for s in range(num_seqs):
+            pre = msa.MSA_EVICT_PREFIX_COST if prefix else 0
             if weights:
-                ev, cost = msa.msa_select_evictions(dims, L, hits[s], alpha, beta, params, evict)
+                ev, cost = msa.msa_select_evictions(dims, L, hits[s], alpha, beta, params, evict, mode=pre)
             else:  # the set with the least expected recompute time
                 ev, cost = msa.msa_select_evictions(dims, L, hits[s], 0.0, 0.0, params, evict,
-                                                    mode=msa.MSA_EVICT_EXPECTED_COST)
+                                                    mode=msa.MSA_EVICT_EXPECTED_COST | pre)
+            exp_hits += float(hits[s][ev].sum())
+            if prefix:
+                # every block from the first evicted one on is rebuilt
+                b0 = int(ev.min())
+                first.append(b0)
+                all_flops += 4.0 * d * hq * sum(range(16 * b0 + 1, L + 1))
+                runs.append([b0, blocks - b0] if b0 > 0 else [blocks])
+                ranges.append([(16 * b0, L), (L, L + 1)])
+                continue
             gone = np.zeros(blocks, bool)
             gone[ev] = True
-            exp_hits += float(hits[s][ev].sum())
             exp_us += float((hits[s][ev] * cost[ev]).sum())
             keys = np.array([sum(range(16 * b + 1, 16 * b + 17)) for b in ev], np.float64)
             exp_flops += float((hits[s][ev] * 4.0 * d * hq * keys).sum())
+            all_flops += float((4.0 * d * hq * keys).sum())
             sizes, rr = [], []
             b = 0
             while b < blocks:  # alternate live segments and holes, in logical order
@@ -684,10 +703,15 @@ def eviction_workloads(seed=1100, num_seqs=16, blocks=512, evict=128, hq=32, hkv
             runs.append(sizes)
             ranges.append(rr)
         wl = W.custom([L] * num_seqs, runs, ranges, hq=hq, hkv=hkv, d=d, seed=seed, name=f"eviction/{name}")
-        out[name] = {"wl": wl, "alpha": alpha, "beta": beta, "expected_hit_blocks": round(exp_hits, 2),
-                     "expected_recompute_gflop": round(exp_flops / 1e9, 3),
-                     "model_expected_recompute_us": round(exp_us, 1),
-                     "segments_after_recompute": int(sum(len(r) for r in runs))}
+        ent = {"wl": wl, "alpha": alpha, "beta": beta, "cost_reading": "prefix" if prefix else "hole",
+               "expected_hit_blocks": round(exp_hits, 2), "all_hit_recompute_gflop": round(all_flops / 1e9, 3),
+               "segments_after_recompute": int(sum(len(r) for r in runs))}
+        if prefix:
+            ent["first_evicted_block_mean"] = round(float(np.mean(first)), 1)
+        else:
+            ent["expected_recompute_gflop"] = round(exp_flops / 1e9, 3)
+            ent["model_expected_recompute_us"] = round(exp_us, 1)
+        out[name] = ent
     return out
 
 

@@ -101,6 +101,9 @@ typedef struct {
     double host_plan_us;         /* time msa_plan_create spent                   */
     double decode_split;         /* split factors the work items were cut with   */
     double prefill_split;        /* (see msa_plan_options)                       */
+    int64_t counters_offset;     /* byte range in the workspace of the merge     */
+    int64_t counters_bytes;      /* counters and the work-queue head: zero       */
+                                 /* before and after every clean launch          */
 } msa_plan_info;
 
 /*
@@ -237,32 +240,49 @@ int msa_plan_estimate(msa_plan_t plan, const msa_cost_params* params, msa_cost_e
  * cost, with weights alpha and beta set from the batch and the hardware).
  * For the sequence's n_blocks = ceil(seq_len / 16) cached blocks:
  *
- *   cost_us(b) = pre_tile_us * Hq * (sum over b's positions p of
+ *   hole(b)    = pre_tile_us * Hq * (sum over b's positions p of
  *                min(p + 1, seq_len)) / (128 * 128)
- *     the attention work of recomputing block b's rows (4*D*Hq*sum min(p+1,
- *     L) flops: each row attends to every earlier key) in units of one
- *     128x128 tile of one head, at the latency model's prefill rate;
- *   score(b)   = alpha * hit_prob[b] + beta * cost_us(b) / max_b cost_us(b)
+ *     the attention work of recomputing block b's own rows (4*D*Hq*sum
+ *     min(p+1, L) flops: each row attends to every earlier key) in units of
+ *     one 128x128 tile of one head, at the latency model's prefill rate.
  *
- * With mode MSA_EVICT_EXPECTED_COST the score is instead
+ * The page holds two views of that cost, and the mode picks one:
+ *   - hole reading (default): cost_us(b) = hole(b).  Only the evicted block
+ *     is rebuilt, so cost grows with position: mid- and late-sequence blocks
+ *     are dear to recompute, early ones cheap (the page: recompute cost
+ *     depends strongly on where the block sits).
+ *   - prefix reading (mode | MSA_EVICT_PREFIX_COST): cost_us(b) = sum over
+ *     b' >= b of hole(b'): a block's cache is only usable with its whole
+ *     prefix, so evicting b leaves every block from b to the end to be
+ *     recomputed.  Cost then falls with position and the tail blocks are the
+ *     cheapest to give up (the page: tail blocks are cheap and should yield
+ *     first).
+ * The score is
+ *   score(b)   = alpha * hit_prob[b] + beta * cost_us(b) / max_b cost_us(b)
+ * or, with mode | MSA_EVICT_EXPECTED_COST,
  *   score(b)   = hit_prob[b] * cost_us(b)
- * the block's expected recompute time (alpha and beta unused): for a fixed
- * number of evictions, the lowest such scores give the least expected
- * recompute time, which the pages' linear score only approximates.
+ * the block's expected recompute time (alpha and beta unused): in the hole
+ * reading, for a fixed number of evictions, the lowest such scores give the
+ * least expected recompute time, which the pages' linear score only
+ * approximates; in the prefix reading it is a per-block ranking.
  * The n_evict blocks of lowest score are written to evicted[0 .. n_evict)
  * in ascending block order; of equal scores the lower block index goes
- * first.  Later blocks cost more to recompute (the pages also call tail
- * blocks cheap; the attention arithmetic says the opposite, and this follows
- * the arithmetic).
+ * first.
+ *   mode       MSA_EVICT_LINEAR or MSA_EVICT_EXPECTED_COST, optionally ORed
+ *              with MSA_EVICT_PREFIX_COST
  *   hit_prob   host float [n_blocks], each in [0, 1]
  *   params     latency-model constants (pre_tile_us is used)
  *   evicted    host int32 [n_evict]
  *   cost_us    host double [n_blocks] or NULL: receives cost_us(b)
- * Returns MSA_ERR_INVALID_ARG for an unknown mode, n_evict outside [0,
+ * Returns MSA_ERR_INVALID_ARG for an unknown mode bit, n_evict outside [0,
  * n_blocks], a probability outside [0, 1], or negative or non-finite
  * weights.
  */
-typedef enum { MSA_EVICT_LINEAR = 0, MSA_EVICT_EXPECTED_COST = 1 } msa_evict_mode;
+typedef enum {
+    MSA_EVICT_LINEAR = 0,
+    MSA_EVICT_EXPECTED_COST = 1,
+    MSA_EVICT_PREFIX_COST = 2
+} msa_evict_mode;
 
 int msa_select_evictions(const msa_dims* dims, int32_t seq_len, const float* hit_prob, int32_t mode, double alpha,
                          double beta, const msa_cost_params* params, int32_t n_evict, int32_t* evicted,
@@ -292,6 +312,75 @@ typedef struct {
 int msa_plan_create_ex(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks_per_seq,
                        const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_range_indptr,
                        const int32_t* q_ranges, const msa_plan_options* opts, msa_plan_t* out);
+
+/*
+ * Adaptive prefill chunk size (AsymCache explainer, "核心方法 3": the
+ * scheduler cuts pending prefill work into chunks and sizes them from how
+ * busy the kernel keeps the GPU: chunks too small and launch and per-chunk
+ * overheads dominate, too large and a step (and every decode request riding
+ * on it) takes too long; MSA paper, methodology: a dynamic chunking
+ * scheduler adapts prefill sizes to maximise hardware utilisation).
+ *
+ * A serving step runs the batch's other query rows (for example one decode
+ * row per running sequence) together with the next c positions of every
+ * pending prefill.  For each candidate c the step's plan is built with
+ * msa_plan_create_ex(opts) and msa_plan_estimate(params) predicts its
+ * launch time T(c); the call returns the c with the lowest predicted time
+ * per prefill token, T(c) / tokens(c), among the candidates with
+ * T(c) <= budget_us (budget_us <= 0: no budget).  Equal costs go to the
+ * larger c; with no candidate inside the budget the smallest candidate is
+ * returned and choice->within_budget is 0.
+ *
+ *   dims .. q_ranges   the step's batch as for msa_plan_create: block tables
+ *                      and lengths of every sequence, and the query ranges of
+ *                      the rows that run besides the prefill chunks.  A
+ *                      pending sequence has no ranges there; its seq_lens
+ *                      entry is ignored, and its block table must already
+ *                      map every position below its `end`.
+ *   pending[n_pending] the pending prefills: rows [start, end) of sequence
+ *                      seq still to run (their K/V is appended before the
+ *                      step's attention, so a chunk of c rows runs with
+ *                      seq_len = start + c and rows [start, start + c)); at
+ *                      most one entry per sequence
+ *   opts               plan options of the step (num_sms, split factors, or
+ *                      NULL for the defaults)
+ *   params             latency-model constants
+ *   granularity        candidate spacing in tokens (0 = 128, one query tile)
+ *   max_chunk          largest chunk to consider (0 = no cap)
+ *   choice             receives the chosen chunk and its prediction
+ *   cand_chunk, cand_time_us   NULL, or arrays of at least 64 entries that
+ *                      receive every candidate (ascending) and its T(c)
+ * Candidates: the multiples of the granularity up to C = min(max_chunk,
+ * largest end - start), thinned to every k-th multiple, k = ceil(multiples /
+ * 63), when there are more than 63, then C itself if it is not the last
+ * one; a chunk larger than a sequence's remainder runs the remainder.
+ * Host only; each candidate costs one msa_plan_create_ex and one
+ * msa_plan_estimate.  Errors: MSA_ERR_INVALID_ARG (a null pointer, a
+ * sequence index out of range or listed twice, a pending sequence with rows
+ * of its own, bad params), MSA_ERR_BAD_Q_RANGE (start < 0 or end <= start),
+ * and whatever msa_plan_create_ex returns for a candidate's batch.
+ */
+typedef struct {
+    int32_t seq;    /* sequence with a pending prefill                    */
+    int32_t start;  /* first position still to run                        */
+    int32_t end;    /* end of the pending positions (exclusive), > start  */
+} msa_pending_prefill;
+
+typedef struct {
+    int32_t chunk;          /* chosen chunk size (positions per pending prefill) */
+    int32_t tokens;         /* prefill rows the step runs with it                */
+    double time_us;         /* predicted launch time of the step                  */
+    double us_per_token;    /* time_us / tokens                                   */
+    int32_t within_budget;  /* 1 if time_us <= budget_us (or no budget), else 0   */
+    int32_t n_candidates;   /* candidates evaluated (<= 64)                       */
+} msa_chunk_choice;
+
+int msa_choose_prefill_chunk(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks_per_seq,
+                             const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_range_indptr,
+                             const int32_t* q_ranges, const msa_pending_prefill* pending, int32_t n_pending,
+                             const msa_plan_options* opts, const msa_cost_params* params, double budget_us,
+                             int32_t granularity, int32_t max_chunk, msa_chunk_choice* choice, int32_t* cand_chunk,
+                             double* cand_time_us);
 
 /* Free a plan (NULL is a no-op).  The host memory of up to two destroyed
  * plans is kept per calling thread and reused by that thread's next
@@ -406,11 +495,29 @@ int msa_attention(const void* q, const void* k_pool, const void* v_pool, int64_t
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the one array: calls that overlap on the GPU
  * (other streams, other host threads) race and corrupt each other's results;
- * serialise them.  msa_plan_check_device does not see this array's error
- * word.
+ * serialise them.  The kernel's error word (timeouts, bad indices) lives in
+ * the same array: msa_plan_check_device does not see it;
+ * msa_no_alloc_check_device does.
  */
 int msa_attention_no_alloc(const void* q, const void* k_pool, const void* v_pool, int64_t pool_tokens,
                            msa_plan_t plan, void* out, int32_t out_dtype, float* lse, msa_stream_t stream);
+
+/*
+ * The error check of msa_attention_no_alloc (the paper has no counterpart).
+ * Synchronises `stream`, reads the error word of the library-owned array
+ * (the MSA_DEVERR_* bits a kernel of the last msa_attention_no_alloc call on
+ * this device recorded) into `detail` (may be NULL), and returns
+ * MSA_ERR_DEVICE_CHECK after clearing it if it is nonzero, else MSA_OK.  Call
+ * it after the no-alloc call it should check and before the next one: every
+ * call starts by clearing the word.  Allocates nothing.
+ */
+int msa_no_alloc_check_device(msa_stream_t stream, int32_t* detail);
+
+/*
+ * For tests of msa_no_alloc_check_device: ORs `bits` into that error word on
+ * `stream` (a one-thread kernel), as a kernel that gave up would.
+ */
+int msa_no_alloc_inject_error(int32_t bits, msa_stream_t stream);
 
 /* Bits of a device error word (msa_plan_check_device's `detail`, the
  * error_word of msa_append_kv / msa_gather_kv): a wait in a role of the
@@ -426,8 +533,12 @@ enum {
 };
 
 /* Synchronise `stream`, read the workspace's error word and return
- * MSA_ERR_DEVICE_CHECK if a kernel recorded an error (then clear it), else
- * MSA_OK.  `detail` (may be NULL) receives the raw error word. */
+ * MSA_ERR_DEVICE_CHECK if a kernel recorded an error, else MSA_OK.  `detail`
+ * (may be NULL) receives the raw error word.  On an error the word is
+ * cleared, and so are the merge counters and the work-queue head: a launch
+ * that gave up can leave them mid-count, and the next msa_attention with this
+ * plan would otherwise merge split groups wrongly.  After MSA_OK nothing is
+ * written (the kernel leaves them zeroed itself). */
 int msa_plan_check_device(msa_plan_t plan, msa_stream_t stream, int32_t* detail);
 
 const char* msa_status_string(int status);

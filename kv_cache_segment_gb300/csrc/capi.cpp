@@ -180,8 +180,15 @@ int msa_plan_check_device(msa_plan_t plan, msa_stream_t stream, int32_t* detail)
         return MSA_ERR_CUDA;
     if (detail) *detail = word;
     if (word != 0) {
-        if (cudaMemset(static_cast<uint8_t*>(plan->workspace) + plan->lay.error, 0, sizeof word) != cudaSuccess)
+        // A launch that gave up may have left merge counters of groups whose
+        // parts had only partly arrived (and the queue head) nonzero; the next
+        // launch would then pick the wrong last part.  Zero them with the word.
+        uint8_t* ws = static_cast<uint8_t*>(plan->workspace);
+        const WsLayout& W = plan->lay;
+        if (cudaMemset(ws + W.error, 0, sizeof word) != cudaSuccess) return MSA_ERR_CUDA;
+        if (W.counters_end > W.counters && cudaMemset(ws + W.counters, 0, W.counters_end - W.counters) != cudaSuccess)
             return MSA_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return MSA_ERR_CUDA;
         return MSA_ERR_DEVICE_CHECK;
     }
     return MSA_OK;

@@ -220,6 +220,97 @@ int msa_plan_estimate(msa_plan_t plan, const msa_cost_params* c, msa_cost_estima
     return estimate(plan, c, box_counts, e);
 }
 
+// Adaptive prefill chunk size: the candidate chunk sizes in ascending order
+// (multiples of the granularity up to the largest pending remainder, capped
+// at max_chunk, thinned to at most 63 multiples, plus the cap itself), a
+// plan and a latency-model prediction of the step for each, and the lowest
+// predicted time per prefill token within the budget.
+int msa_choose_prefill_chunk(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks_per_seq,
+                             const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_range_indptr,
+                             const int32_t* q_ranges, const msa_pending_prefill* pending, int32_t n_pending,
+                             const msa_plan_options* opts, const msa_cost_params* params, double budget_us,
+                             int32_t granularity, int32_t max_chunk, msa_chunk_choice* choice, int32_t* cand_chunk,
+                             double* cand_time_us) {
+    if (!dims || !seq_lens || !q_range_indptr || !pending || !params || !choice) return MSA_ERR_INVALID_ARG;
+    if (num_seqs <= 0 || n_pending <= 0 || n_pending > num_seqs || granularity < 0 || max_chunk < 0 ||
+        !std::isfinite(budget_us) || !params_ok(params))
+        return MSA_ERR_INVALID_ARG;
+    const int32_t g = granularity > 0 ? granularity : msa::kTileRows;
+    std::vector<int32_t> remain(num_seqs, -1), start(num_seqs, 0);
+    int32_t cmax = 0;
+    for (int32_t i = 0; i < n_pending; ++i) {
+        const msa_pending_prefill& pp = pending[i];
+        if (pp.seq < 0 || pp.seq >= num_seqs || remain[pp.seq] >= 0) return MSA_ERR_INVALID_ARG;
+        if (pp.start < 0 || pp.end <= pp.start) return MSA_ERR_BAD_Q_RANGE;
+        // a pending sequence's rows come from the chunk only
+        if (q_range_indptr[pp.seq + 1] != q_range_indptr[pp.seq]) return MSA_ERR_INVALID_ARG;
+        remain[pp.seq] = pp.end - pp.start;
+        start[pp.seq] = pp.start;
+        cmax = std::max(cmax, pp.end - pp.start);
+    }
+    if (max_chunk > 0) cmax = std::min(cmax, max_chunk);
+    std::vector<int32_t> cands;
+    const int32_t n_mult = cmax / g;
+    const int32_t step = std::max(1, (n_mult + 62) / 63);
+    for (int32_t k = 1; k <= n_mult; k += step) cands.push_back(k * g);
+    if (cands.empty() || cands.back() != cmax) cands.push_back(cmax);
+
+    const int32_t n_ranges = q_range_indptr[num_seqs];
+    std::vector<int32_t> lens(num_seqs), indptr(num_seqs + 1), ranges;
+    ranges.reserve(2 * ((size_t)n_ranges + n_pending));
+    int best = -1;
+    double best_per = INFINITY;
+    for (size_t ci = 0; ci < cands.size(); ++ci) {
+        const int32_t c = cands[ci];
+        int64_t tokens = 0;
+        ranges.clear();
+        indptr[0] = 0;
+        for (int32_t s = 0; s < num_seqs; ++s) {
+            if (remain[s] >= 0) {
+                const int32_t n = std::min(c, remain[s]);
+                lens[s] = start[s] + n;
+                ranges.push_back(start[s]);
+                ranges.push_back(start[s] + n);
+                tokens += n;
+            } else {
+                lens[s] = seq_lens[s];
+                for (int32_t r = q_range_indptr[s]; r < q_range_indptr[s + 1]; ++r) {
+                    ranges.push_back(q_ranges[2 * r]);
+                    ranges.push_back(q_ranges[2 * r + 1]);
+                }
+            }
+            indptr[s + 1] = (int32_t)(ranges.size() / 2);
+        }
+        msa_plan_t plan = nullptr;
+        int rc = msa_plan_create_ex(dims, num_seqs, max_blocks_per_seq, block_table, lens.data(), indptr.data(),
+                                    ranges.data(), opts, &plan);
+        if (rc != MSA_OK) return rc;
+        msa_cost_estimate e{};
+        rc = msa_plan_estimate(plan, params, &e);
+        msa_plan_destroy(plan);
+        if (rc != MSA_OK) return rc;
+        if (cand_chunk) cand_chunk[ci] = c;
+        if (cand_time_us) cand_time_us[ci] = e.time_us;
+        const double per = e.time_us / (double)tokens;
+        const bool ok = budget_us <= 0.0 || e.time_us <= budget_us;
+        // ascending c, so "<=" gives equal per-token costs to the larger chunk
+        if (ok && per <= best_per) {
+            best_per = per;
+            best = (int)ci;
+        }
+        if (ci == 0 || (int)ci == best) {
+            choice->chunk = c;
+            choice->tokens = (int32_t)tokens;
+            choice->time_us = e.time_us;
+            choice->us_per_token = per;
+        }
+    }
+    // with nothing inside the budget the smallest chunk stands (set above)
+    choice->within_budget = best >= 0 ? 1 : 0;
+    choice->n_candidates = (int32_t)cands.size();
+    return MSA_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------- eviction --
@@ -228,7 +319,9 @@ extern "C" int msa_select_evictions(const msa_dims* dims, int32_t seq_len, const
                                     double alpha, double beta, const msa_cost_params* params, int32_t n_evict,
                                     int32_t* evicted, double* cost_us) {
     if (!dims || !params || seq_len < 0) return MSA_ERR_INVALID_ARG;
-    if (mode != MSA_EVICT_LINEAR && mode != MSA_EVICT_EXPECTED_COST) return MSA_ERR_INVALID_ARG;
+    if (mode & ~(MSA_EVICT_EXPECTED_COST | MSA_EVICT_PREFIX_COST)) return MSA_ERR_INVALID_ARG;
+    const bool expected = (mode & MSA_EVICT_EXPECTED_COST) != 0;
+    const bool prefix = (mode & MSA_EVICT_PREFIX_COST) != 0;
     if (!(alpha >= 0.0) || !(beta >= 0.0) || !std::isfinite(alpha) || !std::isfinite(beta)) return MSA_ERR_INVALID_ARG;
     if (!(params->pre_tile_us >= 0.0) || !std::isfinite(params->pre_tile_us)) return MSA_ERR_INVALID_ARG;
     const int32_t nb = (seq_len + kBlock - 1) / kBlock;
@@ -238,19 +331,24 @@ extern "C" int msa_select_evictions(const msa_dims* dims, int32_t seq_len, const
     for (int32_t b = 0; b < nb; ++b)
         if (!(hit_prob[b] >= 0.0f && hit_prob[b] <= 1.0f)) return MSA_ERR_INVALID_ARG;
     std::vector<double> cost(nb);
-    double cmax = 0.0;
     for (int32_t b = 0; b < nb; ++b) {
         const int64_t p0 = (int64_t)b * kBlock, p1 = std::min<int64_t>(p0 + kBlock, seq_len);
         // sum over p in [p0, p1) of min(p + 1, seq_len) = p + 1 (p < seq_len)
         const double keys = (double)((p0 + 1 + p1) * (p1 - p0) / 2);
         cost[b] = params->pre_tile_us * dims->num_q_heads * keys / (double)(msa::kTileKeys * msa::kTileRows);
+    }
+    // prefix reading: evicting b leaves blocks b .. end to recompute
+    if (prefix)
+        for (int32_t b = nb - 2; b >= 0; --b) cost[b] += cost[b + 1];
+    double cmax = 0.0;
+    for (int32_t b = 0; b < nb; ++b) {
         cmax = std::max(cmax, cost[b]);
         if (cost_us) cost_us[b] = cost[b];
     }
     std::vector<std::pair<double, int32_t>> sc(nb);
     for (int32_t b = 0; b < nb; ++b)
-        sc[b] = {mode == MSA_EVICT_EXPECTED_COST ? (double)hit_prob[b] * cost[b]
-                                                 : alpha * (double)hit_prob[b] + (cmax > 0.0 ? beta * cost[b] / cmax : 0.0),
+        sc[b] = {expected ? (double)hit_prob[b] * cost[b]
+                          : alpha * (double)hit_prob[b] + (cmax > 0.0 ? beta * cost[b] / cmax : 0.0),
                  b};
     std::stable_sort(sc.begin(), sc.end(), [](const auto& x, const auto& y) { return x.first < y.first; });
     std::vector<int32_t> out(n_evict);

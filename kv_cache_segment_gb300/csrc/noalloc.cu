@@ -40,6 +40,41 @@ int scratch_address(void** out) {
 }  // namespace
 }  // namespace msa
 
+namespace msa {
+namespace {
+__global__ void or_error_word_kernel(int32_t* word, int32_t bits) { atomicOr(word, bits); }
+}  // namespace
+}  // namespace msa
+
+// The planner lays the error word out first (byte 0 of every workspace), so
+// it sits at byte 0 of the shared array whichever plan used it last;
+// msa_attention_no_alloc refuses a layout where it does not.
+
+extern "C" int msa_no_alloc_check_device(msa_stream_t stream, int32_t* detail) {
+    using namespace msa;
+    void* ws = nullptr;
+    const int rc = scratch_address(&ws);
+    if (rc != MSA_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MSA_ERR_CUDA;
+    int32_t word = 0;
+    if (cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return MSA_ERR_CUDA;
+    if (detail) *detail = word;
+    if (word == 0) return MSA_OK;
+    if (cudaMemset(ws, 0, sizeof word) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        return MSA_ERR_CUDA;
+    return MSA_ERR_DEVICE_CHECK;
+}
+
+extern "C" int msa_no_alloc_inject_error(int32_t bits, msa_stream_t stream) {
+    using namespace msa;
+    void* ws = nullptr;
+    const int rc = scratch_address(&ws);
+    if (rc != MSA_OK) return rc;
+    or_error_word_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(static_cast<int32_t*>(ws), bits);
+    return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
 extern "C" int msa_attention_no_alloc(const void* q, const void* k_pool, const void* v_pool, int64_t pool_tokens,
                                       msa_plan_t plan, void* out, int32_t out_dtype, float* lse,
                                       msa_stream_t stream) {
@@ -47,6 +82,7 @@ extern "C" int msa_attention_no_alloc(const void* q, const void* k_pool, const v
     if (!plan) return MSA_ERR_INVALID_ARG;
     if (out_dtype != MSA_OUT_BF16 && out_dtype != MSA_OUT_FP32) return MSA_ERR_INVALID_ARG;
     if (plan->lay.total > kNoAllocWorkspaceBytes) return MSA_ERR_WORKSPACE_TOO_SMALL;
+    if (plan->lay.error != 0) return MSA_ERR_INVALID_ARG;
     if (plan->info.num_q_rows == 0) return MSA_OK;
     if (!q || !k_pool || !v_pool || !out) return MSA_ERR_INVALID_ARG;
     for (const void* p : {q, k_pool, v_pool, (const void*)out})

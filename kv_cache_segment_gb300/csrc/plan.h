@@ -60,7 +60,7 @@ struct msa_plan_s {
     }
 };
 // A field added to msa_plan_s must also be reset in reset().
-static_assert(sizeof(msa_plan_s) == 504, "msa_plan_s changed: update reset()");
+static_assert(sizeof(msa_plan_s) == 520, "msa_plan_s changed: update reset()");
 
 namespace msa {
 

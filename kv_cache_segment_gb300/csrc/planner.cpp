@@ -358,6 +358,8 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
     I.prefill_split = pre_split;
 
     build_image(P);
+    I.counters_offset = (int64_t)P->lay.counters;
+    I.counters_bytes = (int64_t)(P->lay.counters_end - P->lay.counters);
     I.host_plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
     *out = guard.release();
     return MSA_OK;

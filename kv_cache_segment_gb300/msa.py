@@ -31,6 +31,7 @@ MSA_OUT_BF16 = 0
 MSA_OUT_FP32 = 1
 MSA_EVICT_LINEAR = 0
 MSA_EVICT_EXPECTED_COST = 1
+MSA_EVICT_PREFIX_COST = 2  # OR-ed into either mode: the prefix reading of the recompute cost
 MSA_DEVERR_TIMEOUT_PRODUCER = 1 << 0
 MSA_DEVERR_TIMEOUT_MMA = 1 << 1
 MSA_DEVERR_TIMEOUT_COMPUTE = 1 << 2
@@ -60,7 +61,8 @@ class msa_plan_info(ctypes.Structure):
                 ("decode_kv_bytes", ctypes.c_int64), ("decode_qo_bytes", ctypes.c_int64),
                 ("prefill_flops", ctypes.c_double), ("max_pool_row", ctypes.c_int64),
                 ("host_plan_us", ctypes.c_double), ("decode_split", ctypes.c_double),
-                ("prefill_split", ctypes.c_double)]
+                ("prefill_split", ctypes.c_double), ("counters_offset", ctypes.c_int64),
+                ("counters_bytes", ctypes.c_int64)]
 
 
 class msa_cost_params(ctypes.Structure):
@@ -81,6 +83,16 @@ class msa_cost_estimate(ctypes.Structure):
 
 
 COST_PARAM_NAMES = tuple(name for name, _ in msa_cost_params._fields_)
+
+
+class msa_pending_prefill(ctypes.Structure):
+    _fields_ = [("seq", ctypes.c_int32), ("start", ctypes.c_int32), ("end", ctypes.c_int32)]
+
+
+class msa_chunk_choice(ctypes.Structure):
+    _fields_ = [("chunk", ctypes.c_int32), ("tokens", ctypes.c_int32), ("time_us", ctypes.c_double),
+                ("us_per_token", ctypes.c_double), ("within_budget", ctypes.c_int32),
+                ("n_candidates", ctypes.c_int32)]
 
 
 class msa_plan_options(ctypes.Structure):
@@ -113,6 +125,10 @@ def load(path: str = LIB_PATH):
         "msa_plan_estimate": ([vp, ctypes.POINTER(msa_cost_params), ctypes.POINTER(msa_cost_estimate)],
                               ctypes.c_int),
         "msa_plan_destroy": ([vp], ctypes.c_int),
+        "msa_choose_prefill_chunk": ([ctypes.POINTER(msa_dims), i32, i32, vp, vp, vp, vp, vp, i32,
+                                      ctypes.POINTER(msa_plan_options), ctypes.POINTER(msa_cost_params),
+                                      ctypes.c_double, i32, i32, ctypes.POINTER(msa_chunk_choice), vp, vp],
+                                     ctypes.c_int),
         "msa_select_evictions": ([ctypes.POINTER(msa_dims), i32, vp, i32, ctypes.c_double, ctypes.c_double,
                                   ctypes.POINTER(msa_cost_params), i32, vp, vp], ctypes.c_int),
         "msa_append_kv": ([vp, vp, vp, i32, vp, vp, i64, ctypes.POINTER(msa_dims), vp, vp], ctypes.c_int),
@@ -121,6 +137,8 @@ def load(path: str = LIB_PATH):
         "msa_attention": ([vp, vp, vp, i64, vp, vp, i32, vp, vp], ctypes.c_int),
         "msa_attention_no_alloc": ([vp, vp, vp, i64, vp, vp, i32, vp, vp], ctypes.c_int),
         "msa_plan_check_device": ([vp, vp, ctypes.POINTER(i32)], ctypes.c_int),
+        "msa_no_alloc_check_device": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
+        "msa_no_alloc_inject_error": ([i32, vp], ctypes.c_int),
         "msa_status_string": ([ctypes.c_int], ctypes.c_char_p),
     }
     for name, (args, res) in sigs.items():
@@ -208,6 +226,36 @@ def msa_plan_create_ex(dims: msa_dims, block_table, seq_lens, q_range_indptr, q_
                                 ctypes.byref(plan))
     _check(rc, "msa_plan_create_ex")
     return plan.value
+
+
+def msa_choose_prefill_chunk(dims: msa_dims, block_table, seq_lens, q_range_indptr, q_ranges, pending, params,
+                             budget_us: float = 0.0, granularity: int = 0, max_chunk: int = 0, num_sms: int = 0,
+                             decode_split: float = 0.0, prefill_split: float = 0.0):
+    """Chunk size for the pending prefills (list of (seq, start, end)) that
+    minimises the predicted step time per prefill token within budget_us;
+    returns (choice dict, candidates int32[n], predicted times float64[n]).
+    params: dict of msa_cost_params names."""
+    lib = load()
+    table = np.ascontiguousarray(block_table, np.int32)
+    if table.ndim != 2:
+        table = table.reshape(len(seq_lens), -1)
+    lens = np.ascontiguousarray(seq_lens, np.int32)
+    indptr = np.ascontiguousarray(q_range_indptr, np.int32)
+    ranges = np.ascontiguousarray(q_ranges, np.int32).reshape(-1, 2)
+    pend = (msa_pending_prefill * max(1, len(pending)))(*[msa_pending_prefill(*map(int, p)) for p in pending])
+    c = msa_cost_params(*[float(params[k]) for k in COST_PARAM_NAMES])
+    opts = msa_plan_options(int(num_sms), float(decode_split), float(prefill_split), None)
+    choice = msa_chunk_choice()
+    cand = np.zeros(64, np.int32)
+    times = np.zeros(64, np.float64)
+    _check(lib.msa_choose_prefill_chunk(ctypes.byref(dims), len(lens), table.shape[1], table.ctypes.data,
+                                        lens.ctypes.data, indptr.ctypes.data,
+                                        ranges.ctypes.data if ranges.size else None, pend, len(pending),
+                                        ctypes.byref(opts), ctypes.byref(c), float(budget_us), int(granularity),
+                                        int(max_chunk), ctypes.byref(choice), cand.ctypes.data, times.ctypes.data),
+           "msa_choose_prefill_chunk")
+    n = choice.n_candidates
+    return {name: getattr(choice, name) for name, _ in msa_chunk_choice._fields_}, cand[:n], times[:n]
 
 
 def msa_plan_workspace_bytes(plan) -> int:
@@ -320,3 +368,16 @@ def msa_plan_check_device(plan, stream=None):
     word = ctypes.c_int32(0)
     rc = load().msa_plan_check_device(plan, _stream(stream), ctypes.byref(word))
     return rc, word.value
+
+
+def msa_no_alloc_check_device(stream=None):
+    """(status, raw error word) of the last msa_attention_no_alloc call on the
+    current device; synchronises the stream and clears a nonzero word."""
+    word = ctypes.c_int32(0)
+    rc = load().msa_no_alloc_check_device(_stream(stream), ctypes.byref(word))
+    return rc, word.value
+
+
+def msa_no_alloc_inject_error(bits: int, stream=None):
+    """Test hook: OR `bits` into the no-alloc error word on `stream`."""
+    _check(load().msa_no_alloc_inject_error(int(bits), _stream(stream)), "msa_no_alloc_inject_error")

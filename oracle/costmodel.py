@@ -140,3 +140,61 @@ def hole_recompute_flops(head_dim, num_q_heads, start, end, seq_len):
     holding seq_len tokens: 4 * D * Hq * sum over p of min(p + 1, seq_len),
     the position-aware recompute cost (a row at p attends to p + 1 keys)."""
     return 4.0 * head_dim * num_q_heads * sum(min(p + 1, seq_len) for p in range(start, end))
+
+
+# --------------------------------------------------------- prefill chunking --
+#
+# AsymCache explainer, "核心方法 3" (adaptive chunking scheduler) and the MSA
+# paper's methodology (a dynamic chunking scheduler that adapts prefill sizes
+# to the hardware): a step runs the batch's other rows plus the next c
+# positions of each pending prefill; the chunk size trades the step's fixed
+# costs (launch, decode rows, per-item overheads), which a larger chunk
+# spreads over more prefill tokens, against the step's latency.  The choice:
+# the lowest predicted step time per prefill token among the candidates
+# whose predicted time stays within the budget.
+
+def chunk_candidates(max_remaining, granularity=0, max_chunk=0):
+    """Multiples of the granularity (default 128) up to C = min(max_chunk,
+    max_remaining) (no cap when max_chunk is 0), every k-th of them with
+    k = ceil(multiples / 63) when there are more than 63, then C itself if
+    it is not the last one."""
+    g = granularity if granularity > 0 else TILE
+    cap = max_remaining if max_chunk <= 0 else min(max_remaining, max_chunk)
+    n_mult = cap // g
+    step = max(1, -(-n_mult // 63))
+    out = [k * g for k in range(1, n_mult + 1, step)]
+    if not out or out[-1] != cap:
+        out.append(cap)
+    return out
+
+
+def chunk_batch(seq_lens, q_range_indptr, q_ranges, pending, c):
+    """The step's batch with chunk c: (seq_lens, indptr, ranges, prefill
+    tokens).  A pending sequence (seq, start, end) runs rows [start, start +
+    n) with n = min(c, end - start) and holds start + n cached tokens (the
+    chunk's own K/V is appended first); every other sequence keeps its rows."""
+    lens = [int(x) for x in seq_lens]
+    pend = {int(s): (int(a), int(b)) for s, a, b in pending}
+    indptr, ranges, tokens = [0], [], 0
+    for s in range(len(lens)):
+        if s in pend:
+            a, b = pend[s]
+            n = min(c, b - a)
+            lens[s] = a + n
+            ranges.append((a, a + n))
+            tokens += n
+        else:
+            ranges.extend((int(q_ranges[r][0]), int(q_ranges[r][1]))
+                          for r in range(q_range_indptr[s], q_range_indptr[s + 1]))
+        indptr.append(len(ranges))
+    return lens, indptr, ranges, tokens
+
+
+def choose_chunk(cands, times_us, tokens, budget_us):
+    """(chunk, within budget): the lowest times_us / tokens among candidates
+    with times_us <= budget_us (budget_us <= 0: all), equal costs to the
+    larger chunk; with none inside the budget, the smallest candidate."""
+    ok = [(t / n, -c, c) for c, t, n in zip(cands, times_us, tokens) if budget_us <= 0 or t <= budget_us]
+    if not ok:
+        return min(cands), False
+    return min(ok)[2], True

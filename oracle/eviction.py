@@ -4,10 +4,21 @@ against it).
 
 AsymCache explainer, "核心方法 2": blocks are evicted lowest score first,
 the score weighing a block's future hit probability (weight alpha) against
-its position-aware recompute cost (weight beta).  The cost of block b is the
-attention work of recomputing its rows: each row p attends to min(p + 1, L)
-keys, so the work is sum over b's rows of min(p + 1, L), here in units of a
-128x128 tile of one head times Hq heads at `pre_tile_us` per tile and head.
+its position-aware recompute cost (weight beta).  The page gives the cost
+two readings, and both are here:
+
+* hole reading: only the evicted block is rebuilt; its cost is the
+  attention work of recomputing its own rows.  Row p attends to min(p + 1, L)
+  keys, so the work is the sum of min(p + 1, L) over the block's rows, here
+  in units of a 128x128 tile of one head, times Hq heads, at `pre_tile_us`
+  per tile and head.  It grows with position (the page: the cost depends
+  strongly on where the block sits).
+* prefix reading: a block's cache is usable only with its whole prefix, so
+  evicting block b leaves blocks b, b+1, ..., last to recompute; its cost is
+  the sum of the hole costs of those blocks.  It falls with position, so the
+  tail blocks are the cheap ones (the page: tail blocks are cheap and should
+  yield first).
+
 The cost enters normalised by its largest value over the sequence, on the
 keep side (a block that is dear to recompute scores higher); equal scores
 evict the lower block first.
@@ -18,7 +29,7 @@ BLOCK = 16
 
 
 def recompute_cost_us(seq_len, num_q_heads, pre_tile_us):
-    """Per block: pre_tile_us * Hq * (sum of min(p + 1, L) over its rows) / 128^2."""
+    """Hole reading, per block: pre_tile_us * Hq * (sum of min(p + 1, L) over its rows) / 128^2."""
     out = []
     n_blocks = -(-int(seq_len) // BLOCK)
     for b in range(n_blocks):
@@ -29,10 +40,21 @@ def recompute_cost_us(seq_len, num_q_heads, pre_tile_us):
     return out
 
 
-def select_evictions(seq_len, num_q_heads, hit_prob, alpha, beta, pre_tile_us, n_evict, expected_cost=False):
+def prefix_recompute_cost_us(seq_len, num_q_heads, pre_tile_us):
+    """Prefix reading, per block b: the hole costs of blocks b .. last, summed."""
+    hole = recompute_cost_us(seq_len, num_q_heads, pre_tile_us)
+    return [sum(hole[b:]) for b in range(len(hole))]
+
+
+def select_evictions(seq_len, num_q_heads, hit_prob, alpha, beta, pre_tile_us, n_evict, expected_cost=False,
+                     prefix=False):
     """Lowest scores first: alpha * hit + beta * cost / max cost, or (with
-    expected_cost) hit * cost, the block's expected recompute time."""
-    cost = recompute_cost_us(seq_len, num_q_heads, pre_tile_us)
+    expected_cost) hit * cost; cost in the hole reading, or the prefix
+    reading with `prefix`."""
+    if prefix:
+        cost = prefix_recompute_cost_us(seq_len, num_q_heads, pre_tile_us)
+    else:
+        cost = recompute_cost_us(seq_len, num_q_heads, pre_tile_us)
     cmax = max(cost) if cost else 0.0
     scored = []
     for b, c in enumerate(cost):

@@ -28,14 +28,15 @@
  *   oracle_dense_attention() evaluates that directly on the LOGICAL K/V
  *   (never the paged pool), one row at a time, in double precision.
  *
- *   oracle_segmented_attention() follows the explainer's pseudocode for MSA
- *   ("核心方法 1", the multi_segment_attention listing): split the live
- *   blocks of a sequence into physically contiguous segments, attend to each
- *   segment separately, and combine the per-segment results.  The listing's
- *   combine factor ("normalizer(seg)") is garbled on the page; the only
- *   reading that keeps the result exact is the log-sum-exp merge
+ *   oracle_segmented_attention() computes the same result the way MSA
+ *   organises it (AsymCache explainer, "核心方法 1": the live blocks of a
+ *   sequence are split into physically contiguous segments, each segment is
+ *   attended on its own, and the per-segment results are combined; MSA paper
+ *   abstract: the outputs stay exact).  Segment r gives a softmax partial, its
+ *   normalised output o_r and log-sum-exp lse_r over the visible keys it
+ *   holds, and the partials are merged by log-sum-exp, the combination
+ *   under which the result is exact:
  *       LSE = ln sum_r exp(lse_r),   out = sum_r exp(lse_r - LSE) * o_r
- *   where (o_r, lse_r) is segment r's normalised output and log-sum-exp.
  *   Segments are maximal runs of logical blocks i..j whose block-table
  *   entries rise by exactly one per block (logically AND physically
  *   contiguous), found left to right.  This path reads the paged pool

@@ -143,9 +143,70 @@ def pin_recompute_flops(oc):
         assert oc.hole_recompute_flops(128, 8, a, b, L) == 4.0 * 128 * 8 * s
 
 
+# ---------------------------------------------------------------- chunking --
+
+def pin_chunk_candidates(oc):
+    """Multiples of 128 up to the remainder, the remainder itself last; a cap
+    cuts them; a remainder under one tile is the only candidate; 64
+    multiples are thinned to every second (k = ceil(64 / 63) = 2), and the
+    cap is added after 63 * 128 = 8064."""
+    assert oc.chunk_candidates(1000) == [128, 256, 384, 512, 640, 768, 896, 1000]
+    assert oc.chunk_candidates(1000, 128, 300) == [128, 256, 300]
+    assert oc.chunk_candidates(100) == [100]
+    assert oc.chunk_candidates(1024, 256) == [256, 512, 768, 1024]
+    c = oc.chunk_candidates(8192)
+    assert c == [128 * k for k in range(1, 64, 2)] + [8192] and len(c) == 33
+
+
+def _closed_form_times(cands, F=32.0, a=1.0 / 1024.0, p0=4096):
+    # one pending prefill at position p0: fixed step cost F plus attention
+    # work a * sum over its c rows of (p0 + i), ~ a * c * (p0 + c / 2)
+    return [F + a * c * (p0 + c / 2.0) for c in cands]
+
+
+def pin_chunk_closed_form_optimum(oc):
+    """T(c) = F + a c (p0 + c/2): T/c = F/c + a p0 + a c/2 is least at
+    c* = sqrt(2F/a) = sqrt(2 * 32 * 1024) = 256 (per-token 4.25 against
+    4.3125 at 128 and 4.2708 at 384)."""
+    cands = [128 * k for k in range(1, 9)]
+    t = _closed_form_times(cands)
+    assert oc.choose_chunk(cands, t, cands, 0.0) == (256, True)
+
+
+def pin_chunk_budget(oc):
+    """T(256) = 32 + 0.25 * 4224 = 1088 and T(128) = 32 + 0.125 * 4160 = 552:
+    a budget of 1000 leaves 128; a budget of 100 leaves nothing, and the
+    smallest candidate comes back outside the budget."""
+    cands = [128 * k for k in range(1, 9)]
+    t = _closed_form_times(cands)
+    assert t[0] == 552.0 and t[1] == 1088.0
+    assert oc.choose_chunk(cands, t, cands, 1000.0) == (128, True)
+    assert oc.choose_chunk(cands, t, cands, 100.0) == (128, False)
+
+
+def pin_chunk_ties_to_the_larger(oc):
+    """Time proportional to tokens (no fixed cost): every chunk costs the
+    same per token, and the largest wins."""
+    cands = [128, 256, 384]
+    assert oc.choose_chunk(cands, [2.0 * c for c in cands], cands, 0.0) == (384, True)
+
+
+def pin_chunk_batch(oc):
+    """A pending sequence runs rows [start, start + min(c, end - start)) and
+    holds start + that many tokens; the others keep their rows."""
+    lens, indptr, ranges, tokens = oc.chunk_batch([100, 900, 50], [0, 1, 1, 2], [(100, 101), (49, 50)],
+                                                  [(1, 300, 700)], 256)
+    assert lens == [100, 556, 50] and indptr == [0, 1, 2, 3] and ranges == [(100, 101), (300, 556), (49, 50)]
+    assert tokens == 256
+    lens, _, ranges, tokens = oc.chunk_batch([100, 900, 50], [0, 1, 1, 2], [(100, 101), (49, 50)],
+                                             [(1, 300, 700)], 1024)
+    assert lens[1] == 700 and ranges[1] == (300, 700) and tokens == 400
+
+
 COST_PINS = [pin_one_cta_mixed_items, pin_split_prefill_pays_its_merge, pin_row_pair_prefill_counts_two_tiles,
              pin_queue_order, pin_shared_bandwidth,
-             pin_equal_items_in_rounds, pin_tma_boxes, pin_recompute_flops]
+             pin_equal_items_in_rounds, pin_tma_boxes, pin_recompute_flops, pin_chunk_candidates,
+             pin_chunk_closed_form_optimum, pin_chunk_budget, pin_chunk_ties_to_the_larger, pin_chunk_batch]
 
 
 # ------------------------------------------------------------------ eviction --
@@ -203,5 +264,52 @@ def pin_expected_cost_optimum(oe):
         assert math.isclose(got, best, rel_tol=1e-12, abs_tol=1e-12) and len(ev) == n
 
 
+def pin_prefix_cost_closed_form(oe):
+    """Prefix reading: evicting block b leaves positions 16b .. L-1 to
+    recompute, so cost(b) = pre_tile * Hq * sum_{p=16b}^{L-1} (p + 1) / 128^2
+    = pre_tile * Hq * (L(L+1) - 16b(16b+1)) / 2 / 128^2, whatever the blocks
+    after b look like (the last one partial here)."""
+    L, hq, pt = 1000, 32, 0.875
+    cost = oe.prefix_recompute_cost_us(L, hq, pt)
+    assert len(cost) == 63
+    for b in (0, 1, 31, 62):
+        want = pt * hq * ((L * (L + 1) - 16 * b * (16 * b + 1)) // 2) / 16384
+        assert math.isclose(cost[b], want, rel_tol=1e-13)
+
+
+def pin_prefix_hand_worked(oe):
+    """L = 48 (three full blocks), Hq = 1, pre_tile = 128^2 (cost in keys):
+    hole costs 136, 392, 648; prefix costs 1176, 1040, 648.  With hit
+    probabilities 0.9, 0.2, 0.5 the expected costs are 1058.4, 208, 324
+    (prefix) against 122.4, 78.4, 324 (hole): one eviction takes block 1 in
+    both readings, two take blocks 1 and 2 (prefix) but 0 and 1 (hole)."""
+    assert oe.recompute_cost_us(48, 1, 16384.0) == [136.0, 392.0, 648.0]
+    assert oe.prefix_recompute_cost_us(48, 1, 16384.0) == [1176.0, 1040.0, 648.0]
+    hit = [0.9, 0.2, 0.5]
+    assert oe.select_evictions(48, 1, hit, 0, 0, 16384.0, 1, expected_cost=True, prefix=True)[0] == [1]
+    assert oe.select_evictions(48, 1, hit, 0, 0, 16384.0, 2, expected_cost=True, prefix=True)[0] == [1, 2]
+    assert oe.select_evictions(48, 1, hit, 0, 0, 16384.0, 2, expected_cost=True)[0] == [0, 1]
+
+
+def pin_prefix_cost_only_evicts_the_tail(oe):
+    """beta alone in the prefix reading: cost falls strictly with position,
+    so the last blocks go first (the cheap tail yields)."""
+    ev, cost = oe.select_evictions(40 * 16 + 5, 32, np.full(41, 0.5), 0.0, 1.0, 0.875, 7, prefix=True)
+    assert ev == list(range(34, 41))
+    assert all(b < a for a, b in zip(cost[:-1], cost[1:]))
+
+
+def pin_prefix_ties_to_lower_block(oe):
+    """Equal scores evict the lower block first in the prefix reading too
+    (alpha only, equal hits; and zero hit in expected-cost mode)."""
+    ev, _ = oe.select_evictions(20 * 16, 32, np.full(20, 0.3), 1.0, 0.0, 0.875, 5, prefix=True)
+    assert ev == [0, 1, 2, 3, 4]
+    hit = np.full(20, 0.5)
+    hit[[3, 9, 15]] = 0.0
+    ev, _ = oe.select_evictions(20 * 16, 32, hit, 0.0, 0.0, 0.875, 2, expected_cost=True, prefix=True)
+    assert ev == [3, 9]
+
+
 EVICTION_PINS = [pin_block_cost, pin_hit_only, pin_cost_only, pin_cost_on_the_keep_side, pin_ties_to_lower_block,
-                 pin_expected_cost_optimum]
+                 pin_expected_cost_optimum, pin_prefix_cost_closed_form, pin_prefix_hand_worked,
+                 pin_prefix_cost_only_evicts_the_tail, pin_prefix_ties_to_lower_block]

@@ -244,3 +244,81 @@ def test_fit_recovers_known_constants():
     finally:
         for p in plans:
             msa.msa_plan_destroy(p)
+
+
+# ------------------------------------------------------- prefill chunk size --
+
+def _pending_batch():
+    """The small mixed batch: sequences 0-5 decode one row each; the prefills
+    of sequences 6 and 7 are pending from positions 27 and 25 (500 and 1000
+    positions still to run)."""
+    wl = W.small_config(5)
+    pending = [(6, 27, 527), (7, 25, 1025)]
+    indptr, ranges = [0], []
+    for s in range(wl.num_seqs):
+        if s not in (6, 7):
+            ranges.extend(wl.q_ranges[s])
+        indptr.append(len(ranges))
+    dims = msa.make_dims(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, 16, wl.scale)
+    return wl, dims, pending, indptr, ranges
+
+
+@pytest.mark.parametrize("budget", ["none", "median", "tiny"])
+def test_chunk_choice_matches_oracle(budget):
+    """Candidates, each candidate's predicted step time (the oracle's latency
+    model on the plan of that candidate's batch) and the choice."""
+    wl, dims, pending, indptr, ranges = _pending_batch()
+    lens = wl.seq_lens.tolist()
+    choice, cands, times = msa.msa_choose_prefill_chunk(dims, wl.block_table, lens, indptr, ranges, pending, PARAMS,
+                                                        num_sms=152)
+    b = {"none": 0.0, "median": float(sorted(times)[len(times) // 2]), "tiny": 1.0}[budget]
+    if b:
+        choice, cands, times = msa.msa_choose_prefill_chunk(dims, wl.block_table, lens, indptr, ranges, pending,
+                                                            PARAMS, budget_us=b, num_sms=152)
+    assert cands.tolist() == OC.chunk_candidates(1000) == [128, 256, 384, 512, 640, 768, 896, 1000]
+    tokens = []
+    for c, t in zip(cands.tolist(), times.tolist()):
+        lc, ic, rc, n = OC.chunk_batch(lens, indptr, ranges, pending, c)
+        tokens.append(n)
+        plan = msa.msa_plan_create(dims, wl.block_table, lc, ic, rc, 152)
+        try:
+            items = msa.msa_plan_get_items(plan).tolist()
+            order = msa.msa_plan_get_order(plan).tolist()
+            ref = OC.estimate(items, order, wl.block_table, lc, 152, PARAMS, wl.head_dim)
+        finally:
+            msa.msa_plan_destroy(plan)
+        assert t == pytest.approx(ref["time_us"], rel=1e-9), c
+    want = OC.choose_chunk(cands.tolist(), times.tolist(), tokens, b)
+    assert (choice["chunk"], bool(choice["within_budget"])) == want
+    i = cands.tolist().index(choice["chunk"])
+    assert choice["tokens"] == tokens[i] and choice["time_us"] == times[i]
+    assert choice["n_candidates"] == len(cands)
+    if budget == "tiny":
+        assert choice["chunk"] == 128 and not choice["within_budget"]
+
+
+def test_chunk_choice_granularity_and_cap():
+    wl, dims, pending, indptr, ranges = _pending_batch()
+    _, cands, _ = msa.msa_choose_prefill_chunk(dims, wl.block_table, wl.seq_lens, indptr, ranges, pending, PARAMS,
+                                               granularity=256, max_chunk=700, num_sms=152)
+    assert cands.tolist() == OC.chunk_candidates(1000, 256, 700) == [256, 512, 700]
+
+
+@pytest.mark.parametrize("bad", ["own_rows", "negative_start", "empty_range", "twice", "seq_out_of_range"])
+def test_chunk_choice_rejects_bad_pending(bad):
+    wl, dims, pending, indptr, ranges = _pending_batch()
+    want = msa.MSA_ERR_INVALID_ARG
+    if bad == "own_rows":
+        pending = [(0, 10, 500)]  # sequence 0 already runs a decode row in the batch
+    elif bad == "negative_start":
+        pending, want = [(6, -1, 500)], msa.MSA_ERR_BAD_Q_RANGE
+    elif bad == "empty_range":
+        pending, want = [(6, 300, 300)], msa.MSA_ERR_BAD_Q_RANGE
+    elif bad == "twice":
+        pending = [(6, 27, 527), (6, 27, 527)]
+    else:
+        pending = [(8, 0, 100)]
+    with pytest.raises(msa.MsaError) as e:
+        msa.msa_choose_prefill_chunk(dims, wl.block_table, wl.seq_lens, indptr, ranges, pending, PARAMS,
+                                     num_sms=152)
+    assert e.value.status == want

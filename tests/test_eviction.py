@@ -14,7 +14,7 @@ def _dims(hq=32, hkv=8, d=128):
     return msa.make_dims(hq, hkv, d)
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(24))
 def test_library_matches_oracle(seed):
     rng = np.random.default_rng(seed)
     L = int(rng.integers(1, 5000))
@@ -24,11 +24,14 @@ def test_library_matches_oracle(seed):
         hit = np.round(hit * 4) / 4  # many ties
     alpha, beta = float(rng.random() * 2), float(rng.random() * 2)
     n = int(rng.integers(0, nb + 1))
-    mode = seed % 3 == 2
-    ev, cost = msa.msa_select_evictions(_dims(), L, hit, alpha, beta, PARAMS, n, mode=int(mode))
-    want, want_cost = OE.select_evictions(L, 32, hit, alpha, beta, PARAMS["pre_tile_us"], n, expected_cost=mode)
+    expected, prefix = seed % 3 == 2, seed % 4 >= 2
+    mode = (msa.MSA_EVICT_EXPECTED_COST if expected else 0) | (msa.MSA_EVICT_PREFIX_COST if prefix else 0)
+    ev, cost = msa.msa_select_evictions(_dims(), L, hit, alpha, beta, PARAMS, n, mode=mode)
+    want, want_cost = OE.select_evictions(L, 32, hit, alpha, beta, PARAMS["pre_tile_us"], n, expected_cost=expected,
+                                          prefix=prefix)
     assert ev.tolist() == want
-    assert np.allclose(cost, want_cost, rtol=0, atol=0)
+    # the suffix sums may add in another order: equal to the last few ulps
+    assert np.allclose(cost, want_cost, rtol=1e-13 if prefix else 0, atol=0)
 
 
 def test_hit_only_evicts_the_least_likely_blocks():
@@ -45,6 +48,26 @@ def test_cost_only_evicts_the_earliest_blocks():
     ev, cost = msa.msa_select_evictions(_dims(), L, hit, 0.0, 1.0, PARAMS, 7)
     assert ev.tolist() == list(range(7))
     assert np.all(np.diff(cost[:-1]) > 0)
+
+
+def test_prefix_reading_evicts_the_tail_first():
+    """Prefix reading, beta alone: the cost of evicting block b is the
+    recompute of b .. end, which falls with position, so the last blocks go."""
+    L = 40 * 16 + 5
+    hit = np.full(41, 0.5, np.float32)
+    ev, cost = msa.msa_select_evictions(_dims(), L, hit, 0.0, 1.0, PARAMS, 7, mode=msa.MSA_EVICT_PREFIX_COST)
+    assert ev.tolist() == list(range(34, 41))
+    assert np.all(np.diff(cost) < 0)
+
+
+@pytest.mark.parametrize("b", [0, 1, 31, 62])
+def test_prefix_cost_closed_form(b):
+    """prefix cost(b) = pre_tile_us * Hq * (L(L+1) - 16b(16b+1)) / 2 / 128^2."""
+    L, hq = 1000, 32
+    _, cost = msa.msa_select_evictions(_dims(hq), L, np.zeros(63, np.float32), 1.0, 1.0, PARAMS, 0,
+                                       mode=msa.MSA_EVICT_PREFIX_COST)
+    want = PARAMS["pre_tile_us"] * hq * ((L * (L + 1) - 16 * b * (16 * b + 1)) // 2) / 16384
+    assert cost[b] == pytest.approx(want, rel=1e-13)
 
 
 @pytest.mark.parametrize("b,L", [(0, 1000), (10, 1000), (62, 1000)])
@@ -90,5 +113,5 @@ def test_expected_cost_mode_minimises_expected_recompute():
 
 def test_unknown_mode_is_rejected():
     with pytest.raises(msa.MsaError) as e:
-        msa.msa_select_evictions(_dims(), 160, np.zeros(10, np.float32), 1.0, 1.0, PARAMS, 2, mode=7)
+        msa.msa_select_evictions(_dims(), 160, np.zeros(10, np.float32), 1.0, 1.0, PARAMS, 2, mode=4)
     assert e.value.status == msa.MSA_ERR_INVALID_ARG

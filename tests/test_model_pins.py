@@ -43,6 +43,13 @@ MUTATIONS = [
     ("costmodel", "launch_left_out", 'out["time_us"] = params["launch_us"] + t', 'out["time_us"] = t'),
     ("costmodel", "recompute_row_misses_itself", "sum(min(p + 1, seq_len) for p in range(start, end))",
      "sum(min(p, seq_len) for p in range(start, end))"),
+    ("costmodel", "chunk_budget_ignored", "if budget_us <= 0 or t <= budget_us]", "]"),
+    ("costmodel", "chunk_total_time_not_per_token", "ok = [(t / n, -c, c)", "ok = [(t, -c, c)"),
+    ("costmodel", "chunk_ties_to_the_smaller", "ok = [(t / n, -c, c)", "ok = [(t / n, c, c)"),
+    ("costmodel", "chunk_cap_not_a_candidate", "    if not out or out[-1] != cap:\n        out.append(cap)\n",
+     "    if not out:\n        out.append(cap)\n"),
+    ("costmodel", "chunk_thinning_off_by_one", "step = max(1, -(-n_mult // 63))", "step = max(1, n_mult // 63)"),
+    ("costmodel", "chunk_rows_not_capped_by_remainder", "n = min(c, b - a)", "n = c"),
     ("eviction", "cost_row_misses_itself", "keys += min(p + 1, seq_len)", "keys += min(p, seq_len)"),
     ("eviction", "cost_on_the_evict_side", "(beta * c / cmax if cmax > 0 else 0.0)",
      "(-beta * c / cmax if cmax > 0 else 0.0)"),
@@ -50,6 +57,9 @@ MUTATIONS = [
     ("eviction", "ties_to_higher_block", "key=lambda x: (x[0], x[1])", "key=lambda x: (x[0], -x[1])"),
     ("eviction", "expected_cost_added", "s = float(hit_prob[b]) * c", "s = float(hit_prob[b]) + c"),
     ("eviction", "keeps_the_lowest", "scored[:n_evict]", "scored[len(scored) - n_evict:]"),
+    ("eviction", "prefix_sums_the_wrong_side", "sum(hole[b:])", "sum(hole[:b + 1])"),
+    ("eviction", "prefix_leaves_the_block_out", "sum(hole[b:])", "sum(hole[b + 1:])"),
+    ("eviction", "prefix_reading_ignored", "    if prefix:\n", "    if False:\n"),
 ]
 
 

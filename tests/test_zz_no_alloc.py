@@ -63,3 +63,33 @@ def test_no_alloc_rejects_oversized_plan():
         assert e.value.status == msa.MSA_ERR_WORKSPACE_TOO_SMALL
     finally:
         msa.msa_plan_destroy(plan)
+
+
+def test_no_alloc_errors_are_visible_and_cleared():
+    """msa_no_alloc_check_device reads the error word the no-alloc calls
+    share: zero after clean calls; a word planted from the host (as a kernel
+    that gave up would leave it) is reported once and cleared; a call after
+    that is still exact."""
+    wl = W.small_config(5)
+    k, v, q = W.make_values(wl)
+    dev = torch.device("cuda")
+    kp, vp = W.make_pool(wl, k.to(dev), v.to(dev))
+    qd = q.to(dev)
+    sess = MsaSession.from_workload(wl, num_sms=600)
+    stream = torch.cuda.current_stream()
+    ro, rl = oracle_ref(wl, k, v, q)
+    try:
+        out = torch.empty((wl.num_q_rows, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((wl.num_q_rows, wl.num_q_heads), dtype=torch.float32, device=dev)
+        msa.msa_attention_no_alloc(qd, kp, vp, kp.shape[0], sess.plan, out, msa.MSA_OUT_BF16, lse, stream)
+        assert msa.msa_no_alloc_check_device(stream) == (msa.MSA_OK, 0)
+        bits = msa.MSA_DEVERR_TIMEOUT_MMA | msa.MSA_DEVERR_BAD_INDEX
+        msa.msa_no_alloc_inject_error(bits, stream)
+        assert msa.msa_no_alloc_check_device(stream) == (msa.MSA_ERR_DEVICE_CHECK, bits)
+        assert msa.msa_no_alloc_check_device(stream) == (msa.MSA_OK, 0)
+        out.fill_(float("nan"))
+        msa.msa_attention_no_alloc(qd, kp, vp, kp.shape[0], sess.plan, out, msa.MSA_OUT_BF16, lse, stream)
+        assert msa.msa_no_alloc_check_device(stream) == (msa.MSA_OK, 0)
+        compare(out, lse, ro, rl, "no_alloc after a reported error")
+    finally:
+        sess.close()
