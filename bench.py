@@ -731,6 +731,52 @@ def eviction_leg(dev, stream, steps, warm):
     return res
 
 
+def chunking_leg(dev, stream, steps, warm, budget_us=500.0):
+    """Adaptive prefill chunk size on the mixed batch (64 decode rows + 4
+    pending prefills of their last <= 8192 positions, 64/8 heads, D=128):
+    msa_choose_prefill_chunk's choice, unconstrained and under a step budget,
+    against fixed chunks of 512 to 4096; for each, the measured step
+    (attention) time, prefill tokens per second and the model's prediction.
+    Plans use the default split factors, as the chooser's plans do."""
+    import torch
+    from kv_cache_segment_gb300 import costfit, msa
+    from kv_cache_segment_gb300 import workloads as W
+    params = costfit.load_params()
+    if params is None:
+        return {"skipped": "no fitted latency-model constants"}
+    wl = W.config(5)
+    base, pending = W.pending_prefills(wl)
+    dims = msa.make_dims(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, 16, wl.scale)
+    grid = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {"pending": [list(p) for p in pending], "budget_us": budget_us}
+    chosen = {}
+    for key, b in (("chosen", 0.0), ("chosen_within_budget", budget_us)):
+        ch, cands, times = msa.msa_choose_prefill_chunk(dims, base.block_table, base.seq_lens, base.q_range_indptr,
+                                                         base.q_ranges_flat, pending, params, budget_us=b,
+                                                         num_sms=grid)
+        chosen[key] = ch["chunk"]
+        out[key] = {"chunk": ch["chunk"], "predicted_us": round(ch["time_us"], 1),
+                    "within_budget": bool(ch["within_budget"]), "candidates": int(ch["n_candidates"])}
+    rows = {}
+    for c in sorted({512, 1024, 2048, 4096, *chosen.values()}):
+        step = W.with_prefill_chunk(base, pending, c)
+        case = Case(step, dev)
+        _, attn_ms = time_case(case, steps, warm, stream, with_append=False)
+        tokens = sum(min(c, e - a) for _, a, e in pending)
+        rows[str(c)] = {"attention_ms": round(attn_ms, 4), "prefill_tokens": tokens,
+                        "prefill_tokens_per_s": round(tokens / (attn_ms * 1e-3), 1),
+                        "us_per_token": round(attn_ms * 1e3 / tokens, 4),
+                        "predicted_us": _predict_us(case)}
+        del case
+        torch.cuda.empty_cache()
+    out["steps"] = rows
+    best = min(rows, key=lambda k: rows[k]["us_per_token"])
+    out["best_measured_chunk"] = int(best)
+    out["chosen_vs_best_us_per_token"] = round(rows[str(chosen["chosen"])]["us_per_token"] /
+                                               rows[best]["us_per_token"], 4)
+    return out
+
+
 def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
     """Prefill/recompute TFLOP/s (hole recompute + new turn), long context,
     mixed batch, and segmented vs contiguous layouts."""
@@ -828,6 +874,7 @@ def extra_legs(args, dev, stream, peaks, peak_src, traffic, rank):
     out["segmentation_overhead"] = over
     out["gather_then_attention"] = gathers
     out["eviction_policies"] = eviction_leg(dev, stream, steps, warm)
+    out["prefill_chunking"] = chunking_leg(dev, stream, steps, warm)
     out["decode_shapes"] = decode_shapes_leg(dev, stream, peaks, steps, warm, rank)
     out["prefill_shapes"] = prefill_shapes_leg(dev, stream, peaks, steps, warm, rank)
     return out

@@ -6,12 +6,13 @@ AsymCache weighs recompute cost against hit rate with the attention kernel's
 expected latency (MSA paper abstract; AsymCache explainer, "核心方法 2/3");
 this script gives that model its constants for this kernel and GPU.
 
-    python -m kv_cache_segment_gb300.costfit --out cost_params_gb300.json
+    python -m kv_cache_segment_gb300.costfit --out cost_params_gb300.json \
+        --table ../profiles/latency_model_fit.md
 
 Training and validation workloads are synthetic, drawn with the same
 generators as the bench (decode batches of several sizes, lengths and
 segment counts; hole recompute, also at odd GQA ratios; long-context
-chunks; mixed batches) at
+chunks; mixed batches; and the bench's four workloads at full size) at
 different seeds and sizes for the two sets, each planned with three
 different split factors (msa_plan_create_ex).  Each plan is timed as the median of
 `--reps` launches of msa_attention alone (CUDA events on the launching
@@ -61,6 +62,9 @@ def training_set():
     s.append(("long_big", W.long_context(seed=2035, num_seqs=2, length=98304, n_runs=48, chunk=2048)))
     for i, (nd, npf, chunk) in enumerate([(16, 1, 512), (64, 4, 2048), (128, 2, 1024)]):
         s.append((f"mixed{i}", W.mixed_batch(seed=2040 + i, num_decode=nd, num_prefill=npf, chunk=chunk)))
+    # the bench's workloads as the bench draws them (the model plans them)
+    for idx, name in ((2, "bench_decode"), (3, "bench_holes"), (4, "bench_long"), (5, "bench_mixed")):
+        s.append((name, W.config(idx)))
     return s
 
 
@@ -84,7 +88,10 @@ SPLITS = ((3.0, 4.0), (1.0, 1.0), (6.0, 8.0))
 
 
 def measure(wl, dev, reps=15, warmup=3, splits=SPLITS):
-    """[(median msa_attention time in us, session)] for each split plan."""
+    """[(median msa_attention time in us, session)] for each split plan.  The
+    launches run back to back, as in a serving loop or the bench, each
+    bracketed by its own CUDA events, so a launch's time starts when the
+    previous one ends and excludes the host's launch latency."""
     import torch
     from .runner import MsaSession
     k, v, q = W.make_values(wl, device=dev)
@@ -98,15 +105,13 @@ def measure(wl, dev, reps=15, warmup=3, splits=SPLITS):
         for _ in range(warmup):
             sess.attention(q, kp, vp, out=out)
         torch.cuda.synchronize()
-        times = []
-        for _ in range(reps):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
             a.record(stream)
             sess.attention(q, kp, vp, out=out)
             b.record(stream)
-            b.synchronize()
-            times.append(a.elapsed_time(b) * 1e3)
+        torch.cuda.synchronize()
+        times = [a.elapsed_time(b) * 1e3 for a, b in ev]
         rc, word = sess.check_device()
         if rc != 0:
             raise RuntimeError(f"device error word {word:#x}")
@@ -137,9 +142,29 @@ def errors(records, params):
     return {"mean_abs_rel_err": float(np.mean(np.abs(e))), "max_abs_rel_err": float(np.max(np.abs(e)))}
 
 
+def write_table(path, doc, rows):
+    """The per-plan measurements and predictions behind a fit, as text."""
+    with open(path, "w") as f:
+        f.write("# Latency model fit: measured msa_attention launches and predictions\n\n")
+        f.write(f"Device {doc['device']} ({doc['sm_count']} SMs); command `{doc['command']}`.\n")
+        f.write("Each row: the median of the launches of one plan (split factors decode/prefill), CUDA events.\n\n")
+        f.write("Parameters: " + ", ".join(f"{k} {v:g}" for k, v in doc["params"].items()) + "\n\n")
+        for which in ("train", "validation"):
+            e = doc["fit"][which]
+            f.write(f"## {which}: mean |error| {100 * e['mean_abs_rel_err']:.1f} %, "
+                    f"max {100 * e['max_abs_rel_err']:.1f} %\n\n")
+            f.write("| workload | split | items | measured us | predicted us | error |\n|---|---|---|---|---|---|\n")
+            for r in rows[which]:
+                err = r["predicted_us"] / r["measured_us"] - 1.0
+                f.write(f"| {r['workload']} | {r['decode_split']:g}/{r['prefill_split']:g} | {r['items']} | "
+                        f"{r['measured_us']:.1f} | {r['predicted_us']:.1f} | {100 * err:+.1f} % |\n")
+            f.write("\n")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=DEFAULT_PATH)
+    ap.add_argument("--table", default=None, help="also write the per-plan records as a text table here")
     ap.add_argument("--reps", type=int, default=15)
     args = ap.parse_args(argv)
     import torch
@@ -172,12 +197,14 @@ def main(argv=None):
         "sm_count": torch.cuda.get_device_properties(dev).multi_processor_count,
         "params": {k: round(v, 5) for k, v in params.items()},
         "fit": {"train": errors(train, params), "validation": errors(val, params)},
-        "records": rows,
+        "plans": {"train": len(train), "validation": len(val)},
         "seconds": round(time.time() - t0, 1),
-        "command": "python -m kv_cache_segment_gb300.costfit --out <path>",
+        "command": "python -m kv_cache_segment_gb300.costfit --out <path> --table <path>",
     }
     with open(args.out, "w") as f:
         json.dump(doc, f, indent=1)
+    if args.table:
+        write_table(args.table, doc, rows)
     print(json.dumps({"params": doc["params"], "fit": doc["fit"]}))
     for s, _ in keep["train"] + keep["validation"]:
         s.close()

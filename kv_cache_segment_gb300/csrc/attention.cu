@@ -394,7 +394,6 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
         if (it.kind != kPrefill) { kv_cnt += T; continue; }
         const Group g = p.groups[it.group];
         const int nh = g.pad;
-        const int pmin = p.pos[g.row0];  // rows ascend: the tile's smallest position
         if (!wait_bar_w(p, ctl, &ctl->q_full, q_cnt & 1, kErrTimeoutMma)) return;
         ++q_cnt;
         int2 mt_prev = make_int2(0, 0);  // metadata of tile j-1, read when its S was issued
@@ -402,13 +401,12 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
             const int jj = j - 1;
             const uint32_t kj = kv_cnt + j, kp = kv_cnt + jj;
             const int st = kj % C::kStages, stp = kp % C::kStages;
-            const bool precise = j >= 1 && mt_prev.x < kTileKeys && pmin < kTileKeys;
             const int nk = (mt_prev.y + 15) >> 4;
             int2 mt_cur = mt_prev;
             for (int k = 0; k < nh; ++k) {
-                // O_k += P_k V for tile j-1: P_k read from TMEM columns of S_k;
-                // rows that see fewer than 128 keys add a second pass with the
-                // bf16 residual of P (interleaved per 16-key step)
+                // O_k += P_k V for tile j-1: P_k (bf16 pairs) read from TMEM
+                // columns 0..63 of S_k (a softmax warp that needs the bf16
+                // residual of its rows' P adds it itself before P is ready)
                 if (j >= 1) {
                     if (!wait_bar_w(p, ctl, &ctl->p_full[k], (k ? pf1 : pf0) & 1, kErrTimeoutMma)) return;
                     if (k) ++pf1; else ++pf0;
@@ -420,19 +418,15 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
                     ptx::tc_fence_after();
                     const uint32_t vl = lV + (uint32_t)((stp * C::kTileBytes) >> 4);
                     const uint32_t to = tbase + C::kTmemO + k * D, tp = tbase + k * 128;
-                    // 16 keys per MMA: V rows ks*16.. start 16*128 bytes further
-                    if (!precise && nk == kTileKeys / 16) {
-                        ptx::tc_mma_ts_e<-1>(to, tp, vl, hi, kIdescPV, jj > 0 ? 1u : 0u);
+                    // 16 keys per MMA: V rows ks*16.. start 16*128 bytes further.
+                    // O_k starts every item at zero (the softmax warpgroup
+                    // clears it), so every PV MMA accumulates.
+                    if (nk == kTileKeys / 16) {
 #pragma unroll
-                        for (int ks = 1; ks < kTileKeys / 16; ++ks)
+                        for (int ks = 0; ks < kTileKeys / 16; ++ks)
                             ptx::tc_mma_ts_e<1>(to, tp + ks * 8, vl + ks * 128, hi, kIdescPV);
                     } else {
-                        for (int pass = 0; pass < (precise ? 2 : 1); ++pass)
-                            for (int ks = 0; ks < nk; ++ks) {
-                                const uint32_t pcol = precise ? ks * 16 + pass * 8 : ks * 8;  // see prefill_item
-                                ptx::tc_mma_ts_e<-1>(to, tp + pcol, vl + ks * 128, hi, kIdescPV,
-                                                      (jj > 0 || ks > 0 || pass > 0) ? 1u : 0u);
-                            }
+                        for (int ks = 0; ks < nk; ++ks) ptx::tc_mma_ts_e<1>(to, tp + ks * 8, vl + ks * 128, hi, kIdescPV);
                     }
                     ptx::tc_commit_e(&ctl->p_empty[k]);
                 }
@@ -558,6 +552,7 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii
     // lrun: fp32 probability sums (lse); rrun: sums of the bf16-rounded
     // probabilities the PV MMA consumes (output normaliser)
     float mrun0 = -INFINITY, mrun1 = -INFINITY, lrun0 = 0.f, lrun1 = 0.f, rrun0 = 0.f, rrun1 = 0.f;
+    float lqb0 = 0.f, lqb1 = 0.f;  // see the residual check below
     const int key0 = cw * 32;
     const int T = it.pad;
 
@@ -645,10 +640,47 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii
                 }
             }
             const bool tail = key0 + 32 > n;
-            // O += P V over this warp's 32 keys (two 16-key MMA steps).  Keys
-            // below 128: rows may see few keys, so the bf16 residual of P goes
-            // through a second MMA (see prefill_item).  Two instantiations
-            // keep that rare path out of the common loop.
+            // O += P V over this warp's 32 keys (two 16-key MMA steps).  Where
+            // a row's weight sits on few keys the bf16 rounding of P does not
+            // average away, so the bf16 residual p - bf16(p) goes through a
+            // second MMA: on the first tile (rows may see few keys in all) and
+            // wherever this tile's share of the error variance, sum p^2 / l^2,
+            // exceeds 1/16 for a row (as in prefill_item; l here is this
+            // warp's sum over its quarter of every tile so far, at most the
+            // row's total, so the test errs towards the second pass).  Two
+            // instantiations keep that rare path out of the common loop.
+            bool resid = kt0 < kTileKeys;
+            // The running max is exact here, so p <= 1 and a row whose sum
+            // has reached 16 cannot need the pass: lqb, a lower bound of the
+            // row's sum over this warp's keys (rescaled with it, refreshed
+            // only while below 16), spares the shuffles on most tiles.
+            lqb0 *= al0;
+            lqb1 *= al1;
+            if (!resid && __any_sync(0xffffffffu, lqb0 < 16.f || lqb1 < 16.f)) {
+                float lq0 = lrun0 + __shfl_xor_sync(0xffffffffu, lrun0, 1);
+                float lq1 = lrun1 + __shfl_xor_sync(0xffffffffu, lrun1, 1);
+                lq0 += __shfl_xor_sync(0xffffffffu, lq0, 2);
+                lq1 += __shfl_xor_sync(0xffffffffu, lq1, 2);
+                lqb0 = lq0;
+                lqb1 = lq1;
+                bool r0 = mx0 != -INFINITY && ptx::ex2(mx0 - use0) * 16.f > lq0;
+                bool r1 = mx1 != -INFINITY && ptx::ex2(mx1 - use1) * 16.f > lq1;
+                if (__any_sync(0xffffffffu, r0 || r1)) {
+                    float q0 = 0.f, q1 = 0.f;
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        q0 += s[nt][0] * s[nt][0] + s[nt][1] * s[nt][1];
+                        q1 += s[nt][2] * s[nt][2] + s[nt][3] * s[nt][3];
+                    }
+                    q0 += __shfl_xor_sync(0xffffffffu, q0, 1);
+                    q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
+                    q0 += __shfl_xor_sync(0xffffffffu, q0, 2);
+                    q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
+                    r0 = r0 && q0 * 16.f > lq0 * lq0;
+                    r1 = r1 && q1 * 16.f > lq1 * lq1;
+                }
+                resid = __any_sync(0xffffffffu, r0 || r1);
+            }
             auto pv = [&](auto precise_tag) {
                 constexpr bool kPrecise = decltype(precise_tag)::value;
 #pragma unroll
@@ -696,7 +728,7 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii
                     }
                 }
             };
-            if (kt0 < kTileKeys) pv(std::true_type{});
+            if (resid) pv(std::true_type{});
             else pv(std::false_type{});
         }
         if (!compute_sync(p, ctl, 0, cs)) return false;
@@ -896,8 +928,82 @@ __device__ void merge_warp(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
 
 // ----------------------------------------------------- prefill (compute) --
 
-// Softmax and epilogue of Q tile `k` (warpgroup k) of a prefill item.
-// Thread = tile row = TMEM lane.
+// The careful instance of a tile's exponentials, out of line so that the
+// common loop's code stays as it is: S is read back from TMEM 16 columns at a
+// time, P and its bf16 residual are written over the same columns (P of keys
+// 16ks.. in columns 16ks..16ks+7, the residual in 16ks+8..16ks+15), then one
+// 128-column read moves them to where the PV passes take them: P pairs in
+// columns 0..63, residual pairs in 64..127.  Returns (sum p, sum p^2).
+__device__ __noinline__ float2 careful_exps(uint32_t tS, int lim, float sl, float nm) {
+    float sum = 0.f, sq = 0.f;
+#pragma unroll 1
+    for (int ks = 0; ks < 8; ++ks) {
+        float v[16];
+        ptx::tmem_ld16(tS + 16 * ks, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int col = 16 * ks + 2 * i;
+            const float a = col < lim ? ptx::ex2(fmaf(v[2 * i], sl, nm)) : 0.f;
+            const float b = col + 1 < lim ? ptx::ex2(fmaf(v[2 * i + 1], sl, nm)) : 0.f;
+            sum += a + b;
+            sq = fmaf(a, a, fmaf(b, b, sq));
+            pk[i] = ptx::pack_bf16x2(a, b);
+            pk[8 + i] = ptx::pack_bf16x2(a - __uint_as_float(pk[i] << 16), b - __uint_as_float(pk[i] & 0xffff0000u));
+        }
+        ptx::tmem_st16(tS + 16 * ks, pk);
+    }
+    ptx::tmem_wait_st();
+    float r[128];
+    ptx::tmem_ld128(tS, r);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(r);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        ptx::tmem_st8(tS + 8 * ks, w + 16 * ks);
+        ptx::tmem_st8(tS + 64 + 8 * ks, w + 16 * ks + 8);
+    }
+    return make_float2(sum, sq);
+}
+
+// Second PV pass of one softmax warp (quarter q of warpgroup k) for the tile
+// in V stage st: O_k += R V over this warp's 32 rows, R = p - bf16(p) in
+// TMEM columns 64..127 of S_k (keys 2i, 2i+1 in column 64 + i), every other
+// row masked out of the MMA.  The warp issues it itself, so the MMA warp's
+// loop is the same whether or not a tile needs it, and its completion is
+// this warp's P-ready arrival (tcgen05.commit onto p_full): the MMA warp's
+// own pass over O_k for this tile starts only after it.  The pass before
+// has completed already: the S MMA of this tile, whose completion this warp
+// waited for, was issued after it.  O_k is zero before an item's first tile.
+template <int D, bool DEC>
+__device__ bool residual_pass(const AttnParams& p, uint8_t* smem, Ctl* ctl, int k, int q, int lane, int st,
+                              uint32_t ph, int n) {
+    using C = Cfg<D, DEC>;
+    constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, 0, 1);  // as the MMA warp's PV
+    if (!wait_bar(p, ctl, &ctl->v_full[st], ph, kErrTimeoutCompute)) return false;
+    if (n & (kBlock - 1)) {
+        // V rows past the valid keys may hold anything (NaN times a zero
+        // residual is NaN): zero them, as warpgroup 0 also does before its PV
+        uint8_t* vs = smem + C::kOffV + st * C::kTileBytes;
+        const int nz = ((n + 15) & ~15) - n;
+        for (int c = lane; c < nz * (D / 8); c += 32) {
+            const int r = n + c / (D / 8), cc = c % (D / 8);
+            *reinterpret_cast<uint4*>(vs + (cc >> 3) * C::kPanelBytes + r * 128 + (cc & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        ptx::fence_proxy_async_smem();
+    }
+    __syncwarp();
+    ptx::tc_fence_after();
+    const uint64_t dV = ptx::smem_desc(ptx::smem_u32(smem + C::kOffV), C::kPanelBytes, 1024, 2);
+    const uint32_t hi = (uint32_t)(dV >> 32);
+    const uint32_t vl = (uint32_t)dV + (uint32_t)((st * C::kTileBytes) >> 4);
+    const uint32_t to = ctl->tmem_base + C::kTmemO + k * D, ta = ctl->tmem_base + k * 128 + 64;
+    const uint32_t m0 = q == 0 ? 0u : ~0u, m1 = q == 1 ? 0u : ~0u, m2 = q == 2 ? 0u : ~0u, m3 = q == 3 ? 0u : ~0u;
+    const int nk = (n + 15) >> 4;
+    for (int ks = 0; ks < nk; ++ks) ptx::tc_mma_ts_masked_e(to, ta + ks * 8, vl + ks * 128, hi, kIdescPV, m0, m1, m2, m3);
+    ptx::tc_commit_e(&ctl->p_full[k]);
+    return true;
+}
+
 template <int D, bool DEC>
 __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const Item& it, const Group& g,
                              uint32_t& kv_cnt, uint32_t& sk, uint32_t& pvk, uint32_t& ok_cnt, uint32_t& cs, int k,
@@ -908,7 +1014,6 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
     const int r0 = qtile_row0(p, g, k);  // first row of query tile k
     const bool valid = ri < qtile_rows(p, g, k);
     const int prow = valid ? p.pos[r0 + ri] : -1;
-    const int pmin = p.pos[g.row0];      // the group's smallest position (the MMA warp uses the same)
     const int head = qtile_head(p, g, k);
     const uint32_t tlane = ctl->tmem_base + ((uint32_t)(quarter * 32) << 16);
     const uint32_t tS = tlane + k * 128;             // S_k, later P_k (cols 0..63) and its residual (64..127)
@@ -916,10 +1021,8 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
     const int T = it.pad;
     const float sl = p.scale_log2;
     // l: sum of the fp32 probabilities: the normaliser of the output and the
-    // lse.  P reaches the PV MMA rounded to bf16; rows with fewer than 128
-    // keys add the bf16 residual, so the MMA sees p to ~2^-17 where single
-    // roundings would not average away.
-    float m = -INFINITY, l = 0.f;
+    // lse.  P reaches the PV MMA rounded to bf16.  lg_l = log2(l).
+    float m = -INFINITY, l = 0.f, lg_l = -INFINITY;
 
     for (int j = 0; j < T; ++j) {
         const uint32_t kj = kv_cnt + j;
@@ -931,10 +1034,6 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
         ptx::tc_fence_after();
         const int2 mt = ctl->tmeta[kj & 7];
         const int kt0 = mt.x, n = mt.y;
-        // rows that see fewer than 128 keys in total: a bf16 rounding of one
-        // probability is not averaged away, so the PV MMA gets a second pass
-        // with the residual p - bf16(p)
-        const bool precise = kt0 < kTileKeys && pmin < kTileKeys;
         const int lim = max(0, min(n, prow - kt0 + 1));  // visible columns of this row
         float s[128];
         ptx::tmem_ld128(tS, s);
@@ -958,9 +1057,14 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
             mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         }
         float alpha = 1.f;
-        bool resc = false;
+        bool resc = false, careful = false;
         if (lim > 0) {
             const float ms = mx * sl;
+            // Residual check, before m moves (see below): a tile can need the
+            // second PV pass only if its largest p exceeds l_old / 4, i.e.
+            // ms + 2 > m + log2(l_old) in log2 units (always on a row's first
+            // tile, where l_old = 0).
+            careful = ms + 2.f > m + lg_l;
             // keep the running max unless the new one is larger by more than
             // 8 (log2 units): values stay <= 256, rescales of O become rare
             if (ms > m + 8.f) {
@@ -969,7 +1073,11 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
                 m = ms;
             }
         }
-        if (__any_sync(0xffffffffu, resc)) {
+        // one warp vote for both (a second only when one of them is set)
+        uint32_t vote = 0u;
+        if (__any_sync(0xffffffffu, resc || careful))
+            vote = (__any_sync(0xffffffffu, resc) ? 1u : 0u) | (__any_sync(0xffffffffu, careful) ? 2u : 0u);
+        if (vote & 1u) {
             // O_k must hold PV_k(j-1) before it is scaled
             if (!wait_bar(p, ctl, &ctl->p_empty[k], (pvk - 1) & 1, kErrTimeoutCompute)) return false;
             ptx::tc_fence_after();
@@ -985,13 +1093,31 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
             ptx::tmem_wait_st();
         }
         // Probabilities p = 2^(s*scale*log2e - m) on f32x2 pairs (masked
-        // scores are -inf and give 0), summed in two packed accumulators.
+        // scores are -inf and give 0), summed in two packed accumulators; P
+        // goes to TMEM as bf16 pairs, keys 2i and 2i+1 in column i (columns
+        // 0..63), for the MMA warp's PV pass.
+        //
+        // The bf16 rounding of p (relative error up to 2^-8) averages away
+        // over many keys of similar weight, but not where a row's weight sits
+        // on a few keys.  The PV error this tile adds to a row has a variance
+        // proportional to sum_j p_j^2 / l^2 (l: every probability so far, so
+        // that share only falls as later tiles add mass).  Where it exceeds
+        // 1/16 this warp sends the residual p - bf16(p) (columns 64..127)
+        // through a second PV pass of its own, which leaves the product with
+        // p to about 2^-16.  The residual and the squares cost instructions,
+        // so a second, careful instance of the loop computes them; it is
+        // taken only where the bound sum p^2 / (l_old + sum)^2 <= max p /
+        // (4 l_old) cannot rule the pass out.
         const uint64_t sl2 = ptx::f2pack(sl, sl);
         const float nm = m == -INFINITY ? 0.f : -m;
         const uint64_t nm2 = ptx::f2pack(nm, nm);
         uint64_t acc2[2] = {0ull, 0ull};
-        if (!precise) {
-            // P as bf16 pairs, keys 2i and 2i+1 in column i (columns 0..63)
+        float sum, sumsq = 0.f;
+        if (vote & 2u) {
+            const float2 r = careful_exps(tS, lim, sl, nm);
+            sum = r.x;
+            sumsq = r.y;
+        } else {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {  // 16-key steps
                 uint32_t pk[8];
@@ -1007,42 +1133,14 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
                 }
                 ptx::tmem_st8(tS + 8 * ks, pk);
             }
-        } else {
-            // Rows that see fewer than 128 keys (the first key tile of rows
-            // near the start of a sequence): per 16-key step, 8 columns of P
-            // followed by 8 columns of the bf16 residual p - bf16(p), for a
-            // second PV pass.  Kept out of the hot loop above: a rolled loop
-            // that re-reads the 16 score columns it then overwrites.
-#pragma unroll 1
-            for (int ks = 0; ks < 8; ++ks) {
-                float v[16];
-                ptx::tmem_ld16(tS + 16 * ks, v);
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int col = 16 * ks + 2 * i;
-                    const float s0 = col < lim ? v[2 * i] : -INFINITY;
-                    const float s1 = col + 1 < lim ? v[2 * i + 1] : -INFINITY;
-                    float a, b;
-                    ptx::f2unpack(ptx::ffma2(ptx::f2pack(s0, s1), sl2, nm2), a, b);
-                    a = ptx::ex2(a);
-                    b = ptx::ex2(b);
-                    acc2[i & 1] = ptx::fadd2(acc2[i & 1], ptx::f2pack(a, b));
-                    pk[i] = ptx::pack_bf16x2(a, b);
-                    pk[8 + i] = ptx::pack_bf16x2(a - __uint_as_float(pk[i] << 16),
-                                                 b - __uint_as_float(pk[i] & 0xffff0000u));
-                }
-                ptx::tmem_st16(tS + 16 * ks, pk);
-            }
-        }
-        float sum;
-        {
             float a0, a1, b0, b1;
             ptx::f2unpack(acc2[0], a0, a1);
             ptx::f2unpack(acc2[1], b0, b1);
             sum = (a0 + a1) + (b0 + b1);
         }
         l = l * alpha + sum;
+        lg_l = ptx::lg2(l);  // for the next tile's check (off this tile's chain)
+        const bool wresid = (vote & 2u) && __any_sync(0xffffffffu, sumsq * 16.f > l * l);
         if (k == 0 && (n & (kBlock - 1))) {
             // The tile ends inside a block: rows [n, ceil16(n)) of the V stage
             // may be pool rows past L_s holding anything.  The PV MMA covers
@@ -1059,9 +1157,17 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
             }
             ptx::fence_proxy_async_smem();
         }
+        // P ready: one arrival per warp (p_full counts the four warps), made
+        // by lane 0 once the warp's TMEM stores are done, or by the
+        // completion of the warp's residual pass
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&ctl->p_full[k]);
+        __syncwarp();
+        if (wresid) {
+            if (!residual_pass<D, DEC>(p, smem, ctl, k, quarter, lane, st, ph, n)) return false;
+        } else if (lane == 0) {
+            ptx::mbar_arrive(&ctl->p_full[k]);
+        }
         ++pvk;
     }
     kv_cnt += T;
@@ -1079,6 +1185,13 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
     for (int c = 0; c < D / 32; ++c) {
         float ov[32];
         ptx::tmem_ld32(tO + c * 32, ov);
+        {
+            // O_k starts the next item at zero (every PV MMA accumulates)
+            float z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0.f;
+            ptx::tmem_st32(tO + c * 32, z);
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) ov[i] *= inv;
         if (split) {
@@ -1104,6 +1217,7 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
             }
         }
     }
+    ptx::tmem_wait_st();
     ptx::tc_fence_before();
     ptx::mbar_arrive(&ctl->o_empty[k]);
     if (!split) {
@@ -1164,6 +1278,20 @@ __device__ void compute(const AttnParams& p, uint8_t* smem, Ctl* ctl, int warp, 
     const int wg = (warp - C::kFirstCompute) >> 2;  // softmax warpgroup 0 or 1
     const int cw = (warp - C::kFirstCompute) & 3;
     uint32_t kv_cnt = 0, sk = 0, pvk = 0, ok_cnt = 0, cs = 0, n_taken = 0, mg = 0;
+    if constexpr (!DEC) {
+        if (p.has_prefill) {
+            // O_wg starts at zero; every PV MMA accumulates (the epilogue
+            // clears it again for the next item).  The MMA warp first writes
+            // it after this warpgroup's first P-ready signal.
+            const uint32_t tO = ctl->tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + C::kTmemO + wg * D;
+            float z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) ptx::tmem_st32(tO + c * 32, z);
+            ptx::tmem_wait_st();
+        }
+    }
     for (;;) {
         const int ii = take_item(p, ctl, n_taken, kErrTimeoutCompute);
         if (ii < 0) {
@@ -1217,7 +1345,7 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
         ptx::mbar_init(&ctl->q_empty, 1);
         for (int k = 0; k < 2; ++k) {
             ptx::mbar_init(&ctl->s_full[k], 1);
-            ptx::mbar_init(&ctl->p_full[k], 128);
+            ptx::mbar_init(&ctl->p_full[k], 4);  // one arrival per softmax warp
             ptx::mbar_init(&ctl->p_empty[k], 1);
             ptx::mbar_init(&ctl->o_empty[k], 128);
             ptx::mbar_init(&ctl->csync[k], 128);

@@ -179,6 +179,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// log2(x) (approximate, -inf for x = 0).
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Per-warpgroup register budget (all 128 threads of the warpgroup execute it).
 template <int N>
 __device__ __forceinline__ void setmaxnreg_inc() {
@@ -313,6 +320,21 @@ __device__ __forceinline__ void tc_mma_ts_e(uint32_t d_tmem, uint32_t a_tmem, ui
         "mov.b64 db, {%2, %3};\n\telect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(en)
+        : "memory");
+}
+
+// As tc_mma_ts_e, always accumulating, with the output-lane mask of
+// tcgen05.mma: bit i of the 128-bit mask {m0, m1, m2, m3} (m0 bit 0 = lane 0)
+// set means that row / TMEM lane i of D is left as it is.  Rows whose A
+// operand was not written for this MMA are masked out this way.
+__device__ __forceinline__ void tc_mma_ts_masked_e(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                                   uint32_t idesc, uint32_t m0, uint32_t m1, uint32_t m2,
+                                                   uint32_t m3) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 db;\n\tsetp.ne.b32 p, %9, 0;\n\t"
+        "mov.b64 db, {%2, %3};\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, {%5, %6, %7, %8}, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(m0), "r"(m1), "r"(m2), "r"(m3), "r"(1u)
         : "memory");
 }
 

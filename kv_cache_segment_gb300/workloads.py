@@ -398,6 +398,37 @@ def restrict_rows(wl: Workload, kind: str) -> Workload:
     return dataclasses.replace(wl, q_ranges=ranges, name=f"{wl.name}/{kind}-rows")
 
 
+def with_prefill_chunk(wl: Workload, pending, c: int) -> Workload:
+    """The same pool and block tables for a serving step that runs the next
+    min(c, end - start) positions of every pending prefill (seq, start, end):
+    that sequence then holds start + n cached tokens (the chunk's own K/V is
+    appended before attention) and queries rows [start, start + n); every
+    other sequence keeps its length and rows."""
+    lens = wl.seq_lens.copy()
+    ranges = [list(r) for r in wl.q_ranges]
+    for seq, start, end in pending:
+        n = min(int(c), int(end) - int(start))
+        lens[seq] = int(start) + n
+        ranges[seq] = [(int(start), int(start) + n)]
+    return dataclasses.replace(wl, seq_lens=lens.astype(np.int32), q_ranges=ranges, name=f"{wl.name}/chunk{c}")
+
+
+def pending_prefills(wl: Workload, remaining: int = 8192):
+    """The batch with its prefill sequences taken out as pending prefills:
+    every sequence whose rows are not a lone decode row at p = L becomes a
+    pending prefill of its last min(L, remaining) positions with no rows of
+    its own; returns (batch workload, [(seq, start, end)])."""
+    ranges, pending = [], []
+    for s, rs in enumerate(wl.q_ranges):
+        L = int(wl.seq_lens[s])
+        if rs == [(L, L + 1)]:
+            ranges.append(list(rs))
+        else:
+            pending.append((s, max(0, L - remaining), L))
+            ranges.append([])
+    return dataclasses.replace(wl, q_ranges=ranges, name=f"{wl.name}/pending"), pending
+
+
 # ------------------------------------------------------------------ values --
 
 def make_values(wl: Workload, device="cpu", seed: Optional[int] = None, dtype=None):

@@ -322,3 +322,69 @@ def test_chunk_choice_rejects_bad_pending(bad):
         msa.msa_choose_prefill_chunk(dims, wl.block_table, wl.seq_lens, indptr, ranges, pending, PARAMS,
                                      num_sms=152)
     assert e.value.status == want
+
+
+# ----------------------------------------------- split chooser, by hand --
+
+def _equal_decode_batch(n_seqs, length):
+    """n_seqs sequences of `length` tokens in one segment each, one decode
+    row per sequence, 32/8 heads, D = 128: 8 * n_seqs decode groups."""
+    return W.custom([length] * n_seqs, [[length // 16]] * n_seqs, [[(length, length + 1)]] * n_seqs,
+                    hq=32, hkv=8, seed=5)
+
+
+TILE_US_AT_50 = 128 * 128 * 2 * 2 / 50e3  # one 128-key K+V tile (D = 128) at 50 GB/s: 1.31072 us
+
+
+def test_split_chooser_by_hand_one_group_per_cta():
+    """152 groups of 64 tiles on 152 CTAs: factor 1 gives each CTA one whole
+    group, T = launch + item + 64 tiles = 5 + 2 + 83.886 = 90.886 us; any
+    larger factor cuts each group in two or more parts, which adds items and
+    merges on every CTA (factor 1.5 or 2: 5 + 2 x (2 + 2) + 83.886), so the
+    chooser keeps factor 1."""
+    p = dict(launch_us=5.0, dec_item_us=2.0, dec_gbs=1e7, dec_cta_gbs=50.0, pre_item_us=5.0, pre_tile_us=1.0,
+             box_us=0.0, dec_merge_us=2.0, pre_merge_us=20.0)
+    wl = _equal_decode_batch(19, 8192)
+    plan = msa.msa_plan_create_ex(*_args(wl), num_sms=152, choose_with=p)
+    try:
+        info = msa.msa_plan_get_info(plan)
+        assert (info["decode_split"], info["num_items"]) == (1.0, 152)
+        assert msa.msa_plan_estimate(plan, p)["time_us"] == pytest.approx(5.0 + 2.0 + 64 * TILE_US_AT_50, rel=1e-12)
+    finally:
+        msa.msa_plan_destroy(plan)
+    plan = msa.msa_plan_create_ex(*_args(wl), num_sms=152, decode_split=2.0, prefill_split=4.0)
+    try:
+        assert msa.msa_plan_estimate(plan, p)["time_us"] == pytest.approx(5.0 + 2 * 4.0 + 64 * TILE_US_AT_50,
+                                                                          rel=1e-12)
+    finally:
+        msa.msa_plan_destroy(plan)
+
+
+def test_split_chooser_by_hand_finer_parts_fill_the_rounds():
+    """16 groups of 512 tiles on 152 CTAs, free items and merges, every CTA
+    streaming at 50 GB/s.  The work per CTA is 16 x (512 x 1.1 + 0.5) / 152
+    = 59.33 tile costs.  Factor 1: parts of ceil(59.33 / 1.1) = 54 tiles give
+    10 parts a group (9 of 52, one of 44 once the range is cut evenly), 160
+    items: the 8 left over run after the 44-tile ones, makespan 88 tiles.
+    Factor 1.5 gives 15 parts a group, 240 items (makespan 35 + 35 = 70 tiles
+    plus the uneven tail the model replays).  Factor 2: parts of
+    ceil(29.67 / 1.1) = 27 tiles, 19 a group (18 of 27, one of 26), 304
+    items = two full rounds of 152, makespan 54 tiles = 70.78 us + 5 us
+    launch: the least, so the chooser takes 2 (3 ties it; the first minimum
+    stands)."""
+    p = dict(launch_us=5.0, dec_item_us=0.0, dec_gbs=1e7, dec_cta_gbs=50.0, pre_item_us=5.0, pre_tile_us=1.0,
+             box_us=0.0, dec_merge_us=0.0, pre_merge_us=20.0)
+    wl = _equal_decode_batch(2, 65536)
+    plan = msa.msa_plan_create_ex(*_args(wl), num_sms=152, choose_with=p)
+    try:
+        info = msa.msa_plan_get_info(plan)
+        assert (info["decode_split"], info["num_items"]) == (2.0, 304)
+        assert msa.msa_plan_estimate(plan, p)["time_us"] == pytest.approx(5.0 + 54 * TILE_US_AT_50, rel=1e-12)
+    finally:
+        msa.msa_plan_destroy(plan)
+    plan = msa.msa_plan_create_ex(*_args(wl), num_sms=152, decode_split=1.0, prefill_split=4.0)
+    try:
+        assert msa.msa_plan_get_info(plan)["num_items"] == 160
+        assert msa.msa_plan_estimate(plan, p)["time_us"] == pytest.approx(5.0 + 88 * TILE_US_AT_50, rel=1e-12)
+    finally:
+        msa.msa_plan_destroy(plan)

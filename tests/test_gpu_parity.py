@@ -308,16 +308,49 @@ def test_running_max_moves(shape):
     out, lse, _ = run_gpu(wl, k, v, q)
     ro, rl = oracle_ref(wl, k, v, q)
     assert np.nanmax(rl) > 20.0  # the scores really are large
-    extra = None
-    if shape == "spikes":
-        # A row whose weight sits on two or three outlier keys (p = 0.6 / 0.4)
-        # sees the bf16 rounding of P un-averaged: the PV product then
-        # carries up to 2^-8 * sum_j p_j |V_j,d| (bf16 unit roundoff; the
-        # residual pass only covers rows with fewer than 128 keys).  The
-        # oracle gives that sum exactly: the same softmax applied to |V|.
-        wabs, _ = oracle_ref(wl, k, v.abs(), q)
-        extra = 2.0 ** -8 * wabs
-    compare(out, lse, ro, rl, shape, extra=extra)
+    compare(out, lse, ro, rl, shape)
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("opts", [dict(), dict(decode_split=12.0, prefill_split=16.0)])
+def test_attention_sink_with_a_rival_key(d, opts):
+    """Rows whose weight sits on two keys among more than a thousand: key 0
+    of every sequence (an attention sink) takes most of the softmax mass and
+    one rival key far into the sequence most of the rest (weights about
+    0.64 and 0.36), with V of the rival -1.8 times the sink's, so the two
+    products nearly cancel and the stated tolerance is almost all absolute.
+    A single bf16 rounding of P is then not averaged away by the other keys;
+    the output must still meet the stated tolerance with no allowance, for
+    prefill rows before and after the rival, decode rows, and with the key
+    range split into parts merged by log-sum-exp."""
+    # sequences 0-1: prefill rows before and after the rival (and a decode
+    # row in a prefill tile); 2-3: rows short enough for the GQA-packed
+    # decode path (a lone decode row; three trailing rows)
+    lens = [1500, 2100, 1800, 1301]
+    wl = W.custom(lens, [[30, 40, 24], [50, 32, 30, 20], [40, 33, 40], [20, 21, 41]],
+                  [[(0, 40), (560, 900), (1490, 1501)], [(1200, 1450), (2100, 2101)], [(1800, 1801)],
+                   [(1298, 1301)]],
+                  hq=8, hkv=2, d=d, seed=71)
+    k, v, q = W.make_values(wl)
+    q = q.float().abs().to(torch.bfloat16)  # positive q: a positive key gives a large score
+    k = k.float()
+    v = v.float()
+    base = 0
+    # scores ~ amp * 0.8 * sqrt(D); the rival sits 0.6 (natural log) below the sink
+    amp = 14.0 / (0.8 * d ** 0.5)
+    for s, L in enumerate(lens):
+        rival = base + 600 + 37 * s
+        k[base] = amp + 0.02 * k[base]
+        k[rival] = amp - 0.6 / (0.8 * d ** 0.5) + 0.02 * k[rival]
+        v[base] = 2.0 * v[base]
+        v[rival] = -1.8 * v[base]
+        base += L
+    k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    out, lse, info = run_gpu(wl, k, v, q, **opts)
+    assert info["num_prefill_items"] > 0 and info["num_decode_items"] > 0
+    ro, rl = oracle_ref(wl, k, v, q)
+    assert np.nanmax(rl) > 10.0  # the sink does dominate
+    compare(out, lse, ro, rl, f"sink D={d} {opts}")
 
 
 @pytest.mark.parametrize("seed", range(48))
@@ -567,10 +600,42 @@ def test_bounded_wait_runs_out_and_the_context_survives():
     compare(out, lse, ro, rl, "after a timed-out wait")
 
 
+@pytest.mark.parametrize("idx", [5, 3])
+def test_device_check_clears_counters_left_by_an_aborted_launch(idx):
+    """A launch that gave up can leave the merge counters of split groups (and
+    the queue head) mid-count.  Stand in for one from the host: put nonzero
+    counts there and set an error bit.  msa_plan_check_device reports the
+    error and zeroes the counters with the word, so the next launch with the
+    plan (split groups merged by the last part to arrive) is exact."""
+    wl = W.small_config(idx)
+    k, v, q = W.make_values(wl)
+    dev = torch.device("cuda")
+    kp, vp = W.make_pool(wl, k.to(dev), v.to(dev))
+    sess = MsaSession.from_workload(wl, decode_split=12.0, prefill_split=16.0)
+    try:
+        info = sess.info
+        a, nb = info["counters_offset"], info["counters_bytes"]
+        assert nb > 0 and info["num_items"] > info["num_groups"]  # some groups are split
+        sess.workspace[a:a + nb].fill_(1)            # every counter at 0x01010101
+        sess.workspace[0:4].view(torch.int32).fill_(msa.MSA_DEVERR_TIMEOUT_COMPUTE)
+        rc, word = sess.check_device()
+        assert rc == msa.MSA_ERR_DEVICE_CHECK and word == msa.MSA_DEVERR_TIMEOUT_COMPUTE
+        assert int(sess.workspace[a:a + nb].count_nonzero()) == 0
+        assert int(sess.workspace[0:4].count_nonzero()) == 0
+        lse = torch.empty((wl.num_q_rows, wl.num_q_heads), dtype=torch.float32, device=dev)
+        out = sess.attention(q.to(dev), kp, vp, lse=lse)
+        assert sess.check_device() == (0, 0)
+        ro, rl = oracle_ref(wl, k, v, q)
+        compare(out, lse, ro, rl, "after the counters were cleared")
+    finally:
+        sess.close()
+
+
 @pytest.mark.parametrize("name", ["decode", "holes", "mixed", "long"])
 def test_latency_model_predicts_measured_launches(name):
     """The shipped latency-model constants predict the measured launch time
-    of medium workloads it was not fitted on within 25 %."""
+    (back to back, as costfit measures and the bench times) of medium
+    workloads it was not fitted on within 10 %."""
     from kv_cache_segment_gb300 import costfit
     params = costfit.load_params()
     if params is None:
@@ -585,4 +650,4 @@ def test_latency_model_predicts_measured_launches(name):
         pred = msa.msa_plan_estimate(sess.plan, params)["time_us"]
     finally:
         sess.close()
-    assert abs(pred / us - 1.0) < 0.25, (name, pred, us)
+    assert abs(pred / us - 1.0) < 0.10, (name, pred, us)
