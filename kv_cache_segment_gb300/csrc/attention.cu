@@ -549,8 +549,8 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii
     float o[NT][4];
 #pragma unroll
     for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    // lrun: fp32 probability sums (lse); rrun: sums of the bf16-rounded
-    // probabilities the PV MMA consumes (output normaliser)
+    // lrun: fp32 probability sums (lse); rrun: sums of the bf16 values the PV
+    // MMAs consume, P and its residual (output normaliser)
     float mrun0 = -INFINITY, mrun1 = -INFINITY, lrun0 = 0.f, lrun1 = 0.f, rrun0 = 0.f, rrun1 = 0.f;
     float lqb0 = 0.f, lqb1 = 0.f;  // see the residual check below
     const int key0 = cw * 32;
@@ -643,13 +643,19 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii
             // O += P V over this warp's 32 keys (two 16-key MMA steps).  Where
             // a row's weight sits on few keys the bf16 rounding of P does not
             // average away, so the bf16 residual p - bf16(p) goes through a
-            // second MMA: on the first tile (rows may see few keys in all) and
-            // wherever this tile's share of the error variance, sum p^2 / l^2,
-            // exceeds 1/16 for a row (as in prefill_item; l here is this
-            // warp's sum over its quarter of every tile so far, at most the
-            // row's total, so the test errs towards the second pass).  Two
-            // instantiations keep that rare path out of the common loop.
-            bool resid = kt0 < kTileKeys;
+            // second MMA.  In the decode-only launch every tile takes it: a
+            // decode tile has MMA time to spare at D = 128, and at D = 64
+            // (compute close to the tile's HBM time) a per-tile test of
+            // whether a row needs it cost more than the MMA it saves.  In the
+            // launch with prefill items, where the extra MMAs slow the whole
+            // kernel, a tile takes it on a sequence's first 128 keys (rows may
+            // see few keys in all) and wherever this tile's share of the
+            // error variance, sum p^2 / l^2, exceeds 1/16 for a row (as in
+            // prefill_item; l here is this warp's sum over its quarter of
+            // every tile so far, at most the row's total, so the test errs
+            // towards the second pass).  Two instantiations keep the rare
+            // path out of the common loop.
+            bool resid = DEC || kt0 < kTileKeys;
             // The running max is exact here, so p <= 1 and a row whose sum
             // has reached 16 cannot need the pass: lqb, a lower bound of the
             // row's sum over this warp's keys (rescaled with it, refreshed

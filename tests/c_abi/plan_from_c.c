@@ -42,6 +42,30 @@ int main(void) {
     int32_t evicted[1] = {-1};
     double cost[3];
     CHECK(msa_select_evictions(&dims, 40, hit, MSA_EVICT_LINEAR, 1.0, 0.0, &prm, 1, evicted, cost));
+    /* prefix reading: a block costs its own rows and every row after it */
+    int32_t evicted_prefix[1] = {-1};
+    double cost_prefix[3];
+    CHECK(msa_select_evictions(&dims, 40, hit, MSA_EVICT_LINEAR | MSA_EVICT_PREFIX_COST, 0.0, 1.0, &prm, 1,
+                               evicted_prefix, cost_prefix));
+    /* chunk size for a step of one decode row (seq 0, 40 tokens) and a
+     * pending prefill of positions [0, 300) of seq 1 (19 blocks mapped) */
+    static int32_t table2[2][19];
+    for (int b = 0; b < 19; ++b) {
+        table2[0][b] = b < 3 ? b : -1;
+        table2[1][b] = 32 + b;
+    }
+    const int32_t lens2[2] = {40, 0};
+    const int32_t indptr2[3] = {0, 1, 1};
+    const int32_t ranges2[1][2] = {{39, 40}};
+    const msa_pending_prefill pend = {1, 0, 300};
+    const msa_plan_options opts = {152, 0.0, 0.0, NULL};
+    msa_chunk_choice ch, ch_tight;
+    int32_t cand[64];
+    double cand_us[64];
+    CHECK(msa_choose_prefill_chunk(&dims, 2, 19, &table2[0][0], lens2, indptr2, &ranges2[0][0], &pend, 1, &opts,
+                                   &prm, 0.0, 0, 0, &ch, cand, cand_us));
+    CHECK(msa_choose_prefill_chunk(&dims, 2, 19, &table2[0][0], lens2, indptr2, &ranges2[0][0], &pend, 1, &opts,
+                                   &prm, 0.5 * cand_us[0], 0, 0, &ch_tight, NULL, NULL));
     /* an attention call before any upload is refused before any device work */
     const int not_up = msa_attention((const void*)0x1000, (const void*)0x1000, (const void*)0x1000, 64, plan,
                                      (void*)0x1000, MSA_OUT_BF16, NULL, NULL);
@@ -51,5 +75,12 @@ int main(void) {
            info.num_q_rows, n_runs, runs[0], runs[1], runs[2], runs[3], runs[4], runs[5], n_items, ws > 0,
            (long long)est.n_items, evicted[0], cost[1] > cost[0], msa_status_string(not_up), cost[0], cost[1],
            cost[2]);
+    printf("evict_prefix %d cost_prefix %.17g %.17g %.17g\n", evicted_prefix[0], cost_prefix[0], cost_prefix[1],
+           cost_prefix[2]);
+    printf("chunk %d tokens %d within %d ncand %d time %.17g upt %.17g tight_chunk %d tight_within %d cands",
+           ch.chunk, ch.tokens, ch.within_budget, ch.n_candidates, ch.time_us, ch.us_per_token, ch_tight.chunk,
+           ch_tight.within_budget);
+    for (int i = 0; i < ch.n_candidates; ++i) printf(" %d %.17g", cand[i], cand_us[i]);
+    printf("\n");
     return 0;
 }

@@ -22,7 +22,8 @@ def test_plain_c_caller(tmp_path):
                            "-Wl,-rpath," + libdir])
     out = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert out.returncode == 0, out.stderr
-    got = out.stdout.split()
+    lines = out.stdout.splitlines()
+    got = lines[0].split()
     vals = dict(zip(got[0::2], got[1::2]))
     # 11 prefill rows + 1 decode row; seq 0 = runs (block 0, phys 10, 2 blocks) and (block 2, phys 17, 1 block)
     assert vals["rows"] == "12" and vals["runs"] == "2"
@@ -36,3 +37,26 @@ def test_plain_c_caller(tmp_path):
     cost = [float(x) for x in got[got.index("cost") + 1:got.index("cost") + 4]]
     for c, keys in zip(cost, (sum(range(1, 17)), sum(range(17, 33)), sum(range(33, 41)))):
         assert c == pytest.approx(1.0 * 8 * keys / 16384, rel=1e-15)
+
+    # prefix reading: each block's cost is its own hole cost plus every later one
+    # (a suffix sum), so it falls with position; scored on cost alone (alpha 0,
+    # beta 1) the block evicted is the last one
+    pre = lines[1].split()
+    cost_prefix = [float(x) for x in pre[pre.index("cost_prefix") + 1:pre.index("cost_prefix") + 4]]
+    for b in range(3):
+        assert cost_prefix[b] == pytest.approx(sum(cost[b:]), rel=1e-12)
+    assert pre[pre.index("evict_prefix") + 1] == "2"
+    # chunk chooser: candidates 128, 256 and the whole remainder 300; the choice
+    # has the least predicted time per prefill token; a budget below every
+    # candidate's time returns the smallest candidate, flagged outside the budget
+    ch = lines[2].split()
+    cv = dict(zip(ch[0:16:2], ch[1:16:2]))
+    rest = ch[ch.index("cands") + 1:]
+    cands = [int(x) for x in rest[0::2]]
+    times = [float(x) for x in rest[1::2]]
+    assert cands == [128, 256, 300] and cv["ncand"] == "3"
+    per_tok = [t / c for c, t in zip(cands, times)]
+    best = min(range(3), key=lambda i: (per_tok[i], -cands[i]))
+    assert int(cv["chunk"]) == cands[best] and int(cv["tokens"]) == cands[best] and cv["within"] == "1"
+    assert float(cv["time"]) == times[best] and float(cv["upt"]) == pytest.approx(per_tok[best], rel=1e-15)
+    assert cv["tight_chunk"] == "128" and cv["tight_within"] == "0"

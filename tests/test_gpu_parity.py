@@ -631,6 +631,31 @@ def test_device_check_clears_counters_left_by_an_aborted_launch(idx):
         sess.close()
 
 
+@pytest.mark.parametrize("budget", [0.0, 31.0])
+def test_chosen_prefill_chunk_step_matches_oracle(budget):
+    """A serving step as msa_choose_prefill_chunk plans it: the small mixed
+    batch's decode rows plus the chosen chunk of each pending prefill (the
+    chunk's own K/V in the cache, rows [start, start + c)), run through the
+    C ABI and compared with the oracle on the same step."""
+    from kv_cache_segment_gb300 import costfit
+    params = costfit.load_params()
+    if params is None:
+        pytest.skip("no fitted latency-model constants")
+    wl = W.small_config(5)
+    base, pending = W.pending_prefills(wl, remaining=500)
+    dims = msa.make_dims(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, 16, wl.scale)
+    choice, cands, _ = msa.msa_choose_prefill_chunk(dims, base.block_table, base.seq_lens, base.q_range_indptr,
+                                                    base.q_ranges_flat, pending, params, budget_us=budget,
+                                                    granularity=64)
+    assert choice["chunk"] in cands.tolist()
+    step = W.with_prefill_chunk(base, pending, choice["chunk"])
+    assert step.num_q_rows == sum(1 for rs in base.q_ranges for _ in rs) + choice["tokens"]
+    k, v, q = W.make_values(step)
+    out, lse, info = run_gpu(step, k, v, q)
+    ro, rl = oracle_ref(step, k, v, q)
+    compare(out, lse, ro, rl, f"chosen chunk {choice['chunk']}")
+
+
 @pytest.mark.parametrize("name", ["decode", "holes", "mixed", "long"])
 def test_latency_model_predicts_measured_launches(name):
     """The shipped latency-model constants predict the measured launch time
