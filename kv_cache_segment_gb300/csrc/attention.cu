@@ -490,7 +490,7 @@ __device__ __forceinline__ void store_out(const AttnParams& p, int64_t idx, floa
 
 // ------------------------------------------------------ decode (compute) --
 
-template <int D, bool DEC>
+template <int D, bool DEC, bool kHalf>
 __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii, const Item& it, const Group& g,
                             uint32_t& kv_cnt, uint32_t& cs, uint32_t& mg, int cw, int lane) {
     using C = Cfg<D, DEC>;
@@ -556,6 +556,12 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii
     const int key0 = cw * 32;
     const int T = it.pad;
 
+    // A group of at most 8 live rows (M <= 8: one decode row per sequence
+    // with G <= 8, or G = 1 with up to 8 rows) leaves the MMA's rows 8..15 as
+    // padding.  There ("half" tiles) the padding rows carry the bf16 residual
+    // p - bf16(p) of rows 0..7 through the same PV MMAs, so every tile gets
+    // the exact product at no MMA cost, the padding rows' exponentials are
+    // skipped, and rows 8..15 of O are folded into rows 0..7 at the end.
     for (int t = 0; t < T; ++t) {
         const uint32_t k = kv_cnt + t;
         const int st = k % C::kStages;
@@ -581,9 +587,11 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii
                     }
                 } else {
                     const int c0 = 4 * kk + (lane >> 4);  // chunk of k-step 2kk
-                    ptx::ldmatrix_x4(qsa + qrow * (D * 2) + ((c0 ^ (qrow & 7)) << 4), qa0[0], qa0[1], qa0[2], qa0[3]);
-                    const int c1 = c0 + 2;                 // k-step 2kk+1
-                    ptx::ldmatrix_x4(qsa + qrow * (D * 2) + ((c1 ^ (qrow & 7)) << 4), qa1[0], qa1[1], qa1[2], qa1[3]);
+                    ptx::ldmatrix_x4(qsa + qrow * (D * 2) + ((c0 ^ (qrow & 7)) << 4), qa0[0], qa0[1], qa0[2],
+                                     qa0[3]);
+                    const int c1 = c0 + 2;  // k-step 2kk+1
+                    ptx::ldmatrix_x4(qsa + qrow * (D * 2) + ((c1 ^ (qrow & 7)) << 4), qa1[0], qa1[1], qa1[2],
+                                     qa1[3]);
                 }
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
@@ -599,7 +607,7 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
+                for (int e = 0; e < (kHalf ? 2 : 4); ++e) {
                     const int key = key0 + nt * 8 + 2 * tq + (e & 1);
                     const int prow = (e >> 1) ? prow1 : prow0;
                     const bool vis = key < n && kt0 + key <= prow;
@@ -610,28 +618,34 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii
             }
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            if constexpr (!kHalf) {
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            }
             const float mn0 = fmaxf(mrun0, mx0), mn1 = fmaxf(mrun1, mx1);
             const float use0 = mn0 == -INFINITY ? 0.f : mn0;
             const float use1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float al0 = ptx::ex2(mrun0 - use0), al1 = ptx::ex2(mrun1 - use1);
+            const float al0 = ptx::ex2(mrun0 - use0), al1 = kHalf ? al0 : ptx::ex2(mrun1 - use1);
             mrun0 = mn0;
-            mrun1 = mn1;
             float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 s[nt][0] = ptx::ex2(s[nt][0] - use0);
                 s[nt][1] = ptx::ex2(s[nt][1] - use0);
-                s[nt][2] = ptx::ex2(s[nt][2] - use1);
-                s[nt][3] = ptx::ex2(s[nt][3] - use1);
                 sum0 += s[nt][0] + s[nt][1];
-                sum1 += s[nt][2] + s[nt][3];
+                if constexpr (!kHalf) {
+                    s[nt][2] = ptx::ex2(s[nt][2] - use1);
+                    s[nt][3] = ptx::ex2(s[nt][3] - use1);
+                    sum1 += s[nt][2] + s[nt][3];
+                }
             }
             lrun0 = lrun0 * al0 + sum0;
-            lrun1 = lrun1 * al1 + sum1;
             rrun0 *= al0;
-            rrun1 *= al1;
+            if constexpr (!kHalf) {
+                mrun1 = mn1;
+                lrun1 = lrun1 * al1 + sum1;
+                rrun1 *= al1;
+            }
             if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
                 for (int i = 0; i < NT; ++i) {
@@ -642,74 +656,85 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii
             const bool tail = key0 + 32 > n;
             // O += P V over this warp's 32 keys (two 16-key MMA steps).  Where
             // a row's weight sits on few keys the bf16 rounding of P does not
-            // average away, so the bf16 residual p - bf16(p) goes through a
-            // second MMA.  In the decode-only launch every tile takes it: a
-            // decode tile has MMA time to spare at D = 128, and at D = 64
-            // (compute close to the tile's HBM time) a per-tile test of
-            // whether a row needs it cost more than the MMA it saves.  In the
-            // launch with prefill items, where the extra MMAs slow the whole
-            // kernel, a tile takes it on a sequence's first 128 keys (rows may
-            // see few keys in all) and wherever this tile's share of the
-            // error variance, sum p^2 / l^2, exceeds 1/16 for a row (as in
-            // prefill_item; l here is this warp's sum over its quarter of
-            // every tile so far, at most the row's total, so the test errs
-            // towards the second pass).  Two instantiations keep the rare
-            // path out of the common loop.
+            // average away, so the bf16 residual p - bf16(p) goes through the
+            // MMA too: in half tiles as rows 8..15 of the same MMA, otherwise
+            // as a second MMA.  In the decode-only launch every full tile
+            // takes the second MMA (a decode tile has MMA time to spare).  In
+            // the launch with prefill items, where extra MMAs slow the whole
+            // kernel, a full tile takes it on a sequence's first 128 keys
+            // (rows may see few keys in all) and wherever this tile's share
+            // of the error variance, sum p^2 / l^2, exceeds 1/16 for a row
+            // (as in prefill_item; l here is this warp's sum over its quarter
+            // of every tile so far, at most the row's total, so the test errs
+            // towards the second MMA).  Two instantiations keep the rare path
+            // out of the common loop.
             bool resid = DEC || kt0 < kTileKeys;
-            // The running max is exact here, so p <= 1 and a row whose sum
-            // has reached 16 cannot need the pass: lqb, a lower bound of the
-            // row's sum over this warp's keys (rescaled with it, refreshed
-            // only while below 16), spares the shuffles on most tiles.
-            lqb0 *= al0;
-            lqb1 *= al1;
-            if (!resid && __any_sync(0xffffffffu, lqb0 < 16.f || lqb1 < 16.f)) {
-                float lq0 = lrun0 + __shfl_xor_sync(0xffffffffu, lrun0, 1);
-                float lq1 = lrun1 + __shfl_xor_sync(0xffffffffu, lrun1, 1);
-                lq0 += __shfl_xor_sync(0xffffffffu, lq0, 2);
-                lq1 += __shfl_xor_sync(0xffffffffu, lq1, 2);
-                lqb0 = lq0;
-                lqb1 = lq1;
-                bool r0 = mx0 != -INFINITY && ptx::ex2(mx0 - use0) * 16.f > lq0;
-                bool r1 = mx1 != -INFINITY && ptx::ex2(mx1 - use1) * 16.f > lq1;
-                if (__any_sync(0xffffffffu, r0 || r1)) {
-                    float q0 = 0.f, q1 = 0.f;
+            if constexpr (!kHalf) {
+                // The running max is exact here, so p <= 1 and a row whose
+                // sum has reached 16 cannot need the pass: lqb, a lower bound
+                // of the row's sum over this warp's keys (rescaled with it,
+                // refreshed only while below 16), spares the shuffles on most
+                // tiles.
+                lqb0 *= al0;
+                lqb1 *= al1;
+                if (!resid && __any_sync(0xffffffffu, lqb0 < 16.f || lqb1 < 16.f)) {
+                    float lq0 = lrun0 + __shfl_xor_sync(0xffffffffu, lrun0, 1);
+                    float lq1 = lrun1 + __shfl_xor_sync(0xffffffffu, lrun1, 1);
+                    lq0 += __shfl_xor_sync(0xffffffffu, lq0, 2);
+                    lq1 += __shfl_xor_sync(0xffffffffu, lq1, 2);
+                    lqb0 = lq0;
+                    lqb1 = lq1;
+                    bool r0 = mx0 != -INFINITY && ptx::ex2(mx0 - use0) * 16.f > lq0;
+                    bool r1 = mx1 != -INFINITY && ptx::ex2(mx1 - use1) * 16.f > lq1;
+                    if (__any_sync(0xffffffffu, r0 || r1)) {
+                        float q0 = 0.f, q1 = 0.f;
 #pragma unroll
-                    for (int nt = 0; nt < 4; ++nt) {
-                        q0 += s[nt][0] * s[nt][0] + s[nt][1] * s[nt][1];
-                        q1 += s[nt][2] * s[nt][2] + s[nt][3] * s[nt][3];
+                        for (int nt = 0; nt < 4; ++nt) {
+                            q0 += s[nt][0] * s[nt][0] + s[nt][1] * s[nt][1];
+                            q1 += s[nt][2] * s[nt][2] + s[nt][3] * s[nt][3];
+                        }
+                        q0 += __shfl_xor_sync(0xffffffffu, q0, 1);
+                        q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
+                        q0 += __shfl_xor_sync(0xffffffffu, q0, 2);
+                        q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
+                        r0 = r0 && q0 * 16.f > lq0 * lq0;
+                        r1 = r1 && q1 * 16.f > lq1 * lq1;
                     }
-                    q0 += __shfl_xor_sync(0xffffffffu, q0, 1);
-                    q1 += __shfl_xor_sync(0xffffffffu, q1, 1);
-                    q0 += __shfl_xor_sync(0xffffffffu, q0, 2);
-                    q1 += __shfl_xor_sync(0xffffffffu, q1, 2);
-                    r0 = r0 && q0 * 16.f > lq0 * lq0;
-                    r1 = r1 && q1 * 16.f > lq1 * lq1;
+                    resid = __any_sync(0xffffffffu, r0 || r1);
                 }
-                resid = __any_sync(0xffffffffu, r0 || r1);
             }
+            // bf16 residual of the pair (x, y) given its bf16 pack w
+            auto lo_of = [](float x, float y, uint32_t w) {
+                return ptx::pack_bf16x2(x - __uint_as_float(w << 16), y - __uint_as_float(w & 0xffff0000u));
+            };
             auto pv = [&](auto precise_tag) {
-                constexpr bool kPrecise = decltype(precise_tag)::value;
+                constexpr bool kPrecise = decltype(precise_tag)::value && !kHalf;
 #pragma unroll
                 for (int kst = 0; kst < 2; ++kst) {
                     uint32_t a[4];
                     a[0] = ptx::pack_bf16x2(s[2 * kst][0], s[2 * kst][1]);
-                    a[1] = ptx::pack_bf16x2(s[2 * kst][2], s[2 * kst][3]);
                     a[2] = ptx::pack_bf16x2(s[2 * kst + 1][0], s[2 * kst + 1][1]);
-                    a[3] = ptx::pack_bf16x2(s[2 * kst + 1][2], s[2 * kst + 1][3]);
+                    if constexpr (kHalf) {
+                        a[1] = lo_of(s[2 * kst][0], s[2 * kst][1], a[0]);
+                        a[3] = lo_of(s[2 * kst + 1][0], s[2 * kst + 1][1], a[2]);
+                    } else {
+                        a[1] = ptx::pack_bf16x2(s[2 * kst][2], s[2 * kst][3]);
+                        a[3] = ptx::pack_bf16x2(s[2 * kst + 1][2], s[2 * kst + 1][3]);
+                    }
                     const int kbase = key0 + kst * 16;
                     if (kbase >= n) break;
-                    rrun0 += bf16x2_sum(a[0]) + bf16x2_sum(a[2]);
-                    rrun1 += bf16x2_sum(a[1]) + bf16x2_sum(a[3]);
+                    if constexpr (kHalf) {
+                        rrun0 += (bf16x2_sum(a[0]) + bf16x2_sum(a[2])) + (bf16x2_sum(a[1]) + bf16x2_sum(a[3]));
+                    } else {
+                        rrun0 += bf16x2_sum(a[0]) + bf16x2_sum(a[2]);
+                        rrun1 += bf16x2_sum(a[1]) + bf16x2_sum(a[3]);
+                    }
                     uint32_t alo[4] = {0u, 0u, 0u, 0u};
                     if constexpr (kPrecise) {
-                        alo[0] = ptx::pack_bf16x2(s[2 * kst][0] - __uint_as_float(a[0] << 16),
-                                                  s[2 * kst][1] - __uint_as_float(a[0] & 0xffff0000u));
-                        alo[1] = ptx::pack_bf16x2(s[2 * kst][2] - __uint_as_float(a[1] << 16),
-                                                  s[2 * kst][3] - __uint_as_float(a[1] & 0xffff0000u));
-                        alo[2] = ptx::pack_bf16x2(s[2 * kst + 1][0] - __uint_as_float(a[2] << 16),
-                                                  s[2 * kst + 1][1] - __uint_as_float(a[2] & 0xffff0000u));
-                        alo[3] = ptx::pack_bf16x2(s[2 * kst + 1][2] - __uint_as_float(a[3] << 16),
-                                                  s[2 * kst + 1][3] - __uint_as_float(a[3] & 0xffff0000u));
+                        alo[0] = lo_of(s[2 * kst][0], s[2 * kst][1], a[0]);
+                        alo[1] = lo_of(s[2 * kst][2], s[2 * kst][3], a[1]);
+                        alo[2] = lo_of(s[2 * kst + 1][0], s[2 * kst + 1][1], a[2]);
+                        alo[3] = lo_of(s[2 * kst + 1][2], s[2 * kst + 1][3], a[3]);
                         rrun0 += bf16x2_sum(alo[0]) + bf16x2_sum(alo[2]);
                         rrun1 += bf16x2_sum(alo[1]) + bf16x2_sum(alo[3]);
                     }
@@ -734,13 +759,22 @@ __device__ bool decode_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, int ii
                     }
                 }
             };
-            if (resid) pv(std::true_type{});
-            else pv(std::false_type{});
+            if (kHalf || !resid) pv(std::false_type{});
+            else pv(std::true_type{});
         }
         if (!compute_sync(p, ctl, 0, cs)) return false;
         if (cw == 0 && lane == 0) {
             ptx::mbar_arrive(&ctl->k_empty[st]);
             ptx::mbar_arrive(&ctl->v_empty[st]);
+        }
+    }
+    if constexpr (kHalf) {
+        // rows 8..15 hold (p - bf16(p)) V of rows 0..7
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+            o[i][0] += o[i][2];
+            o[i][1] += o[i][3];
+            o[i][2] = o[i][3] = 0.f;
         }
     }
     kv_cnt += T;
@@ -1313,7 +1347,15 @@ __device__ void compute(const AttnParams& p, uint8_t* smem, Ctl* ctl, int warp, 
         bool ok = true;
         if (DEC || it.kind == kDecode) {
             // decode items run on warpgroup 0; warpgroup 1 only keeps count
-            if (wg == 0) ok = decode_item<D, DEC>(p, smem, ctl, ii, it, g, kv_cnt, cs, mg, cw, lane);
+            if (wg == 0) {
+                // half tiles (at most 8 live rows) in the decode-only kernel;
+                // the kernel with prefill items has no registers to spare for
+                // a second copy of the decode loop
+                if (DEC && g.nrows * p.G <= 8)
+                    ok = decode_item<D, DEC, DEC>(p, smem, ctl, ii, it, g, kv_cnt, cs, mg, cw, lane);
+                else
+                    ok = decode_item<D, DEC, false>(p, smem, ctl, ii, it, g, kv_cnt, cs, mg, cw, lane);
+            }
             else kv_cnt += it.pad;
         } else if constexpr (!DEC) {
             if (wg < g.pad) {

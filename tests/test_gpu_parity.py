@@ -311,6 +311,28 @@ def test_running_max_moves(shape):
     compare(out, lse, ro, rl, shape)
 
 
+def _sink_and_rival(wl, lens, d):
+    """Values where key 0 of every sequence (an attention sink) takes most of
+    a row's softmax mass and one rival key far into the sequence most of the
+    rest (weights about 0.64 and 0.36), with V of the rival -1.8 times the
+    sink's."""
+    k, v, q = W.make_values(wl)
+    q = q.float().abs().to(torch.bfloat16)  # positive q: a positive key gives a large score
+    k = k.float()
+    v = v.float()
+    base = 0
+    # scores ~ amp * 0.8 * sqrt(D); the rival sits 0.6 (natural log) below the sink
+    amp = 14.0 / (0.8 * d ** 0.5)
+    for s, L in enumerate(lens):
+        rival = base + 600 + 37 * s
+        k[base] = amp + 0.02 * k[base]
+        k[rival] = amp - 0.6 / (0.8 * d ** 0.5) + 0.02 * k[rival]
+        v[base] = 2.0 * v[base]
+        v[rival] = -1.8 * v[base]
+        base += L
+    return k.to(torch.bfloat16), v.to(torch.bfloat16), q
+
+
 @pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("opts", [dict(), dict(decode_split=12.0, prefill_split=16.0)])
 def test_attention_sink_with_a_rival_key(d, opts):
@@ -331,26 +353,35 @@ def test_attention_sink_with_a_rival_key(d, opts):
                   [[(0, 40), (560, 900), (1490, 1501)], [(1200, 1450), (2100, 2101)], [(1800, 1801)],
                    [(1298, 1301)]],
                   hq=8, hkv=2, d=d, seed=71)
-    k, v, q = W.make_values(wl)
-    q = q.float().abs().to(torch.bfloat16)  # positive q: a positive key gives a large score
-    k = k.float()
-    v = v.float()
-    base = 0
-    # scores ~ amp * 0.8 * sqrt(D); the rival sits 0.6 (natural log) below the sink
-    amp = 14.0 / (0.8 * d ** 0.5)
-    for s, L in enumerate(lens):
-        rival = base + 600 + 37 * s
-        k[base] = amp + 0.02 * k[base]
-        k[rival] = amp - 0.6 / (0.8 * d ** 0.5) + 0.02 * k[rival]
-        v[base] = 2.0 * v[base]
-        v[rival] = -1.8 * v[base]
-        base += L
-    k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    k, v, q = _sink_and_rival(wl, lens, d)
     out, lse, info = run_gpu(wl, k, v, q, **opts)
     assert info["num_prefill_items"] > 0 and info["num_decode_items"] > 0
     ro, rl = oracle_ref(wl, k, v, q)
     assert np.nanmax(rl) > 10.0  # the sink does dominate
     compare(out, lse, ro, rl, f"sink D={d} {opts}")
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (2, 2), (32, 2)])
+@pytest.mark.parametrize("opts", [dict(), dict(decode_split=12.0)])
+def test_attention_sink_decode_only(d, hq, hkv, opts):
+    """The sink-and-rival values in a launch of decode rows only (the
+    decode-only kernel): groups of at most 8 (query row x head) rows, whose
+    padding rows carry the bf16 residual of P through the same MMAs (G = 4
+    with one row, G = 1 with one and three rows), and groups of more (G = 4
+    with three rows, G = 16 with one), which take a second MMA; with and
+    without the key range split into parts."""
+    lens = [1500, 2100, 1800, 1301]
+    rows = 1 if hq // hkv == 16 else 3  # (query row x head) rows of a decode group: at most 16
+    wl = W.custom(lens, [[30, 40, 24], [50, 32, 30, 20], [40, 33, 40], [20, 21, 41]],
+                  [[(1499, 1500)], [(2101 - rows, 2101)], [(1799, 1800)], [(1301 - rows, 1301)]], hq=hq, hkv=hkv,
+                  d=d, seed=72)
+    k, v, q = _sink_and_rival(wl, lens, d)
+    out, lse, info = run_gpu(wl, k, v, q, **opts)
+    assert info["num_prefill_items"] == 0 and info["num_decode_items"] > 0
+    ro, rl = oracle_ref(wl, k, v, q)
+    assert np.nanmax(rl) > 10.0
+    compare(out, lse, ro, rl, f"decode-only sink D={d} G={hq // hkv} {opts}")
 
 
 @pytest.mark.parametrize("seed", range(48))
