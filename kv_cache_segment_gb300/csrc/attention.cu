@@ -403,6 +403,11 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
             const int st = kj % C::kStages, stp = kp % C::kStages;
             const int nk = (mt_prev.y + 15) >> 4;
             int2 mt_cur = mt_prev;
+            // V of tile j-1 and K of tile j first: they are normally loaded
+            // long before, and waiting for them here keeps their waits off the
+            // path from a warpgroup's P-ready signal to its next S
+            if (j >= 1 && !wait_bar_w(p, ctl, &ctl->v_full[stp], (kp / C::kStages) & 1, kErrTimeoutMma)) return;
+            if (j < T && !wait_bar_w(p, ctl, &ctl->k_full[st], (kj / C::kStages) & 1, kErrTimeoutMma)) return;
             for (int k = 0; k < nh; ++k) {
                 // O_k += P_k V for tile j-1: P_k (bf16 pairs) read from TMEM
                 // columns 0..63 of S_k (a softmax warp that needs the bf16
@@ -410,8 +415,6 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
                 if (j >= 1) {
                     if (!wait_bar_w(p, ctl, &ctl->p_full[k], (k ? pf1 : pf0) & 1, kErrTimeoutMma)) return;
                     if (k) ++pf1; else ++pf0;
-                    if (k == 0 && !wait_bar_w(p, ctl, &ctl->v_full[stp], (kp / C::kStages) & 1, kErrTimeoutMma))
-                        return;
                     if (jj == 0 &&
                         !wait_bar_w(p, ctl, &ctl->o_empty[k], ((k ? oc1 : oc0) & 1) ^ 1, kErrTimeoutMma))
                         return;
@@ -432,10 +435,7 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
                 }
                 // S_k = Q_k K^T for tile j
                 if (j < T) {
-                    if (k == 0) {
-                        if (!wait_bar_w(p, ctl, &ctl->k_full[st], (kj / C::kStages) & 1, kErrTimeoutMma)) return;
-                        mt_cur = ctl->tmeta[kj & 7];
-                    }
+                    if (k == 0) mt_cur = ctl->tmeta[kj & 7];
                     ptx::tc_fence_after();
                     const uint32_t kl = lK + (uint32_t)((st * C::kTileBytes) >> 4);
                     const uint32_t ql = lQ + (uint32_t)((k * C::kTileBytes) >> 4);
