@@ -355,7 +355,9 @@ int msa_plan_create_ex(const msa_dims* dims, int32_t num_seqs, int32_t max_block
  * 63), when there are more than 63, then C itself if it is not the last
  * one; a chunk larger than a sequence's remainder runs the remainder.
  * Host only; each candidate costs one msa_plan_create_ex and one
- * msa_plan_estimate.  Errors: MSA_ERR_INVALID_ARG (a null pointer, a
+ * msa_plan_estimate, and the candidates are evaluated on up to 8 host
+ * threads (the result does not depend on how many; opts->num_sms = 0 is
+ * resolved on the calling thread's current device first).  Errors: MSA_ERR_INVALID_ARG (a null pointer, a
  * sequence index out of range or listed twice, a pending sequence with rows
  * of its own, bad params), MSA_ERR_BAD_Q_RANGE (start < 0 or end <= start),
  * and whatever msa_plan_create_ex returns for a candidate's batch.

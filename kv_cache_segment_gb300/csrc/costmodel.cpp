@@ -10,7 +10,8 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
-#include <queue>
+#include <cstring>
+#include <thread>
 #include <utility>
 #include <vector>
 
@@ -54,24 +55,113 @@ int64_t tile_extra_boxes(const msa_plan_s* P, int32_t seq, int32_t t0, int32_t t
 // Per sequence, prefix sums of the extra boxes of its full 128-key tiles:
 // items start on tile boundaries, so an item's count is a difference of two
 // prefix sums plus, when its end is not on a boundary, its partial last tile.
+// One pass per sequence walks its tiles and runs together (both in logical
+// order); the sums of all sequences share one array.
 struct BoxCounts {
-    std::vector<std::vector<int64_t>> prefix;  // [seq][i] = sum over full tiles j < i
-    explicit BoxCounts(const msa_plan_s* P) : prefix(P->seq_lens.size()) {
-        for (size_t s = 0; s < P->seq_lens.size(); ++s) {
+    std::vector<int64_t> prefix;  // prefix[base[s] + i] = sum over full tiles j < i of sequence s
+    std::vector<size_t> base;
+    explicit BoxCounts(const msa_plan_s* P) : base(P->seq_lens.size() + 1, 0) {
+        const size_t S = P->seq_lens.size();
+        for (size_t s = 0; s < S; ++s) base[s + 1] = base[s] + (size_t)(P->seq_lens[s] / kTileKeys) + 1;
+        prefix.assign(base[S], 0);
+        for (size_t s = 0; s < S; ++s) {
             const int32_t full = P->seq_lens[s] / kTileKeys;
-            prefix[s].assign((size_t)full + 1, 0);
-            for (int32_t i = 0; i < full; ++i)
-                prefix[s][i + 1] = prefix[s][i] + tile_extra_boxes(P, (int32_t)s, i * kTileKeys, (i + 1) * kTileKeys);
+            const int32_t rb = P->run_indptr[s + 1];
+            int32_t r = P->run_indptr[s];  // first run that ends after the current tile's start
+            int64_t* pf = prefix.data() + base[s];
+            for (int32_t i = 0; i < full; ++i) {
+                const int32_t t0 = i * kTileKeys, t1 = t0 + kTileKeys;
+                while (r < rb && P->runs[r].log_start + P->runs[r].n_tok <= t0) ++r;
+                int64_t boxes = 0;
+                int32_t cur = t0;
+                for (int32_t q = r; q < rb && cur < t1; ++q) {
+                    const msa::Run& R = P->runs[q];
+                    const int32_t pend = std::min(t1, R.log_start + R.n_tok);
+                    if (pend <= cur) continue;
+                    if (cur == t0 && pend - cur == kTileKeys) {
+                        boxes += 1;
+                    } else {
+                        const int64_t nb = (pend - cur + kBlock - 1) / kBlock;
+                        boxes += nb / 4 + (nb % 4) / 2 + nb % 2;
+                    }
+                    cur = pend;
+                }
+                pf[i + 1] = pf[i] + (boxes > 1 ? boxes - 1 : 0);
+            }
         }
     }
     int64_t item(const msa_plan_s* P, const msa::Item& it) const {
         if (it.ke <= it.kb) return 0;
-        const std::vector<int64_t>& pf = prefix[it.seq];
+        const int64_t* pf = prefix.data() + base[it.seq];
+        const size_t last = base[it.seq + 1] - base[it.seq] - 1;
         const int32_t i0 = it.kb / kTileKeys, i1 = it.ke / kTileKeys;  // full tiles [i0, i1)
-        int64_t n = pf[std::min<size_t>(i1, pf.size() - 1)] - pf[std::min<size_t>(i0, pf.size() - 1)];
+        int64_t n = pf[std::min<size_t>(i1, last)] - pf[std::min<size_t>(i0, last)];
         if (it.ke % kTileKeys) n += tile_extra_boxes(P, it.seq, i1 * kTileKeys, it.ke);
         return n;
     }
+};
+
+// Binary min-heap of (key, CTA) pairs in lexicographic order (the CTA index
+// breaks ties, so the order in which entries leave it is fixed), with room
+// for every CTA reserved up front and a replace-top for "pop, then push".
+// Keys are finite and non-negative (times and byte counts that start at +0
+// and only grow), so the IEEE bit pattern of a key, as an unsigned integer,
+// orders like its value: an entry is stored as one 128-bit integer, key bits
+// above the CTA index, and compared in one step.
+class MinHeap {
+public:
+    using Ev = std::pair<double, int32_t>;
+    explicit MinHeap(size_t cap) { h_.reserve(cap); }
+    bool empty() const { return h_.empty(); }
+    size_t size() const { return h_.size(); }
+    Ev top() const { return decode(h_[0]); }
+    void push(Ev v) {
+        const K key = encode(v);
+        size_t i = h_.size();
+        h_.push_back(key);
+        while (i > 0) {
+            const size_t p = (i - 1) / 2;
+            if (!(key < h_[p])) break;
+            h_[i] = h_[p];
+            i = p;
+        }
+        h_[i] = key;
+    }
+    void pop() {
+        const K last = h_.back();
+        h_.pop_back();
+        if (!h_.empty()) sift_down(last);
+    }
+    void replace_top(Ev v) { sift_down(encode(v)); }
+
+private:
+    using K = unsigned __int128;
+    static K encode(Ev v) {
+        uint64_t bits;
+        std::memcpy(&bits, &v.first, sizeof bits);
+        return ((K)bits << 32) | (uint32_t)v.second;
+    }
+    static Ev decode(K k) {
+        const uint64_t bits = (uint64_t)(k >> 32);
+        double d;
+        std::memcpy(&d, &bits, sizeof d);
+        return {d, (int32_t)(uint32_t)k};
+    }
+    // place v at the root and move it down to where it belongs
+    void sift_down(K v) {
+        const size_t n = h_.size();
+        size_t i = 0;
+        for (;;) {
+            size_t c = 2 * i + 1;
+            if (c >= n) break;
+            c += (size_t)((c + 1 < n) & (h_[c + 1] < h_[c]));
+            if (!(h_[c] < v)) break;
+            h_[i] = h_[c];
+            i = c;
+        }
+        h_[i] = v;
+    }
+    std::vector<K> h_;
 };
 
 bool params_ok(const msa_cost_params* c) {
@@ -120,9 +210,8 @@ int estimate(const msa_plan_s* P, const msa_cost_params* c, const BoxCounts& box
     // time (fixed phases) and one in sigma (streams).  Which of several CTAs
     // freed at the same instant takes which item does not change the finish
     // times, the CTAs being alike.
-    using Ev = std::pair<double, int32_t>;
-    std::priority_queue<Ev, std::vector<Ev>, std::greater<Ev>> fixed_q, stream_q;
     const int32_t grid = std::max(1, P->grid);
+    MinHeap fixed_q((size_t)grid), stream_q((size_t)grid);
     std::vector<int32_t> item(grid, -1);
     size_t next = 0;
     double t = 0.0, sigma = 0.0;
@@ -142,11 +231,18 @@ int estimate(const msa_plan_s* P, const msa_cost_params* c, const BoxCounts& box
         const double t_stream = stream_q.empty() ? INFINITY : t + (stream_q.top().first - sigma) / r;
         if (t_fixed <= t_stream) {
             const int32_t b = fixed_q.top().second;
-            fixed_q.pop();
             if (r > 0.0) sigma += (t_fixed - t) * r;
             t = t_fixed;
-            if (bytes[item[b]] > 0.0) stream_q.push({sigma + bytes[item[b]], b});
-            else take(b);
+            if (bytes[item[b]] > 0.0) {
+                fixed_q.pop();
+                stream_q.push({sigma + bytes[item[b]], b});
+            } else if (next < P->order.size()) {  // the CTA's next item, in place of this one
+                item[b] = P->order[next++];
+                fixed_q.replace_top({t + fixed[item[b]], b});
+            } else {
+                item[b] = -1;
+                fixed_q.pop();
+            }
         } else {
             const int32_t b = stream_q.top().second;
             sigma = stream_q.top().first;
@@ -255,15 +351,24 @@ int msa_choose_prefill_chunk(const msa_dims* dims, int32_t num_seqs, int32_t max
     for (int32_t k = 1; k <= n_mult; k += step) cands.push_back(k * g);
     if (cands.empty() || cands.back() != cmax) cands.push_back(cmax);
 
-    const int32_t n_ranges = q_range_indptr[num_seqs];
-    std::vector<int32_t> lens(num_seqs), indptr(num_seqs + 1), ranges;
-    ranges.reserve(2 * ((size_t)n_ranges + n_pending));
-    int best = -1;
-    double best_per = INFINITY;
-    for (size_t ci = 0; ci < cands.size(); ++ci) {
+    // The SM count is resolved here: a worker thread would see the CUDA
+    // runtime's default device rather than the caller's current one.
+    msa_plan_options o = opts ? *opts : msa_plan_options{0, 0.0, 0.0, nullptr};
+    if (o.num_sms == 0) {
+        o.num_sms = msa::device_sm_count();
+        if (o.num_sms <= 0) return MSA_ERR_CUDA;
+    }
+    const size_t n_cand = cands.size();
+    std::vector<double> time_us(n_cand, 0.0);
+    std::vector<int64_t> tokens(n_cand, 0);
+    std::vector<int> status(n_cand, MSA_OK);
+    // Candidate ci: the step's batch with min(c, remainder) rows of every
+    // pending prefill, planned and priced.  Candidates are independent.
+    auto evaluate = [&](size_t ci) {
         const int32_t c = cands[ci];
-        int64_t tokens = 0;
-        ranges.clear();
+        std::vector<int32_t> lens(num_seqs), indptr(num_seqs + 1), ranges;
+        ranges.reserve(2 * ((size_t)q_range_indptr[num_seqs] + n_pending));
+        int64_t tok = 0;
         indptr[0] = 0;
         for (int32_t s = 0; s < num_seqs; ++s) {
             if (remain[s] >= 0) {
@@ -271,7 +376,7 @@ int msa_choose_prefill_chunk(const msa_dims* dims, int32_t num_seqs, int32_t max
                 lens[s] = start[s] + n;
                 ranges.push_back(start[s]);
                 ranges.push_back(start[s] + n);
-                tokens += n;
+                tok += n;
             } else {
                 lens[s] = seq_lens[s];
                 for (int32_t r = q_range_indptr[s]; r < q_range_indptr[s + 1]; ++r) {
@@ -281,18 +386,51 @@ int msa_choose_prefill_chunk(const msa_dims* dims, int32_t num_seqs, int32_t max
             }
             indptr[s + 1] = (int32_t)(ranges.size() / 2);
         }
+        tokens[ci] = tok;
         msa_plan_t plan = nullptr;
         int rc = msa_plan_create_ex(dims, num_seqs, max_blocks_per_seq, block_table, lens.data(), indptr.data(),
-                                    ranges.data(), opts, &plan);
-        if (rc != MSA_OK) return rc;
-        msa_cost_estimate e{};
-        rc = msa_plan_estimate(plan, params, &e);
+                                    ranges.data(), &o, &plan);
+        if (rc == MSA_OK) {
+            msa_cost_estimate e{};
+            rc = msa_plan_estimate(plan, params, &e);
+            time_us[ci] = e.time_us;
+        }
         msa_plan_destroy(plan);
-        if (rc != MSA_OK) return rc;
+        status[ci] = rc;
+    };
+    // Up to 8 host threads share the candidates (each plans with its own
+    // scratch); if threads cannot be started, this thread does the rest.
+    const unsigned hw = std::thread::hardware_concurrency();
+    const size_t n_thr = std::min<size_t>(n_cand, std::max<unsigned>(1u, std::min(hw, 8u)));
+    std::vector<std::thread> pool;
+    size_t started = 1;
+    if (n_thr > 1) {
+        try {
+            pool.reserve(n_thr - 1);
+            for (size_t k = 1; k < n_thr; ++k) {
+                pool.emplace_back([&, k] {
+                    for (size_t ci = k; ci < n_cand; ci += n_thr) evaluate(ci);
+                });
+                ++started;
+            }
+        } catch (...) {
+        }
+    }
+    for (size_t ci = 0; ci < n_cand; ci += n_thr) evaluate(ci);
+    for (auto& th : pool) th.join();
+    // candidates of workers that never started
+    for (size_t k = started; k < n_thr; ++k)
+        for (size_t ci = k; ci < n_cand; ci += n_thr) evaluate(ci);
+
+    int best = -1;
+    double best_per = INFINITY;
+    for (size_t ci = 0; ci < n_cand; ++ci) {
+        if (status[ci] != MSA_OK) return status[ci];
+        const int32_t c = cands[ci];
         if (cand_chunk) cand_chunk[ci] = c;
-        if (cand_time_us) cand_time_us[ci] = e.time_us;
-        const double per = e.time_us / (double)tokens;
-        const bool ok = budget_us <= 0.0 || e.time_us <= budget_us;
+        if (cand_time_us) cand_time_us[ci] = time_us[ci];
+        const double per = time_us[ci] / (double)tokens[ci];
+        const bool ok = budget_us <= 0.0 || time_us[ci] <= budget_us;
         // ascending c, so "<=" gives equal per-token costs to the larger chunk
         if (ok && per <= best_per) {
             best_per = per;
@@ -300,8 +438,8 @@ int msa_choose_prefill_chunk(const msa_dims* dims, int32_t num_seqs, int32_t max
         }
         if (ci == 0 || (int)ci == best) {
             choice->chunk = c;
-            choice->tokens = (int32_t)tokens;
-            choice->time_us = e.time_us;
+            choice->tokens = (int32_t)tokens[ci];
+            choice->time_us = time_us[ci];
             choice->us_per_token = per;
         }
     }

@@ -45,6 +45,7 @@ thread_local std::vector<std::unique_ptr<msa_plan_s>> t_recycled;
 thread_local std::vector<Pending> t_pend;
 thread_local std::vector<double> t_cost;
 thread_local std::vector<uint64_t> t_keys;  // queue-order sort keys
+thread_local std::vector<unsigned __int128> t_ord;  // (key, item) pairs being sorted
 }  // namespace
 
 // Number of KV tiles the kernels walk over keys [kb, ke): 128-key windows
@@ -152,9 +153,14 @@ void split_items(msa_plan_s* P, const std::vector<Pending>& pend, double dec_spl
         const uint64_t kvh = (uint64_t)(g.kind == kDecode ? g.head : g.head / P->G);
         keys[i] = ((0x1FFFFull - (bits >> 47)) << 46) | (((uint64_t)it.seq & 0x3FFFFFFull) << 20) | (kvh & 0xFFFFFull);
     }
+    // sort (key, generation index) as one 128-bit integer: the same order as a
+    // stable sort by key, on contiguous values
+    std::vector<unsigned __int128>& ord = t_ord;
+    ord.resize(n_items);
+    for (int32_t i = 0; i < n_items; ++i) ord[i] = ((unsigned __int128)keys[i] << 32) | (uint32_t)i;
+    std::sort(ord.begin(), ord.end());
     P->order.resize(n_items);
-    for (int32_t i = 0; i < n_items; ++i) P->order[i] = i;
-    std::stable_sort(P->order.begin(), P->order.end(), [&](int32_t a, int32_t b) { return keys[a] < keys[b]; });
+    for (int32_t i = 0; i < n_items; ++i) P->order[i] = (int32_t)(uint32_t)ord[i];
 }
 
 
