@@ -1,5 +1,5 @@
 """The bench's host-side contract (CPU only): the reference arm's JSON line
-carries the keys the driver reads, and the code hash that keys the stored
+carries every key of the bench line format, and the code hash that keys the stored
 DRAM-traffic figures ignores comments but not code."""
 import io
 import json
