@@ -312,8 +312,12 @@ int msa_plan_get_order(msa_plan_t plan, int32_t* order, int32_t* n_items) {
 int msa_plan_estimate(msa_plan_t plan, const msa_cost_params* c, msa_cost_estimate* e) {
     if (!plan || !c || !e) return MSA_ERR_INVALID_ARG;
     if (!params_ok(c)) return MSA_ERR_INVALID_ARG;
-    const BoxCounts box_counts(plan);
-    return estimate(plan, c, box_counts, e);
+    try {
+        const BoxCounts box_counts(plan);
+        return estimate(plan, c, box_counts, e);
+    } catch (...) {  // allocation failure: no exception leaves the C ABI
+        return MSA_ERR_INVALID_ARG;
+    }
 }
 
 // Adaptive prefill chunk size: the candidate chunk sizes in ascending order
@@ -321,12 +325,12 @@ int msa_plan_estimate(msa_plan_t plan, const msa_cost_params* c, msa_cost_estima
 // at max_chunk, thinned to at most 63 multiples, plus the cap itself), a
 // plan and a latency-model prediction of the step for each, and the lowest
 // predicted time per prefill token within the budget.
-int msa_choose_prefill_chunk(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks_per_seq,
-                             const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_range_indptr,
-                             const int32_t* q_ranges, const msa_pending_prefill* pending, int32_t n_pending,
-                             const msa_plan_options* opts, const msa_cost_params* params, double budget_us,
-                             int32_t granularity, int32_t max_chunk, msa_chunk_choice* choice, int32_t* cand_chunk,
-                             double* cand_time_us) {
+static int choose_prefill_chunk(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks_per_seq,
+                                const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_range_indptr,
+                                const int32_t* q_ranges, const msa_pending_prefill* pending, int32_t n_pending,
+                                const msa_plan_options* opts, const msa_cost_params* params, double budget_us,
+                                int32_t granularity, int32_t max_chunk, msa_chunk_choice* choice,
+                                int32_t* cand_chunk, double* cand_time_us) {
     if (!dims || !seq_lens || !q_range_indptr || !pending || !params || !choice) return MSA_ERR_INVALID_ARG;
     if (num_seqs <= 0 || n_pending <= 0 || n_pending > num_seqs || granularity < 0 || max_chunk < 0 ||
         !std::isfinite(budget_us) || !params_ok(params))
@@ -365,6 +369,7 @@ int msa_choose_prefill_chunk(const msa_dims* dims, int32_t num_seqs, int32_t max
     // Candidate ci: the step's batch with min(c, remainder) rows of every
     // pending prefill, planned and priced.  Candidates are independent.
     auto evaluate = [&](size_t ci) {
+      try {
         const int32_t c = cands[ci];
         std::vector<int32_t> lens(num_seqs), indptr(num_seqs + 1), ranges;
         ranges.reserve(2 * ((size_t)q_range_indptr[num_seqs] + n_pending));
@@ -397,6 +402,9 @@ int msa_choose_prefill_chunk(const msa_dims* dims, int32_t num_seqs, int32_t max
         }
         msa_plan_destroy(plan);
         status[ci] = rc;
+      } catch (...) {  // allocation failure in this candidate
+        status[ci] = MSA_ERR_INVALID_ARG;
+      }
     };
     // Up to 8 host threads share the candidates (each plans with its own
     // scratch); if threads cannot be started, this thread does the rest.
@@ -449,13 +457,28 @@ int msa_choose_prefill_chunk(const msa_dims* dims, int32_t num_seqs, int32_t max
     return MSA_OK;
 }
 
+int msa_choose_prefill_chunk(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks_per_seq,
+                             const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_range_indptr,
+                             const int32_t* q_ranges, const msa_pending_prefill* pending, int32_t n_pending,
+                             const msa_plan_options* opts, const msa_cost_params* params, double budget_us,
+                             int32_t granularity, int32_t max_chunk, msa_chunk_choice* choice, int32_t* cand_chunk,
+                             double* cand_time_us) {
+    try {
+        return choose_prefill_chunk(dims, num_seqs, max_blocks_per_seq, block_table, seq_lens, q_range_indptr,
+                                    q_ranges, pending, n_pending, opts, params, budget_us, granularity, max_chunk,
+                                    choice, cand_chunk, cand_time_us);
+    } catch (...) {  // allocation failure: no exception leaves the C ABI
+        return MSA_ERR_INVALID_ARG;
+    }
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------- eviction --
 
-extern "C" int msa_select_evictions(const msa_dims* dims, int32_t seq_len, const float* hit_prob, int32_t mode,
-                                    double alpha, double beta, const msa_cost_params* params, int32_t n_evict,
-                                    int32_t* evicted, double* cost_us) {
+static int select_evictions(const msa_dims* dims, int32_t seq_len, const float* hit_prob, int32_t mode,
+                            double alpha, double beta, const msa_cost_params* params, int32_t n_evict,
+                            int32_t* evicted, double* cost_us) {
     if (!dims || !params || seq_len < 0) return MSA_ERR_INVALID_ARG;
     if (mode & ~(MSA_EVICT_EXPECTED_COST | MSA_EVICT_PREFIX_COST)) return MSA_ERR_INVALID_ARG;
     const bool expected = (mode & MSA_EVICT_EXPECTED_COST) != 0;
@@ -494,4 +517,14 @@ extern "C" int msa_select_evictions(const msa_dims* dims, int32_t seq_len, const
     std::sort(out.begin(), out.end());
     for (int32_t i = 0; i < n_evict; ++i) evicted[i] = out[i];
     return MSA_OK;
+}
+
+extern "C" int msa_select_evictions(const msa_dims* dims, int32_t seq_len, const float* hit_prob, int32_t mode,
+                                    double alpha, double beta, const msa_cost_params* params, int32_t n_evict,
+                                    int32_t* evicted, double* cost_us) {
+    try {
+        return select_evictions(dims, seq_len, hit_prob, mode, alpha, beta, params, n_evict, evicted, cost_us);
+    } catch (...) {  // allocation failure: no exception leaves the C ABI
+        return MSA_ERR_INVALID_ARG;
+    }
 }
