@@ -180,7 +180,11 @@ void plan_release(msa_plan_s* P) {
         return;
     }
     P->reset();
-    t_recycled.emplace_back(P);
+    try {
+        t_recycled.emplace_back(P);
+    } catch (...) {  // no room to keep it: free it instead
+        delete P;
+    }
 }
 
 int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
