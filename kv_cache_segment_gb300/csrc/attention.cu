@@ -114,8 +114,16 @@ struct Cfg {
     static constexpr int kOffCtl = kOffScr + kScrBytes;
     static constexpr int kCtlBytes = 1536;
     static constexpr int kSmem = kOffCtl + kCtlBytes + 1024;  // + slack to align the base to 1024
-    static constexpr uint32_t kTmemCols = 512;        // S0 [0,128) S1 [128,256) O0, O1 from 256
-    static constexpr uint32_t kTmemO = 256;
+    // TMEM: S buffers of 128 columns from column 0, then O0 and O1 (D columns
+    // each).  At D = 128 that is S0, S1, O0, O1.  At D = 64 a third S buffer
+    // fits, and the S MMAs rotate over the three (kRot): slot n of a CTA's
+    // prefill work (tile j, query tile k, counted across items) uses buffer
+    // n % 3, so the S of a query tile's next key tile is issued ahead of the
+    // PV of its current one.
+    static constexpr bool kRot = !DEC && D == 64;
+    static constexpr int kSBufs = kRot ? 3 : 2;
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kTmemO = kSBufs * 128;
     static_assert(kSmem + 64 <= 232448, "shared memory over the per-CTA limit");
     static_assert(kTmemO + 2 * D <= kTmemCols, "TMEM budget");
 };
@@ -123,7 +131,8 @@ struct Cfg {
 struct Ctl {
     uint64_t k_full[8], k_empty[8], v_full[8], v_empty[8];
     uint64_t q_full, q_empty;
-    uint64_t s_full[2], p_full[2], p_empty[2], o_empty[2];
+    uint64_t s_full[3], p_full[3], p_empty[3];  // per S buffer
+    uint64_t o_empty[2];
     uint64_t o_full;
     uint64_t drain;
     uint64_t csync[2];  // bounded barriers of warpgroup 0 / 1 (128 threads each)
@@ -449,6 +458,116 @@ __device__ void mma_issuer(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lan
                         ptx::tc_mma_ss_e<1>(ts, ql + off, kl + off, hi, kIdescS);
                     }
                     ptx::tc_commit_e(&ctl->s_full[k]);
+                }
+            }
+            if (j >= 1) {
+                ptx::tc_commit_e(&ctl->v_empty[stp]);
+                if (jj == T - 1) {
+                    ptx::tc_commit_e(&ctl->o_full);
+                    ++oc0;
+                    if (nh == 2) ++oc1;
+                }
+            }
+            if (j < T) {
+                ptx::tc_commit_e(&ctl->k_empty[st]);
+                if (j == T - 1) ptx::tc_commit_e(&ctl->q_empty);
+            }
+            mt_prev = mt_cur;
+        }
+        kv_cnt += T;
+    }
+}
+
+// MMA warp of the rotating-buffer launch (D = 64, three S buffers).  The
+// prefill slots of the CTA, n = j * nh + k for key tile j and query tile k of
+// an item, counted on across items, take S buffer n % 3.  The loop is the
+// two-buffer one with the S MMA moved in front of the PV: as soon as query
+// tile k's P of tile j-1 is ready, S_k(j) goes into the buffer that the PV
+// of slot n - 3 (issued before it; the tensor pipe runs one thread's MMAs
+// in order) has read, and only then PV_k(j-1).  A warpgroup's next S thus
+// waits for its P-ready signal and four MMAs, not for twelve.  Per buffer
+// b: s_full[b] (S ready), p_full[b] (P ready, four warp arrivals) and
+// p_empty[b] (the PV that read P done).  The MMA warp waits for the P of
+// the slots in order, so no barrier runs two phases ahead of its waiter:
+// S(n + 3) is issued after the wait for P(n), which the warpgroup signals
+// after its wait for S(n); P(n + 3) follows S(n + 3); and a warpgroup at slot
+// n that waits for the PV of its previous tile's slot n - nh has seen S(n),
+// issued after PV(n - nh - 3), while PV(n - nh + 3) waits for P(n).
+template <int D, bool DEC>
+__device__ void mma_issuer_rot(const AttnParams& p, uint8_t* smem, Ctl* ctl, int lane) {
+    using C = Cfg<D, DEC>;
+    constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, 128, 0, 0);  // Q K-major, K K-major
+    constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, 0, 1);   // P (TMEM), V MN-major
+    const uint32_t tbase = ctl->tmem_base;
+    const uint64_t dQ = ptx::smem_desc(ptx::smem_u32(smem + C::kOffQ), 16, 1024, 2);
+    const uint32_t hi = (uint32_t)(dQ >> 32);
+    const uint32_t lQ = (uint32_t)dQ;
+    const uint32_t lK = (uint32_t)ptx::smem_desc(ptx::smem_u32(smem + C::kOffK), 16, 1024, 2);
+    const uint32_t lV = (uint32_t)ptx::smem_desc(ptx::smem_u32(smem + C::kOffV), C::kPanelBytes, 1024, 2);
+    uint32_t kv_cnt = 0, q_cnt = 0, oc0 = 0, oc1 = 0, n_taken = 0;
+    // S buffer of the next S slot; S buffer and P-ready phase of the next PV slot
+    uint32_t bs = 0, bp = 0, php = 0;
+
+    for (;;) {
+        const int ii = take_item_w(p, ctl, n_taken, kErrTimeoutMma, lane);
+        if (ii < 0) return;
+        const Item it = p.items[ii];
+        const int T = it.pad;  // KV tiles of this item
+        if (it.kind != kPrefill) { kv_cnt += T; continue; }
+        const Group g = p.groups[it.group];
+        const int nh = g.pad;
+        if (!wait_bar_w(p, ctl, &ctl->q_full, q_cnt & 1, kErrTimeoutMma)) return;
+        ++q_cnt;
+        int2 mt_prev = make_int2(0, 0);  // metadata of tile j-1, read when its S was issued
+        for (int j = 0; j <= T; ++j) {
+            const int jj = j - 1;
+            const uint32_t kj = kv_cnt + j, kp = kv_cnt + jj;
+            const int st = kj % C::kStages, stp = kp % C::kStages;
+            const int nk = (mt_prev.y + 15) >> 4;
+            int2 mt_cur = mt_prev;
+            if (j >= 1 && !wait_bar_w(p, ctl, &ctl->v_full[stp], (kp / C::kStages) & 1, kErrTimeoutMma)) return;
+            if (j < T && !wait_bar_w(p, ctl, &ctl->k_full[st], (kj / C::kStages) & 1, kErrTimeoutMma)) return;
+            for (int k = 0; k < nh; ++k) {
+                if (j >= 1) {
+                    if (!wait_bar_w(p, ctl, &ctl->p_full[bp], php, kErrTimeoutMma)) return;
+                    if (jj == 0 &&
+                        !wait_bar_w(p, ctl, &ctl->o_empty[k], ((k ? oc1 : oc0) & 1) ^ 1, kErrTimeoutMma))
+                        return;
+                }
+                ptx::tc_fence_after();
+                // S_k = Q_k K^T for tile j, first
+                if (j < T) {
+                    if (k == 0) mt_cur = ctl->tmeta[kj & 7];
+                    const uint32_t kl = lK + (uint32_t)((st * C::kTileBytes) >> 4);
+                    const uint32_t ql = lQ + (uint32_t)((k * C::kTileBytes) >> 4);
+                    const uint32_t ts = tbase + bs * 128;
+                    ptx::tc_mma_ss_e<0>(ts, ql, kl, hi, kIdescS);
+#pragma unroll
+                    for (int ks = 1; ks < D / 16; ++ks) {
+                        const uint32_t off = (uint32_t)(((ks >> 2) * C::kPanelBytes + (ks & 3) * 32) >> 4);
+                        ptx::tc_mma_ss_e<1>(ts, ql + off, kl + off, hi, kIdescS);
+                    }
+                    ptx::tc_commit_e(&ctl->s_full[bs]);
+                    bs = bs == 2 ? 0 : bs + 1;
+                }
+                // then O_k += P_k V for tile j-1
+                if (j >= 1) {
+                    const uint32_t vl = lV + (uint32_t)((stp * C::kTileBytes) >> 4);
+                    const uint32_t to = tbase + C::kTmemO + k * D, tp = tbase + bp * 128;
+                    if (nk == kTileKeys / 16) {
+#pragma unroll
+                        for (int ks = 0; ks < kTileKeys / 16; ++ks)
+                            ptx::tc_mma_ts_e<1>(to, tp + ks * 8, vl + ks * 128, hi, kIdescPV);
+                    } else {
+                        for (int ks = 0; ks < nk; ++ks) ptx::tc_mma_ts_e<1>(to, tp + ks * 8, vl + ks * 128, hi, kIdescPV);
+                    }
+                    ptx::tc_commit_e(&ctl->p_empty[bp]);
+                    if (bp == 2) {
+                        bp = 0;
+                        php ^= 1;
+                    } else {
+                        ++bp;
+                    }
                 }
             }
             if (j >= 1) {
@@ -1007,16 +1126,18 @@ __device__ __noinline__ float2 careful_exps(uint32_t tS, int lim, float sl, floa
 
 // Second PV pass of one softmax warp (quarter q of warpgroup k) for the tile
 // in V stage st: O_k += R V over this warp's 32 rows, R = p - bf16(p) in
-// TMEM columns 64..127 of S_k (keys 2i, 2i+1 in column 64 + i), every other
-// row masked out of the MMA.  The warp issues it itself, so the MMA warp's
-// loop is the same whether or not a tile needs it, and its completion is
-// this warp's P-ready arrival (tcgen05.commit onto p_full): the MMA warp's
-// own pass over O_k for this tile starts only after it.  The pass before
-// has completed already: the S MMA of this tile, whose completion this warp
-// waited for, was issued after it.  O_k is zero before an item's first tile.
+// TMEM columns 64..127 of the tile's S buffer sbuf (keys 2i, 2i+1 in column
+// 64 + i), every other row masked out of the MMA.  The warp issues it
+// itself, so the MMA warp's loop is the same whether or not a tile needs
+// it, and its completion is this warp's P-ready arrival (tcgen05.commit onto
+// p_full): the MMA warp's own pass over O_k for this tile starts only after
+// it.  The pass before has completed already: with two S buffers the S MMA
+// of this tile, whose completion this warp waited for, was issued after it;
+// with three the caller waits for it.  O_k is zero before an item's first
+// tile.
 template <int D, bool DEC>
 __device__ bool residual_pass(const AttnParams& p, uint8_t* smem, Ctl* ctl, int k, int q, int lane, int st,
-                              uint32_t ph, int n) {
+                              uint32_t ph, int n, uint32_t sbuf) {
     using C = Cfg<D, DEC>;
     constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, 0, 1);  // as the MMA warp's PV
     if (!wait_bar(p, ctl, &ctl->v_full[st], ph, kErrTimeoutCompute)) return false;
@@ -1036,11 +1157,11 @@ __device__ bool residual_pass(const AttnParams& p, uint8_t* smem, Ctl* ctl, int 
     const uint64_t dV = ptx::smem_desc(ptx::smem_u32(smem + C::kOffV), C::kPanelBytes, 1024, 2);
     const uint32_t hi = (uint32_t)(dV >> 32);
     const uint32_t vl = (uint32_t)dV + (uint32_t)((st * C::kTileBytes) >> 4);
-    const uint32_t to = ctl->tmem_base + C::kTmemO + k * D, ta = ctl->tmem_base + k * 128 + 64;
+    const uint32_t to = ctl->tmem_base + C::kTmemO + k * D, ta = ctl->tmem_base + sbuf * 128 + 64;
     const uint32_t m0 = q == 0 ? 0u : ~0u, m1 = q == 1 ? 0u : ~0u, m2 = q == 2 ? 0u : ~0u, m3 = q == 3 ? 0u : ~0u;
     const int nk = (n + 15) >> 4;
     for (int ks = 0; ks < nk; ++ks) ptx::tc_mma_ts_masked_e(to, ta + ks * 8, vl + ks * 128, hi, kIdescPV, m0, m1, m2, m3);
-    ptx::tc_commit_e(&ctl->p_full[k]);
+    ptx::tc_commit_e(&ctl->p_full[sbuf]);
     return true;
 }
 
@@ -1056,9 +1177,12 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
     const int prow = valid ? p.pos[r0 + ri] : -1;
     const int head = qtile_head(p, g, k);
     const uint32_t tlane = ctl->tmem_base + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t tS = tlane + k * 128;             // S_k, later P_k (cols 0..63) and its residual (64..127)
     const uint32_t tO = tlane + C::kTmemO + k * D;  // O_k
     const int T = it.pad;
+    const int nh = g.pad;
+    // rotating S buffers: sk counts the slots of every earlier prefill item
+    const uint32_t sb = sk;
+    if constexpr (C::kRot) sk += (uint32_t)(T * nh);
     const float sl = p.scale_log2;
     // l: sum of the fp32 probabilities: the normaliser of the output and the
     // lse.  P reaches the PV MMA rounded to bf16.  lg_l = log2(l).
@@ -1068,8 +1192,25 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
         const uint32_t kj = kv_cnt + j;
         const int st = kj % C::kStages;
         const uint32_t ph = (kj / C::kStages) & 1;
-        if (!wait_bar(p, ctl, &ctl->s_full[k], sk & 1, kErrTimeoutCompute)) return false;
-        ++sk;
+        // this tile's S buffer and phase; the S buffer of this query tile's
+        // previous tile (whose PV is the last write into O_k before this
+        // tile's) and the phase of its PV-done barrier
+        uint32_t sbuf, sph, pb, pph;
+        if constexpr (C::kRot) {
+            const uint32_t n = sb + (uint32_t)(j * nh + k), np = n - (uint32_t)nh;
+            sbuf = n % 3;
+            sph = (n / 3) & 1;
+            pb = np % 3;
+            pph = (np / 3) & 1;
+        } else {
+            sbuf = k;
+            sph = sk & 1;
+            ++sk;
+            pb = k;
+            pph = (pvk - 1) & 1;
+        }
+        const uint32_t tS = tlane + sbuf * 128;  // S, later P (cols 0..63) and its residual (64..127)
+        if (!wait_bar(p, ctl, &ctl->s_full[sbuf], sph, kErrTimeoutCompute)) return false;
         if (!wait_bar(p, ctl, &ctl->meta_full[kj & 7], (kj >> 3) & 1, kErrTimeoutCompute)) return false;
         ptx::tc_fence_after();
         const int2 mt = ctl->tmeta[kj & 7];
@@ -1119,7 +1260,7 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
             vote = (__any_sync(0xffffffffu, resc) ? 1u : 0u) | (__any_sync(0xffffffffu, careful) ? 2u : 0u);
         if (vote & 1u) {
             // O_k must hold PV_k(j-1) before it is scaled
-            if (!wait_bar(p, ctl, &ctl->p_empty[k], (pvk - 1) & 1, kErrTimeoutCompute)) return false;
+            if (!wait_bar(p, ctl, &ctl->p_empty[pb], pph, kErrTimeoutCompute)) return false;
             ptx::tc_fence_after();
             const float f = resc ? alpha : 1.f;
 #pragma unroll 1
@@ -1204,9 +1345,14 @@ __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const
         ptx::tc_fence_before();
         __syncwarp();
         if (wresid) {
-            if (!residual_pass<D, DEC>(p, smem, ctl, k, quarter, lane, st, ph, n)) return false;
+            if constexpr (C::kRot) {
+                // with rotating buffers this tile's S can complete before the
+                // PV of the previous tile into O_k is issued: wait for it
+                if (j > 0 && !wait_bar(p, ctl, &ctl->p_empty[pb], pph, kErrTimeoutCompute)) return false;
+            }
+            if (!residual_pass<D, DEC>(p, smem, ctl, k, quarter, lane, st, ph, n, sbuf)) return false;
         } else if (lane == 0) {
-            ptx::mbar_arrive(&ctl->p_full[k]);
+            ptx::mbar_arrive(&ctl->p_full[sbuf]);
         }
         ++pvk;
     }
@@ -1360,8 +1506,9 @@ __device__ void compute(const AttnParams& p, uint8_t* smem, Ctl* ctl, int warp, 
         } else if constexpr (!DEC) {
             if (wg < g.pad) {
                 ok = prefill_item<D, DEC>(p, smem, ctl, it, g, kv_cnt, sk, pvk, ok_cnt, cs, wg, warp, lane);
-            } else {  // a one-head item: only the o_full phase and the ring position move on
+            } else {  // a one-head item: only the o_full phase and the ring positions move on
                 kv_cnt += it.pad;
+                if constexpr (Cfg<D, DEC>::kRot) sk += (uint32_t)it.pad;
                 ++ok_cnt;
             }
         }
@@ -1391,10 +1538,12 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
         }
         ptx::mbar_init(&ctl->q_full, 1);
         ptx::mbar_init(&ctl->q_empty, 1);
+        for (int b = 0; b < 3; ++b) {
+            ptx::mbar_init(&ctl->s_full[b], 1);
+            ptx::mbar_init(&ctl->p_full[b], 4);  // one arrival per softmax warp
+            ptx::mbar_init(&ctl->p_empty[b], 1);
+        }
         for (int k = 0; k < 2; ++k) {
-            ptx::mbar_init(&ctl->s_full[k], 1);
-            ptx::mbar_init(&ctl->p_full[k], 4);  // one arrival per softmax warp
-            ptx::mbar_init(&ctl->p_empty[k], 1);
             ptx::mbar_init(&ctl->o_empty[k], 128);
             ptx::mbar_init(&ctl->csync[k], 128);
         }
@@ -1440,7 +1589,10 @@ __global__ void __launch_bounds__(Cfg<D, DEC>::kThreads, 1)
         } else if (warp == 1) {
             if constexpr (!DEC) {
                 if (p.has_prefill) {
-                    mma_issuer<D, DEC>(p, smem, ctl, lane);
+                    if constexpr (C::kRot)
+                        mma_issuer_rot<D, DEC>(p, smem, ctl, lane);
+                    else
+                        mma_issuer<D, DEC>(p, smem, ctl, lane);
                     __syncwarp();
                     if (lane == 0) {
                         // every MMA lane 0 issued must have completed before TMEM is released

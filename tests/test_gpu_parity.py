@@ -237,8 +237,10 @@ def test_edge_cases(case):
 @pytest.mark.parametrize("hq,hkv,d", [(4, 4, 128), (6, 2, 128), (10, 2, 128), (6, 2, 64)])
 @pytest.mark.parametrize("opts", [dict(), dict(decode_split=12.0, prefill_split=16.0)])
 def test_odd_gqa_ratios(hq, hkv, d, opts):
-    """G = Hq/Hkv odd: prefill items carry one query head (the second softmax
-    warpgroup idles), and a decode item packs floor(16 / G) rows.  Sequence 0
+    """G = Hq/Hkv odd: a prefill item carries one query head over two
+    consecutive 128-row tiles (over one, with the second softmax warpgroup
+    idle, where the group is shorter), and a decode item packs floor(16 / G)
+    rows.  Sequence 0
     has two full 128-row tiles and a ragged prefill tail; sequence 1 has 3
     decode rows; sequence 2 has 4 rows, which is a decode item for G <= 4
     and a 4-row prefill tile for G = 5.  The second plan splits groups, so
@@ -255,10 +257,11 @@ def test_odd_gqa_ratios(hq, hkv, d, opts):
 @pytest.mark.parametrize("name", ["holes", "mixed", "long", "holes_g3"])
 @pytest.mark.parametrize("opts", [dict(), dict(decode_split=12.0, prefill_split=16.0)])
 def test_d64_prefill_workloads(name, opts):
-    """Head dim 64 (P in its own TMEM columns, S refilled while the softmax
-    works) on small hole-recompute, mixed and long-context shapes, with and
-    without split groups; rows near a sequence start take the residual pass
-    in S's columns."""
+    """Head dim 64 (the S MMAs rotate over three TMEM buffers, so a query
+    tile's next S is computed while its softmax still works) on small
+    hole-recompute, mixed and long-context shapes, with and without split
+    groups; rows near a sequence start take the residual pass in S's
+    columns."""
     if name == "holes":
         wl = W.hole_recompute(seed=41, num_seqs=2, cached_blocks=64, evict_blocks=16, hole_range=(2, 6),
                               turn_tokens=72, hq=8, hkv=2, d=64)
@@ -278,17 +281,21 @@ def test_d64_prefill_workloads(name, opts):
     compare(out, lse, ro, rl, f"D=64 {name} {opts}")
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("shape", ["rising", "falling", "spikes"])
-def test_running_max_moves(shape):
+def test_running_max_moves(shape, d):
     """Scores far from N(0,1): keys whose scores rise along the sequence (the
     running max moves up by more than the lazy-rescale threshold many times,
     so O is rescaled in TMEM and in registers), fall (the first keys dominate
     and later probabilities underflow), or carry a few large outliers.  q is
     made positive and K[t] = a(t) + 0.25 N(0,1), so the score of key t is
-    about a(t) * 0.8 * sqrt(D) = 9 a(t); a(t) stays <= 3.5 (lse up to ~40),
-    where fp32 accumulation in the MMA still meets the lse bound."""
+    about a(t) * 0.8 * sqrt(D); a(t) stays <= 3.5 sqrt(128 / D), so the
+    score stays <= ~32 (lse up to ~40), where fp32 accumulation in the MMA
+    still meets the lse bound.  At D = 64 the O rescales wait for the PV of
+    the previous tile, which can still be in flight there (the S MMAs rotate
+    over three TMEM buffers)."""
     wl = W.custom([1500, 700], [[20, 44, 30], [10, 34]], [[(0, 260), (1490, 1501)], [(600, 700), (700, 701)]],
-                  hq=8, hkv=2, seed=13)
+                  hq=8, hkv=2, d=d, seed=13)
     k, v, q = W.make_values(wl)
     g = torch.Generator().manual_seed(5)
     T = k.shape[0]
@@ -296,13 +303,14 @@ def test_running_max_moves(shape):
     for s in range(wl.num_seqs):
         a, b = int(wl.kv_indptr[s]), int(wl.kv_indptr[s + 1])
         t[a:b] = torch.linspace(0.0, 1.0, b - a)
+    top = 3.5 * (128.0 / d) ** 0.5
     if shape == "rising":
-        amp = 3.5 * t
+        amp = top * t
     elif shape == "falling":
-        amp = 3.5 * (1.0 - t)
+        amp = top * (1.0 - t)
     else:
         amp = torch.zeros(T)
-        amp[torch.randint(0, T, (40,), generator=g)] = 3.5
+        amp[torch.randint(0, T, (40,), generator=g)] = top
     k = (amp[:, None, None] + 0.25 * torch.randn(k.shape, generator=g)).to(torch.bfloat16)
     q = q.float().abs().to(torch.bfloat16)
     out, lse, _ = run_gpu(wl, k, v, q)
