@@ -34,7 +34,11 @@
  *     never allocates device memory.  The plan is a library-owned host
  *     object; the workspace it needs is caller-allocated device memory.
  *   - Device work is asynchronous on the given stream (a cudaStream_t; NULL
- *     is the legacy default stream).
+ *     is the legacy default stream) and keeps stream order.  msa_append_kv
+ *     and decode-only attention launches use programmatic dependent launch:
+ *     such a kernel may be scheduled while the kernel before it in the stream
+ *     is still running, but touches no memory until that one has completed,
+ *     so stream order holds for the caller as with plain launches.
  *   - bf16 means IEEE bfloat16 (2 bytes).  Layouts are row-major, C order.
  *   - Pool layout ("NHD"): K and V pools are bf16 [pool_tokens, Hkv, D];
  *     pool row = physical_block * block_size + offset_in_block.  A segment of

@@ -22,6 +22,12 @@ __global__ void __launch_bounds__(256) append_kv_kernel(const uint4* __restrict_
                                                         uint4* __restrict__ k_pool, uint4* __restrict__ v_pool,
                                                         int64_t pool_tokens, int32_t row_chunks,
                                                         int32_t* error_word) {
+    // Launched with programmatic stream serialization: the next kernel (the
+    // step's attention launch) may start its launch and set-up now, and this
+    // one touches nothing before the kernels ahead of it in the stream have
+    // finished.
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < n; t += warps) {
@@ -54,10 +60,19 @@ int launch_append_kv(const void* k_new, const void* v_new, const int64_t* slot, 
     int64_t blocks = ((int64_t)n + warps_per_block - 1) / warps_per_block;
     const int64_t cap = (int64_t)sms * 8;  // 8 resident blocks of 256 threads per SM
     if (blocks > cap) blocks = cap;
-    append_kv_kernel<<<(unsigned)blocks, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot, n, static_cast<uint4*>(k_pool),
-        static_cast<uint4*>(v_pool), pool_tokens, row_chunks, error_word);
-    return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, append_kv_kernel, static_cast<const uint4*>(k_new),
+                                             static_cast<const uint4*>(v_new), slot, n, static_cast<uint4*>(k_pool),
+                                             static_cast<uint4*>(v_pool), pool_tokens, row_chunks, error_word);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 // The transpose of the scatter: k_out[t] = k_pool[slot[t]] (and V).  It is

@@ -87,6 +87,14 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, 
     }
 }
 
+// Programmatic dependent launch.  pdl_trigger: the next kernel of the
+// stream (launched with programmatic stream serialization) may be scheduled
+// once every CTA of this grid has issued it or exited.  pdl_wait: wait until
+// the grids this one depends on have completed and their memory operations
+// are visible; a no-op for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
