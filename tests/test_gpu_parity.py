@@ -451,6 +451,64 @@ def test_cuda_graph_replay_equals_eager(idx):
         sess.close()
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_append_then_decode_attention_back_to_back(d):
+    """The serving step's order, issued back to back with no synchronisation:
+    append a new last token into every sequence's pool rows, then a
+    decode-only attention launch whose rows see it, four times over with
+    different values for that token and an output buffer per step.  Both
+    kernels are programmatic dependents of the kernel before them and wait
+    for it before touching memory; every step's result must be the one of
+    its own appended values (the new key is made to dominate its row's
+    softmax, and its row held NaN before the first append).  This checks
+    the results of the serving order, not the wait as such: an append of
+    12 rows ends long before the attention's first K/V loads, so a kernel
+    copy without the wait passed it too."""
+    dev = torch.device("cuda")
+    wl = W.batched_decode(seed=61, num_seqs=12, len_range=(300, 2500), max_seg=4, pool_tokens=1 << 16,
+                          hq=16, hkv=4, d=d)
+    k, v, q = W.make_values(wl)
+    last = torch.as_tensor([int(wl.kv_indptr[s + 1]) - 1 for s in range(wl.num_seqs)])
+    slot = torch.as_tensor([int(wl.block_table[s][(int(wl.seq_lens[s]) - 1) // 16]) * 16 +
+                            (int(wl.seq_lens[s]) - 1) % 16 for s in range(wl.num_seqs)], dtype=torch.int64)
+    k0, v0 = k.clone(), v.clone()
+    k0[last] = float("nan")
+    v0[last] = float("nan")
+    kp, vp = W.make_pool(wl, k0.to(dev), v0.to(dev))
+    sess = MsaSession.from_workload(wl)
+    try:
+        assert sess.info["num_prefill_items"] == 0
+        g = torch.Generator().manual_seed(62)
+        G = wl.num_q_heads // wl.num_kv_heads
+        steps = []
+        for i in range(4):
+            # a key along the sum of the row's query heads of its kv head:
+            # score about 10, so the new token carries most of the weight
+            qs = q.float().view(wl.num_seqs, wl.num_kv_heads, G, d).sum(2)
+            kn = (20.0 * qs / qs.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+            vn = torch.randn((wl.num_seqs, wl.num_kv_heads, d), generator=g).to(torch.bfloat16) * (i + 1)
+            steps.append((kn, vn))
+        outs = []
+        qd, slot_d = q.to(dev), slot.to(dev)
+        new = [(kn.to(dev).contiguous(), vn.to(dev).contiguous()) for kn, vn in steps]
+        for kn, vn in new:
+            append_kv(kn, vn, slot_d, kp, vp, sess.dims)
+            out = torch.empty((wl.num_q_rows, wl.num_q_heads, d), dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((wl.num_q_rows, wl.num_q_heads), dtype=torch.float32, device=dev)
+            sess.attention(qd, kp, vp, out=out, lse=lse)
+            outs.append((out, lse))
+        torch.cuda.synchronize()
+        assert sess.check_device()[0] == 0
+        for i, ((kn, vn), (out, lse)) in enumerate(zip(steps, outs)):
+            ki, vi = k.clone(), v.clone()
+            ki[last] = kn
+            vi[last] = vn
+            ro, rl = oracle_ref(wl, ki, vi, q)
+            compare(out, lse, ro, rl, f"append + attention step {i} D={d}")
+    finally:
+        sess.close()
+
+
 def test_two_sessions_on_two_streams_at_once():
     """Plans with their own workspaces launched on two streams without
     ordering between them (a decode batch and a hole-recompute batch, split
