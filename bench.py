@@ -7,7 +7,10 @@ appended into the paged pool (msa_append_kv) and attention of every query
 row over all segments of all sequences in one persistent launch
 (msa_attention).  The plan (segments + balanced work list) is built once per
 batch on the host and uploaded before the timed region; its host cost is
-reported as plan_us.  The e2e figure rebuilds and uploads the plan from host
+reported as plan_us.  The K timed steps are issued back to back with CUDA
+events at their ends only; the attention kernel's own duration (the
+roofline's denominator) comes from a second pass of K steps with an event
+pair around each attention launch.  The e2e figure rebuilds and uploads the plan from host
 arrays every step and copies the step's inputs/outputs through pinned host
 memory.
 
