@@ -403,12 +403,13 @@ def test_random_workloads_match_oracle(seed):
     compare(out, lse, ro, rl, f"random {seed}: {wl.num_q_heads}/{wl.num_kv_heads} heads, D={wl.head_dim}, {opts}")
 
 
-@pytest.mark.parametrize("idx", [3, 5])
+@pytest.mark.parametrize("idx", [2, 3, 5])
 def test_cuda_graph_replay_equals_eager(idx):
     """append + attention captured once in a CUDA graph and replayed: the
     calls neither synchronise nor allocate, and the kernel resets its own
     queue and merge counters, so every replay gives the eager call's bits
-    (split groups included: many CTAs force them)."""
+    (split groups included: many CTAs force them).  The decode-only batch
+    (2) captures the append -> attention programmatic dependency as well."""
     wl = W.small_config(idx)
     k, v, q = W.make_values(wl)
     dev = torch.device("cuda")
