@@ -1510,7 +1510,14 @@ __device__ void compute(const AttnParams& p, uint8_t* smem, Ctl* ctl, int warp, 
                 ok = prefill_item<D, DEC>(p, smem, ctl, it, g, kv_cnt, sk, pvk, ok_cnt, cs, wg, warp, lane);
             } else {  // a one-head item: only the o_full phase and the ring positions move on
                 kv_cnt += it.pad;
-                if constexpr (Cfg<D, DEC>::kRot) sk += (uint32_t)it.pad;
+                if constexpr (Cfg<D, DEC>::kRot) {
+                    // The S buffers' barriers move on with this item's slots,
+                    // which are all warpgroup 0's: wait until the item is done,
+                    // so that this warpgroup's next wait on a buffer is at most
+                    // one phase ahead of it (a parity wait cannot tell further)
+                    sk += (uint32_t)it.pad;
+                    ok = wait_bar(p, ctl, &ctl->o_full, ok_cnt & 1, kErrTimeoutCompute);
+                }
                 ++ok_cnt;
             }
         }

@@ -281,6 +281,50 @@ def test_d64_prefill_workloads(name, opts):
     compare(out, lse, ro, rl, f"D=64 {name} {opts}")
 
 
+@pytest.mark.parametrize("num_sms", [1, 3])
+@pytest.mark.parametrize("name", ["holes", "holes_g3", "mixed"])
+def test_d64_many_items_per_cta(name, num_sms):
+    """Head dim 64 on one or three CTAs, so that every CTA walks many items:
+    the rotation of the three S buffers runs on across items (slots counted
+    across them), through one-query-tile items (G = 3) and, in the mixed
+    batch, past decode items that the same CTAs run in between."""
+    if name == "holes":
+        wl = W.hole_recompute(seed=45, num_seqs=2, cached_blocks=64, evict_blocks=16, hole_range=(2, 6),
+                              turn_tokens=72, hq=8, hkv=2, d=64)
+    elif name == "holes_g3":
+        wl = W.hole_recompute(seed=46, num_seqs=2, cached_blocks=48, evict_blocks=12, hole_range=(2, 5),
+                              turn_tokens=100, hq=6, hkv=2, d=64)
+    else:
+        wl = W.mixed_batch(seed=47, num_decode=6, num_prefill=2, chunk=200, median=600, cap=3000, max_seg=8,
+                           hq=16, hkv=2, d=64)
+    k, v, q = W.make_values(wl)
+    out, lse, info = run_gpu(wl, k, v, q, num_sms=num_sms)
+    assert info["grid"] == num_sms and info["num_prefill_items"] > 4 * num_sms
+    ro, rl = oracle_ref(wl, k, v, q)
+    compare(out, lse, ro, rl, f"D=64 {name} on {num_sms} CTAs")
+
+
+def test_full_size_d64_hole_recompute_sampled():
+    """The bench's head-dim-64 prefill shape (16 sequences of 8,192 cached
+    tokens with 25 % recomputed in holes plus a 512-token turn, 32/8 heads)
+    at full size, under the plan the bench times, checked on sampled rows:
+    ~34 items per CTA through the rotating S buffers."""
+    from kv_cache_segment_gb300 import costfit
+    params = costfit.load_params()
+    opts = dict(choose_with=params) if params is not None else {}
+    wl = W.hole_recompute(seed=1003, hq=32, hkv=8, d=64)
+    dev = torch.device("cuda")
+    k, v, q = W.make_values(wl, device=dev)
+    out, lse, info = run_gpu(wl, k, v, q, **opts)
+    assert info["num_prefill_items"] > 20 * info["grid"]
+    rng = np.random.default_rng(1003)
+    rows = _sample_rows(wl, rng, per_seq=4)
+    rows = rows[rng.permutation(len(rows))[:48]]
+    rows.sort()
+    ro, rl = oracle_ref(wl, k.cpu(), v.cpu(), q.cpu(), rows=rows)
+    compare(out[torch.as_tensor(rows, device=dev)], lse[torch.as_tensor(rows, device=dev)], ro, rl, wl.name)
+
+
 @pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("shape", ["rising", "falling", "spikes"])
 def test_running_max_moves(shape, d):
