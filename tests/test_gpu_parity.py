@@ -281,27 +281,38 @@ def test_d64_prefill_workloads(name, opts):
     compare(out, lse, ro, rl, f"D=64 {name} {opts}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("num_sms", [1, 3])
-@pytest.mark.parametrize("name", ["holes", "holes_g3", "mixed"])
-def test_d64_many_items_per_cta(name, num_sms):
-    """Head dim 64 on one or three CTAs, so that every CTA walks many items:
-    the rotation of the three S buffers runs on across items (slots counted
-    across them), through one-query-tile items (G = 3) and, in the mixed
-    batch, past decode items that the same CTAs run in between."""
+@pytest.mark.parametrize("name", ["holes", "holes_g3", "mixed", "decode_split"])
+def test_many_items_per_cta(name, num_sms, d):
+    """One or three CTAs, so that every CTA walks many items and all state
+    carried from item to item is exercised: at D = 64 the rotation of the
+    three S buffers (slots counted across items), through one-query-tile
+    items (G = 3, where warpgroup 1 sits items out) and, in the mixed batch,
+    past decode items that the same CTAs run in between; at both head
+    dimensions the O hand-over between items, the stage rings, and in the
+    decode-only launch the merge warp's hand-offs and split groups merged by
+    the last of their parts."""
+    opts = {}
     if name == "holes":
         wl = W.hole_recompute(seed=45, num_seqs=2, cached_blocks=64, evict_blocks=16, hole_range=(2, 6),
-                              turn_tokens=72, hq=8, hkv=2, d=64)
+                              turn_tokens=72, hq=8, hkv=2, d=d)
     elif name == "holes_g3":
         wl = W.hole_recompute(seed=46, num_seqs=2, cached_blocks=48, evict_blocks=12, hole_range=(2, 5),
-                              turn_tokens=100, hq=6, hkv=2, d=64)
-    else:
+                              turn_tokens=100, hq=6, hkv=2, d=d)
+    elif name == "mixed":
         wl = W.mixed_batch(seed=47, num_decode=6, num_prefill=2, chunk=200, median=600, cap=3000, max_seg=8,
-                           hq=16, hkv=2, d=64)
+                           hq=16, hkv=2, d=d)
+    else:
+        wl = W.batched_decode(seed=48, num_seqs=6, len_range=(300, 2100), pool_tokens=1 << 16, hq=8, hkv=2, d=d)
+        opts = dict(decode_split=12.0)
     k, v, q = W.make_values(wl)
-    out, lse, info = run_gpu(wl, k, v, q, num_sms=num_sms)
-    assert info["grid"] == num_sms and info["num_prefill_items"] > 4 * num_sms
+    out, lse, info = run_gpu(wl, k, v, q, num_sms=num_sms, **opts)
+    assert info["grid"] == num_sms and info["num_items"] > 4 * num_sms
+    if name == "decode_split":
+        assert info["num_prefill_items"] == 0 and info["num_items"] > info["num_groups"]
     ro, rl = oracle_ref(wl, k, v, q)
-    compare(out, lse, ro, rl, f"D=64 {name} on {num_sms} CTAs")
+    compare(out, lse, ro, rl, f"D={d} {name} on {num_sms} CTAs")
 
 
 def test_full_size_d64_hole_recompute_sampled():
