@@ -458,6 +458,21 @@ def test_random_workloads_match_oracle(seed):
     compare(out, lse, ro, rl, f"random {seed}: {wl.num_q_heads}/{wl.num_kv_heads} heads, D={wl.head_dim}, {opts}")
 
 
+@pytest.mark.parametrize("seed", range(24))
+def test_random_workloads_on_few_ctas(seed):
+    """Seeded random workloads (as above, other seeds) on 1, 2 or 5 CTAs, so
+    that every CTA runs many items of mixed kinds, query-tile counts and
+    head dimensions back to back."""
+    wl, opts = random_workload(1000 + seed)
+    num_sms = (1, 2, 5)[seed % 3]
+    k, v, q = W.make_values(wl)
+    out, lse, info = run_gpu(wl, k, v, q, num_sms=num_sms, **opts)
+    assert info["grid"] == num_sms or info["num_items"] == 0
+    ro, rl = oracle_ref(wl, k, v, q)
+    compare(out, lse, ro, rl, f"random {1000 + seed} on {num_sms} CTAs: {wl.num_q_heads}/{wl.num_kv_heads} heads, "
+                              f"D={wl.head_dim}, {opts}")
+
+
 @pytest.mark.parametrize("idx", [2, 3, 5])
 def test_cuda_graph_replay_equals_eager(idx):
     """append + attention captured once in a CUDA graph and replayed: the
