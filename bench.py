@@ -1035,6 +1035,8 @@ def profile_main(args):
         wl = W.config(3)
     elif args.profile == "mixed":
         wl = W.config(5)
+    elif args.profile == "prefill64":  # the head-dim-64 prefill shape of prefill_shapes
+        wl = W.hole_recompute(seed=1003, hq=32, hkv=8, d=64)
     else:
         wl = W.long_context(seed=1004, num_seqs=1)
     case = Case(wl, dev, plan_opts=_plan_opts())
@@ -1059,7 +1061,7 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline only (no e2e, extras or CPU baseline)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--profile", choices=["decode", "prefill", "mixed", "long"], default=None,
+    ap.add_argument("--profile", choices=["decode", "prefill", "mixed", "long", "prefill64"], default=None,
                     help="run a small case for an ncu capture and exit")
     args = ap.parse_args()
     if args.warmup < 3:
