@@ -165,18 +165,23 @@ __device__ __forceinline__ bool wait_bar(const AttnParams& p, Ctl* ctl, uint64_t
     return false;
 }
 
-// Query tile k (0 or 1) of a prefill group: for G even the two tiles are
-// two query heads of one kv head over the same rows; for odd G they are two
-// consecutive 128-row tiles of one head.  Either way both share the group's
-// K/V tiles, so the two softmax warpgroups alternate on the tensor core.
+// Query tile k (0 or 1) of a prefill group: two query heads of one kv head
+// over the same <= 128 rows, or, for the last query head of a kv head when
+// G is odd, consecutive 128-row tiles of that one head.  Either way both share the group's K/V tiles, so the two softmax
+// warpgroups alternate on the tensor core.
+// A group of more than 128 rows is always the second form; one of at most
+// 128 rows has one tile in that form, where the two readings agree.
+__device__ __forceinline__ bool qtile_rows_mode(const AttnParams& p, const Group& g) {
+    return (p.G & 1) && g.nrows > kTileRows;
+}
 __device__ __forceinline__ int qtile_head(const AttnParams& p, const Group& g, int k) {
-    return g.head + ((p.G & 1) ? 0 : k);
+    return g.head + (qtile_rows_mode(p, g) ? 0 : k);
 }
 __device__ __forceinline__ int qtile_row0(const AttnParams& p, const Group& g, int k) {
-    return g.row0 + ((p.G & 1) ? k * kTileRows : 0);
+    return g.row0 + (qtile_rows_mode(p, g) ? k * kTileRows : 0);
 }
 __device__ __forceinline__ int qtile_rows(const AttnParams& p, const Group& g, int k) {
-    return (p.G & 1) ? min(kTileRows, g.nrows - k * kTileRows) : g.nrows;
+    return qtile_rows_mode(p, g) ? min(kTileRows, g.nrows - k * kTileRows) : g.nrows;
 }
 
 // Sum of the two bf16 values packed in w, as fp32 (exact).
@@ -1168,14 +1173,14 @@ __device__ bool residual_pass(const AttnParams& p, uint8_t* smem, Ctl* ctl, int 
 template <int D, bool DEC>
 __device__ bool prefill_item(const AttnParams& p, uint8_t* smem, Ctl* ctl, const Item& it, const Group& g,
                              uint32_t& kv_cnt, uint32_t& sk, uint32_t& pvk, uint32_t& ok_cnt, uint32_t& cs, int k,
-                             int warp, int lane) {
+                             int r0, int qrows, int head, int warp, int lane) {
     using C = Cfg<D, DEC>;
     const int quarter = warp & 3;
     const int ri = quarter * 32 + lane;  // tile row = TMEM lane
-    const int r0 = qtile_row0(p, g, k);  // first row of query tile k
-    const bool valid = ri < qtile_rows(p, g, k);
+    // r0 / qrows / head: first row, rows and query head of query tile k
+    // (computed by the caller)
+    const bool valid = ri < qrows;
     const int prow = valid ? p.pos[r0 + ri] : -1;
-    const int head = qtile_head(p, g, k);
     const uint32_t tlane = ctl->tmem_base + ((uint32_t)(quarter * 32) << 16);
     const uint32_t tO = tlane + C::kTmemO + k * D;  // O_k
     const int T = it.pad;
@@ -1507,7 +1512,8 @@ __device__ void compute(const AttnParams& p, uint8_t* smem, Ctl* ctl, int warp, 
             else kv_cnt += it.pad;
         } else if constexpr (!DEC) {
             if (wg < g.pad) {
-                ok = prefill_item<D, DEC>(p, smem, ctl, it, g, kv_cnt, sk, pvk, ok_cnt, cs, wg, warp, lane);
+                ok = prefill_item<D, DEC>(p, smem, ctl, it, g, kv_cnt, sk, pvk, ok_cnt, cs, wg, qtile_row0(p, g, wg),
+                                          qtile_rows(p, g, wg), qtile_head(p, g, wg), warp, lane);
             } else {  // a one-head item: only the o_full phase and the ring positions move on
                 kv_cnt += it.pad;
                 if constexpr (Cfg<D, DEC>::kRot) {

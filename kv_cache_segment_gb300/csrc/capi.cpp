@@ -108,8 +108,10 @@ int msa_plan_get_items(msa_plan_t plan, int32_t* items, int32_t* n_items) {
             const msa::Item& it = plan->items[i];
             const msa::Group& g = plan->groups[it.group];
             int32_t* o = items + 9 * i;
-            // query heads covered: G (decode); 2, or 1 over up to 256 rows when G is odd (prefill)
-            const int32_t heads = g.kind == msa::kPrefill && (plan->G & 1) ? 1 : g.pad;
+            // query heads covered: G (decode); prefill: 2 over <= 128 rows, or
+            // 1 over up to 256 rows (the last query head of a kv head, odd G)
+            const int32_t heads =
+                g.kind == msa::kPrefill && !(g.pad == 2 && g.nrows <= msa::kTileRows) ? 1 : g.pad;
             o[0] = g.kind; o[1] = g.seq; o[2] = g.head; o[3] = heads; o[4] = g.row0;
             o[5] = g.nrows; o[6] = it.kb; o[7] = it.ke; o[8] = it.part;
         }

@@ -28,8 +28,11 @@ struct Run {
 // An output group: the rows and heads one merge produces.
 //   decode : rows [row0, row0+nrows) x query heads [head*G, head*G+G), kv head = head
 //   prefill: `pad` query tiles of 128 rows x one head, all of one kv head:
-//            G even: rows [row0, row0+nrows) (<= 128) x heads [head, head+pad);
-//            G odd:  head `head` x rows [row0, row0+nrows) (<= 128 * pad),
+//            pad == 2, nrows <= 128: rows [row0, row0+nrows) x heads
+//                    [head, head+2) (every head for even G, all but the
+//                    last of each kv head for odd G);
+//            otherwise (the last query head of a kv head, odd G): head
+//                    `head` x rows [row0, row0+nrows) (<= 128 * pad),
 //                    tile k = rows [row0 + 128k, ...)
 // n_parts > 1 means the key range was split; parts write partials to slots
 // [slot, slot + n_parts) (two tile slots each for prefill) and the last to

@@ -297,25 +297,37 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
         if (n == 0) continue;
         const int32_t L = seq_lens[s];
         const int32_t ra = P->run_indptr[s], rb = P->run_indptr[s + 1];
-        auto add_groups = [&](int32_t kind, int32_t row0, int32_t nrows) {
+        // Groups over rows [row0, row0 + nrows).  decode: one group per kv
+        // head (all G query heads packed), Group.pad = G.  prefill: two
+        // query tiles of 128 rows x one head that share a kv head, Group.pad
+        // = the number of query tiles (1 or 2) -- `pairs`: query heads 2i
+        // and 2i + 1 of every kv head over <= 128 rows (all heads for even
+        // G, all but the last for odd G); otherwise the last query head of
+        // every kv head (odd G: no second head left to pair with) over two
+        // consecutive row tiles (<= 256 rows).  The kernel tells the two
+        // prefill forms apart by pad == 2 with nrows <= 128.
+        auto add_groups = [&](int32_t kind, int32_t row0, int32_t nrows, bool pairs) {
             const int32_t pmax = P->pos[row0 + nrows - 1];  // rows ascend within a sequence
             const int32_t ke = std::min(pmax + 1, L);
             const int64_t tiles = count_tiles(0, ke);
-            // decode: one group per kv head (all G query heads packed);
-            // prefill: two query tiles of 128 rows x one head that share a kv
-            // head -- a pair of query heads over <= 128 rows (G even), or one
-            // query head over two consecutive row tiles (G odd: no second
-            // head of the same kv head to pair with); Group.pad = G for
-            // decode, the number of query tiles (1 or 2) for prefill
-            const int32_t hpg = kind == kDecode ? G : (G % 2 == 0 ? 2 : 1);
-            const int32_t ngr = kind == kDecode ? Hkv : Hq / hpg;
-            const int32_t pad = kind == kDecode ? G : (G % 2 == 0 ? 2 : (nrows + kTileRows - 1) / kTileRows);
-            for (int32_t h = 0; h < ngr; ++h) {
+            auto push = [&](int32_t head, int32_t pad) {
                 Pending pd;
-                pd.g = Group{kind, s, kind == kDecode ? h : h * hpg, row0, nrows, 1, -1, pad};
+                pd.g = Group{kind, s, head, row0, nrows, 1, -1, pad};
                 pd.ke = ke;
                 pd.tiles = tiles;
                 pend.push_back(pd);
+            };
+            int32_t heads = 0;  // query heads these groups cover
+            if (kind == kDecode) {
+                for (int32_t h = 0; h < Hkv; ++h) push(h, G);
+                heads = Hq;
+            } else if (pairs) {
+                for (int32_t kv = 0; kv < Hkv; ++kv)
+                    for (int32_t i = 0; 2 * i + 1 < G; ++i) push(kv * G + 2 * i, 2);
+                heads = Hkv * (G - (G & 1));
+            } else {
+                for (int32_t kv = 0; kv < Hkv; ++kv) push(kv * G + G - 1, (nrows + kTileRows - 1) / kTileRows);
+                heads = Hkv;
             }
             if (kind == kDecode) {
                 dec_kv += (int64_t)ke * Hkv * D * 2 * 2;
@@ -323,20 +335,25 @@ int plan_create(const msa_dims* dims, int32_t num_seqs, int32_t max_blocks,
                 dec_rows_total += nrows;
             } else {
                 for (int32_t r = row0; r < row0 + nrows; ++r)
-                    prefill_flops += 4.0 * D * Hq * (double)std::min(P->pos[r] + 1, L);
-                pre_rows_total += nrows;
+                    prefill_flops += 4.0 * D * heads * (double)std::min(P->pos[r] + 1, L);
+                if (!pairs || G % 2 == 0) pre_rows_total += nrows;  // each row once
             }
         };
         if (n <= P->dec_rows) {
-            add_groups(kDecode, r0, n);
+            add_groups(kDecode, r0, n, false);
         } else {
             // 128-row tiles (the remainder too, unless the decode path takes
-            // it); for odd G two consecutive tiles form one group
+            // it); for odd G the last query head of each kv head takes two
+            // consecutive tiles per group
             const int32_t full = n / kTileRows, rem = n % kTileRows;
             const int32_t pre_rows = full * kTileRows + (rem > P->dec_rows ? rem : 0);
-            const int32_t span = G % 2 == 0 ? kTileRows : 2 * kTileRows;
-            for (int32_t a = 0; a < pre_rows; a += span) add_groups(kPrefill, r0 + a, std::min(span, pre_rows - a));
-            if (rem > 0 && rem <= P->dec_rows) add_groups(kDecode, r0 + full * kTileRows, rem);
+            if (G >= 2)
+                for (int32_t a = 0; a < pre_rows; a += kTileRows)
+                    add_groups(kPrefill, r0 + a, std::min(kTileRows, pre_rows - a), true);
+            if (G & 1)
+                for (int32_t a = 0; a < pre_rows; a += 2 * kTileRows)
+                    add_groups(kPrefill, r0 + a, std::min(2 * kTileRows, pre_rows - a), false);
+            if (rem > 0 && rem <= P->dec_rows) add_groups(kDecode, r0 + full * kTileRows, rem, false);
         }
     }
 

@@ -104,10 +104,13 @@ def _check_coverage(wl, plan, enumerate_keys=True):
             assert a[2] == b[1] and a[1] < a[2]
         if kind == 0:
             assert nrows * G <= 16
-        elif G % 2 == 0:
-            assert nh == 2 and nrows <= 128  # two heads of one kv head over one row tile
+        elif nh == 2:
+            # two heads of one kv head over one row tile; for odd G never the
+            # kv head's last query head
+            assert nrows <= 128 and (head % G) % 2 == 0 and (G % 2 == 0 or head % G <= G - 3)
         else:
-            assert nh == 1 and nrows <= 256  # one head over one or two row tiles
+            # odd G: the last query head of a kv head over one or two row tiles
+            assert G % 2 == 1 and head % G == G - 1 and nrows <= 256
     assert np.all(owner == 1)
     if enumerate_keys:
         # every visible key of every row is inside exactly one part's range
