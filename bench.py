@@ -911,7 +911,7 @@ def prefill_shapes_leg(dev, stream, peaks, steps, warm, rank):
         tf = case.flops() / (ms * 1e-3) / 1e12
         res.append({"hq": hq, "hkv": hkv, "head_dim": d, "G": hq // hkv, "attention_ms": round(ms, 4),
                     "prefill_tflops": round(tf, 1), "tensor_frac": round(tf / peaks["bf16_tflops"], 4),
-                    "items": int(case.info["num_items"])})
+                    "items": int(case.info["num_items"]), "model_predicted_us": _predict_us(case)})
         del case
         torch.cuda.empty_cache()
     return res
@@ -937,7 +937,7 @@ def decode_shapes_leg(dev, stream, peaks, steps, warm, rank):
         gbs = case.decode_bytes() / (ms * 1e-3) / 1e9
         res.append({"hq": hq, "hkv": hkv, "head_dim": d, "G": hq // hkv, "seqs": n, "attention_ms": round(ms, 4),
                     "decode_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
-                    "items": int(case.info["num_items"])})
+                    "items": int(case.info["num_items"]), "model_predicted_us": _predict_us(case)})
         del case
         torch.cuda.empty_cache()
     return res

@@ -188,7 +188,7 @@ int msa_plan_get_order(msa_plan_t plan, int32_t* order, int32_t* n_items);
  *
  * Each work item runs two phases on the CTA that takes it:
  *   fixed phase (time):
- *     decode : dec_item_us            prefill: pre_item_us + pre_tile_us * tiles * qtiles
+ *     decode : dec_item_us            prefill: pre_item_us + tile_us * tiles * qtiles
  *     + box_us * extra_boxes + dec_merge_us / pre_merge_us (if its group is
  *       split into parts: a decode part's partial is 16 rows, a prefill
  *       part's 128 rows x 1 or 2 heads, and the last part merges them all)
@@ -198,7 +198,11 @@ int msa_plan_get_order(msa_plan_t plan, int32_t* order, int32_t* n_items);
  *     CTAs share HBM and the last ones run faster.
  * tiles = 128-key windows the item walks; qtiles = the prefill item's query
  * tiles of 128 rows x one head (1 or 2: two heads of one kv head, or for an
- * odd Hq/Hkv one head over two consecutive row tiles); extra_boxes = TMA boxes beyond one per tile (a tile that is
+ * odd Hq/Hkv one head over two consecutive row tiles); tile_us = pre_tile_us *
+ * (1 - pre_tile_dfrac + pre_tile_dfrac * D / 128), the time of one (key tile x
+ * query tile) at head dim D: pre_tile_us is its time at D = 128, and the share
+ * pre_tile_dfrac of it (the MMAs, the K/V loads) scales with D while the rest
+ * (the softmax over 128 x 128 scores) does not; extra_boxes = TMA boxes beyond one per tile (a tile that is
  * not a full 128-key window inside one segment is fetched per segment piece,
  * a piece's whole 16-key blocks in boxes of 4, 2 and 1 blocks).  Items are
  * handed out in the plan's order to `grid` CTAs, a
@@ -214,10 +218,11 @@ typedef struct {
     double dec_gbs;      /* HBM bandwidth the decode streams share (GB/s)   */
     double dec_cta_gbs;  /* most one CTA streams on its own (GB/s)          */
     double pre_item_us;
-    double pre_tile_us;
+    double pre_tile_us;  /* (key tile x query tile) at head dim 128 (us)       */
     double box_us;
     double dec_merge_us;
     double pre_merge_us;
+    double pre_tile_dfrac; /* share of pre_tile_us proportional to D, in [0, 1] */
 } msa_cost_params;
 
 typedef struct {
@@ -244,11 +249,12 @@ int msa_plan_estimate(msa_plan_t plan, const msa_cost_params* params, msa_cost_e
  * cost, with weights alpha and beta set from the batch and the hardware).
  * For the sequence's n_blocks = ceil(seq_len / 16) cached blocks:
  *
- *   hole(b)    = pre_tile_us * Hq * (sum over b's positions p of
+ *   hole(b)    = tile_us * Hq * (sum over b's positions p of
  *                min(p + 1, seq_len)) / (128 * 128)
  *     the attention work of recomputing block b's own rows (4*D*Hq*sum
  *     min(p+1, L) flops: each row attends to every earlier key) in units of
- *     one 128x128 tile of one head, at the latency model's prefill rate.
+ *     one 128x128 tile of one head, at the latency model's prefill rate
+ *     (tile_us as in msa_plan_estimate, at dims->head_dim).
  *
  * The page holds two views of that cost, and the mode picks one:
  *   - hole reading (default): cost_us(b) = hole(b).  Only the evicted block
@@ -275,12 +281,12 @@ int msa_plan_estimate(msa_plan_t plan, const msa_cost_params* params, msa_cost_e
  *   mode       MSA_EVICT_LINEAR or MSA_EVICT_EXPECTED_COST, optionally ORed
  *              with MSA_EVICT_PREFIX_COST
  *   hit_prob   host float [n_blocks], each in [0, 1]
- *   params     latency-model constants (pre_tile_us is used)
+ *   params     latency-model constants (pre_tile_us and pre_tile_dfrac are used)
  *   evicted    host int32 [n_evict]
  *   cost_us    host double [n_blocks] or NULL: receives cost_us(b)
  * Returns MSA_ERR_INVALID_ARG for an unknown mode bit, n_evict outside [0,
- * n_blocks], a probability outside [0, 1], or negative or non-finite
- * weights.
+ * n_blocks], a probability outside [0, 1], negative or non-finite
+ * weights, or a pre_tile_dfrac outside [0, 1].
  */
 typedef enum {
     MSA_EVICT_LINEAR = 0,

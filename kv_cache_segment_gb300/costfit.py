@@ -12,11 +12,12 @@ this script gives that model its constants for this kernel and GPU.
 Training and validation workloads are synthetic, drawn with the same
 generators as the bench (decode batches of several sizes, lengths and
 segment counts; hole recompute, also at odd GQA ratios; long-context
-chunks; mixed batches; and the bench's four workloads at full size) at
+chunks; mixed batches; head dim 64 besides 128; and the bench's four
+workloads at full size) at
 different seeds and sizes for the two sets, each planned with three
 different split factors (msa_plan_create_ex).  Each plan is timed as the median of
 `--reps` launches of msa_attention alone (CUDA events on the launching
-stream, after warm-up launches).  The nine parameters are fitted by
+stream, after warm-up launches).  The ten parameters are fitted by
 bounded least squares on log(predicted / measured).
 """
 from __future__ import annotations
@@ -57,6 +58,11 @@ def training_set():
         s.append((f"long{i}", W.long_context(seed=2030 + i, num_seqs=1, length=length, n_runs=runs, chunk=chunk)))
     # odd Hq/Hkv: prefill items are two row tiles of one head
     s.append(("holes_g1", W.hole_recompute(seed=2026, num_seqs=8, cached_blocks=256, evict_blocks=64, hq=8, hkv=8)))
+    # head dim 64: the share of a prefill tile's time that scales with D
+    s.append(("holes_d64", W.hole_recompute(seed=2027, num_seqs=8, cached_blocks=512, evict_blocks=128, d=64)))
+    s.append(("long_d64", W.long_context(seed=2036, num_seqs=1, length=65536, n_runs=32, chunk=2048, d=64)))
+    s.append(("decode_d64", W.batched_decode(seed=2012, num_seqs=64, len_range=(2048, 16384), max_seg=8,
+                                             pool_tokens=1 << 21, d=64)))
     # launches the size of the bench's prefill workloads
     s.append(("holes_big", W.hole_recompute(seed=2025, num_seqs=16, cached_blocks=512, evict_blocks=128)))
     s.append(("long_big", W.long_context(seed=2035, num_seqs=2, length=98304, n_runs=48, chunk=2048)))
@@ -75,6 +81,8 @@ def validation_set():
     for i, (n, cb, ev) in enumerate([(4, 384, 96), (12, 512, 64)]):
         s.append((f"v_holes{i}", W.hole_recompute(seed=3010 + i, num_seqs=n, cached_blocks=cb, evict_blocks=ev)))
     s.append(("v_holes_g3", W.hole_recompute(seed=3012, num_seqs=6, cached_blocks=384, evict_blocks=96, hq=24, hkv=8)))
+    s.append(("v_holes_d64", W.hole_recompute(seed=3013, num_seqs=12, cached_blocks=384, evict_blocks=96, d=64)))
+    s.append(("v_mixed_d64", W.mixed_batch(seed=3032, num_decode=48, num_prefill=2, chunk=1024, d=64)))
     s.append(("v_long", W.long_context(seed=3020, num_seqs=2, length=49152, n_runs=32, chunk=1536)))
     for i, (nd, npf, chunk) in enumerate([(32, 2, 1024), (96, 3, 2048)]):
         s.append((f"v_mixed{i}", W.mixed_batch(seed=3030 + i, num_decode=nd, num_prefill=npf, chunk=chunk)))
@@ -126,15 +134,27 @@ def predict(plan, params):
 def fit(records, x0=None):
     """records: [(plan, measured_us)] -> params dict (least squares on logs)."""
     from scipy.optimize import least_squares
-    names = msa.COST_PARAM_NAMES
-    x0 = np.asarray(x0 if x0 is not None else [5.0, 2.0, 6400.0, 80.0, 5.0, 1.0, 0.02, 5.0, 20.0], float)
+    names = list(msa.COST_PARAM_NAMES)
+    x0 = np.asarray(x0 if x0 is not None else [5.0, 2.0, 6400.0, 80.0, 5.0, 1.0, 0.02, 5.0, 20.0, 0.5], float)
+    start = dict(zip(names, x0))
+    # pre_tile_dfrac only matters for prefill at a head dim other than 128;
+    # with no such record nothing determines it, and it stays 0 (the same
+    # tile time at every head dim)
+    fixed = {}
+    if all(predict(pl, dict(start, pre_tile_dfrac=0.0)) == predict(pl, dict(start, pre_tile_dfrac=1.0))
+           for pl, _ in records):
+        fixed["pre_tile_dfrac"] = 0.0
+    free = [k for k in names if k not in fixed]
+    # every constant is >= 0; pre_tile_dfrac is a share, <= 1
+    upper = np.array([1.0 if k == "pre_tile_dfrac" else np.inf for k in free])
 
     def resid(x):
-        p = dict(zip(names, x))
+        p = dict(zip(free, x), **fixed)
         return np.array([math.log(max(predict(pl, p), 1e-3) / t) for pl, t in records])
 
-    r = least_squares(resid, x0, bounds=(np.zeros(len(names)), np.full(len(names), np.inf)), x_scale="jac")
-    return dict(zip(names, (float(v) for v in r.x)))
+    r = least_squares(resid, np.array([start[k] for k in free]), bounds=(np.zeros(len(free)), upper), x_scale="jac")
+    got = dict(zip(free, (float(v) for v in r.x)), **fixed)
+    return {k: got[k] for k in names}
 
 
 def errors(records, params):

@@ -165,11 +165,17 @@ private:
 };
 
 bool params_ok(const msa_cost_params* c) {
-    const double prm[9] = {c->launch_us, c->dec_item_us, c->dec_gbs, c->dec_cta_gbs, c->pre_item_us,
-                           c->pre_tile_us, c->box_us, c->dec_merge_us, c->pre_merge_us};
+    const double prm[10] = {c->launch_us, c->dec_item_us, c->dec_gbs,     c->dec_cta_gbs,  c->pre_item_us,
+                            c->pre_tile_us, c->box_us, c->dec_merge_us, c->pre_merge_us, c->pre_tile_dfrac};
     for (double v : prm)
         if (!(v >= 0.0) || !std::isfinite(v)) return false;
-    return true;
+    return c->pre_tile_dfrac <= 1.0;
+}
+
+// Time of one (128-key tile x 128-row query tile) at head dim D: the share
+// pre_tile_dfrac of the D = 128 time scales with D, the rest does not.
+double tile_us(const msa_cost_params* c, int32_t head_dim) {
+    return c->pre_tile_us * (1.0 - c->pre_tile_dfrac + c->pre_tile_dfrac * (double)head_dim / 128.0);
 }
 
 int estimate(const msa_plan_s* P, const msa_cost_params* c, const BoxCounts& box_counts, msa_cost_estimate* e) {
@@ -177,6 +183,7 @@ int estimate(const msa_plan_s* P, const msa_cost_params* c, const BoxCounts& box
     msa_cost_estimate out{};
     std::vector<double> fixed(n, 0.0), bytes(n, 0.0);
     const double tile_bytes = 2.0 * kTileKeys * P->dims.head_dim * 2.0;  // K and V, bf16
+    const double t_tile = tile_us(c, P->dims.head_dim);
     for (size_t i = 0; i < n; ++i) {
         const msa::Item& it = P->items[i];
         const msa::Group& g = P->groups[it.group];
@@ -190,7 +197,7 @@ int estimate(const msa_plan_s* P, const msa_cost_params* c, const BoxCounts& box
             out.decode_tiles += tiles;
             out.stream_bytes += (int64_t)bytes[i];
         } else {
-            f = c->pre_item_us + c->pre_tile_us * (double)(tiles * g.pad);
+            f = c->pre_item_us + t_tile * (double)(tiles * g.pad);
             out.prefill_tile_heads += tiles * g.pad;
         }
         f += c->box_us * (double)boxes +
@@ -485,6 +492,8 @@ static int select_evictions(const msa_dims* dims, int32_t seq_len, const float* 
     const bool prefix = (mode & MSA_EVICT_PREFIX_COST) != 0;
     if (!(alpha >= 0.0) || !(beta >= 0.0) || !std::isfinite(alpha) || !std::isfinite(beta)) return MSA_ERR_INVALID_ARG;
     if (!(params->pre_tile_us >= 0.0) || !std::isfinite(params->pre_tile_us)) return MSA_ERR_INVALID_ARG;
+    if (!(params->pre_tile_dfrac >= 0.0 && params->pre_tile_dfrac <= 1.0)) return MSA_ERR_INVALID_ARG;
+    const double t_tile = tile_us(params, dims->head_dim);
     const int32_t nb = (seq_len + kBlock - 1) / kBlock;
     if (n_evict < 0 || n_evict > nb) return MSA_ERR_INVALID_ARG;
     if (nb > 0 && !hit_prob) return MSA_ERR_INVALID_ARG;
@@ -496,7 +505,7 @@ static int select_evictions(const msa_dims* dims, int32_t seq_len, const float* 
         const int64_t p0 = (int64_t)b * kBlock, p1 = std::min<int64_t>(p0 + kBlock, seq_len);
         // sum over p in [p0, p1) of min(p + 1, seq_len) = p + 1 (p < seq_len)
         const double keys = (double)((p0 + 1 + p1) * (p1 - p0) / 2);
-        cost[b] = params->pre_tile_us * dims->num_q_heads * keys / (double)(msa::kTileKeys * msa::kTileRows);
+        cost[b] = t_tile * dims->num_q_heads * keys / (double)(msa::kTileKeys * msa::kTileRows);
     }
     // prefix reading: evicting b leaves blocks b .. end to recompute
     if (prefix)

@@ -70,7 +70,7 @@ class msa_cost_params(ctypes.Structure):
                 ("dec_gbs", ctypes.c_double), ("dec_cta_gbs", ctypes.c_double),
                 ("pre_item_us", ctypes.c_double), ("pre_tile_us", ctypes.c_double),
                 ("box_us", ctypes.c_double), ("dec_merge_us", ctypes.c_double),
-                ("pre_merge_us", ctypes.c_double)]
+                ("pre_merge_us", ctypes.c_double), ("pre_tile_dfrac", ctypes.c_double)]
 
 
 class msa_cost_estimate(ctypes.Structure):
@@ -83,6 +83,13 @@ class msa_cost_estimate(ctypes.Structure):
 
 
 COST_PARAM_NAMES = tuple(name for name, _ in msa_cost_params._fields_)
+
+
+def _cost_params(d) -> msa_cost_params:
+    """msa_cost_params from a dict of its field names.  A set without
+    pre_tile_dfrac (one fitted with no head-dim term) prices a tile the same
+    at every head dim, i.e. pre_tile_dfrac = 0."""
+    return msa_cost_params(*[float(d.get(k, 0.0) if k == "pre_tile_dfrac" else d[k]) for k in COST_PARAM_NAMES])
 
 
 class msa_pending_prefill(ctypes.Structure):
@@ -217,7 +224,7 @@ def msa_plan_create_ex(dims: msa_dims, block_table, seq_lens, q_range_indptr, q_
     ranges = np.ascontiguousarray(q_ranges, np.int32).reshape(-1, 2)
     params = None
     if choose_with is not None:
-        params = msa_cost_params(*[float(choose_with[k]) for k in COST_PARAM_NAMES])
+        params = _cost_params(choose_with)
     opts = msa_plan_options(int(num_sms), float(decode_split), float(prefill_split),
                             ctypes.pointer(params) if params is not None else None)
     plan = ctypes.c_void_p()
@@ -243,7 +250,7 @@ def msa_choose_prefill_chunk(dims: msa_dims, block_table, seq_lens, q_range_indp
     indptr = np.ascontiguousarray(q_range_indptr, np.int32)
     ranges = np.ascontiguousarray(q_ranges, np.int32).reshape(-1, 2)
     pend = (msa_pending_prefill * max(1, len(pending)))(*[msa_pending_prefill(*map(int, p)) for p in pending])
-    c = msa_cost_params(*[float(params[k]) for k in COST_PARAM_NAMES])
+    c = _cost_params(params)
     opts = msa_plan_options(int(num_sms), float(decode_split), float(prefill_split), None)
     choice = msa_chunk_choice()
     cand = np.zeros(64, np.int32)
@@ -304,7 +311,7 @@ def msa_plan_get_order(plan) -> np.ndarray:
 def msa_plan_estimate(plan, params) -> dict:
     """Expected launch time and work features of a plan (see include/msa.h);
     `params` is a dict with the msa_cost_params field names."""
-    c = msa_cost_params(*[float(params[k]) for k in COST_PARAM_NAMES])
+    c = _cost_params(params)
     e = msa_cost_estimate()
     _check(load().msa_plan_estimate(plan, ctypes.byref(c), ctypes.byref(e)), "msa_plan_estimate")
     return {name: getattr(e, name) for name, _ in msa_cost_estimate._fields_}
@@ -319,7 +326,7 @@ def msa_select_evictions(dims: msa_dims, seq_len: int, hit_prob, alpha: float, b
     nb = -(-int(seq_len) // 16)
     ev = np.zeros(max(int(n_evict), 1), np.int32)
     cost = np.zeros(max(nb, 1), np.float64)
-    c = msa_cost_params(*[float(params[k]) for k in COST_PARAM_NAMES])
+    c = _cost_params(params)
     _check(lib.msa_select_evictions(ctypes.byref(dims), int(seq_len), hp.ctypes.data if hp.size else None,
                                     int(mode), float(alpha), float(beta), ctypes.byref(c), int(n_evict),
                                     ev.ctypes.data, cost.ctypes.data), "msa_select_evictions")

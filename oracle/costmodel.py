@@ -7,7 +7,7 @@ kernel's expected latency (MSA paper abstract; AsymCache explainer, "æ ¸å¿ƒæ–¹æ³
 queue:
 
   fixed phase (us)   dec_item                                 (decode)
-                   | pre_item + pre_tile * tiles * qtiles     (prefill)
+                   | pre_item + tile_us * tiles * qtiles      (prefill)
                      + box * extra_boxes
                      + dec_merge | pre_merge   [group split into parts]
   stream phase (B)   decode only: tiles * 128 * D * 2 * 2 (K and V, bf16),
@@ -15,6 +15,10 @@ queue:
   tiles        128-key windows [kb + 128 i, min(kb + 128 (i+1), ke))
   qtiles       query tiles of 128 rows x one head: ceil(rows / 128) x heads
                (two heads over <= 128 rows, or one head over <= 256 rows)
+  tile_us      pre_tile * ((1 - dfrac) + dfrac * D / 128): pre_tile is a
+               tile's time at head dim 128, of which the share dfrac (MMAs,
+               K/V loads) is proportional to D and the rest (the softmax of
+               128 x 128 scores) is not
   extra_boxes  per tile, the TMA boxes beyond one: a full 128-key window
                inside one segment is one box; any other tile is fetched per
                segment piece, a piece of b whole 16-key blocks in boxes of 4,
@@ -56,6 +60,13 @@ def _boxes(segs, t0, t1):
     return boxes
 
 
+def tile_us(params, head_dim):
+    """Time of one (128-key tile x 128-row query tile) at head dim D.  A
+    parameter set without pre_tile_dfrac has no head-dim term (dfrac 0)."""
+    dfrac = params.get("pre_tile_dfrac", 0.0)
+    return params["pre_tile_us"] * ((1.0 - dfrac) + dfrac * head_dim / 128.0)
+
+
 def estimate(items, order, block_table, seq_lens, grid, params, head_dim):
     """items: rows (kind, seq, head, heads, row0, nrows, kb, ke, part) as
     msa_plan_get_items returns them; order: msa_plan_get_order; params: dict
@@ -87,7 +98,7 @@ def estimate(items, order, block_table, seq_lens, grid, params, head_dim):
             out["decode_tiles"] += tiles
         else:
             qtiles = -(-nrows // TILE) * heads
-            f = params["pre_item_us"] + params["pre_tile_us"] * tiles * qtiles
+            f = params["pre_item_us"] + tile_us(params, head_dim) * tiles * qtiles
             b = 0.0
             out["prefill_tile_heads"] += tiles * qtiles
         merge = params["dec_merge_us"] if kind == 0 else params["pre_merge_us"]

@@ -11,8 +11,9 @@ two readings, and both are here:
   attention work of recomputing its own rows.  Row p attends to min(p + 1, L)
   keys, so the work is the sum of min(p + 1, L) over the block's rows, here
   in units of a 128x128 tile of one head, times Hq heads, at `pre_tile_us`
-  per tile and head.  It grows with position (the page: the cost depends
-  strongly on where the block sits).
+  per tile and head (the latency model's tile time at the attention's head
+  dim: oracle.costmodel.tile_us).  It grows with position (the page: the
+  cost depends strongly on where the block sits).
 * prefix reading: a block's cache is usable only with its whole prefix, so
   evicting block b leaves blocks b, b+1, ..., last to recompute; its cost is
   the sum of the hole costs of those blocks.  It falls with position, so the

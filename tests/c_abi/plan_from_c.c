@@ -35,7 +35,9 @@ int main(void) {
     CHECK(msa_plan_get_items(plan, NULL, &n_items));
     size_t ws = 0;
     CHECK(msa_plan_workspace_bytes(plan, &ws));
-    const msa_cost_params prm = {10.0, 2.0, 6000.0, 50.0, 5.0, 1.0, 0.0, 1.0, 40.0};
+    /* the last field, the share of a tile's time proportional to the head dim,
+     * changes nothing at D = 128 */
+    const msa_cost_params prm = {10.0, 2.0, 6000.0, 50.0, 5.0, 1.0, 0.0, 1.0, 40.0, 0.5};
     msa_cost_estimate est;
     CHECK(msa_plan_estimate(plan, &prm, &est));
     const float hit[3] = {0.9f, 0.1f, 0.5f};

@@ -5,11 +5,12 @@ against values worked out by hand here, on hand-built work lists: nothing in
 these pins calls the library.
 
 The model (MSA paper abstract; AsymCache explainer, "核心方法 2/3"): a work
-item costs a fixed phase (decode: dec_item; prefill: pre_item + pre_tile x
-tiles x heads; plus box x extra TMA boxes and, for a part of a split group, a
-merge constant) and, for decode, a stream of tiles x 128 x D x 2 B x 2 (K and
-V) bytes at min(per-CTA rate, shared rate / streaming CTAs); CTAs take items
-in queue order as they free up.  The eviction score: alpha x hit + beta x
+item costs a fixed phase (decode: dec_item; prefill: pre_item + tile x
+tiles x heads, tile = pre_tile x (1 - dfrac + dfrac x D / 128); plus box x
+extra TMA boxes and, for a part of a split group, a merge constant) and,
+for decode, a stream of tiles x 128 x D x 2 B x 2 (K and V) bytes at
+min(per-CTA rate, shared rate / streaming CTAs); CTAs take items in queue
+order as they free up.  The eviction score: alpha x hit + beta x
 cost / max cost, lowest first, ties to the lower block; or hit x cost.
 """
 from __future__ import annotations
@@ -76,6 +77,23 @@ def pin_row_pair_prefill_counts_two_tiles(oc):
     r = oc.estimate(items, [0, 1], tables, {0: 384, 1: 384}, 1, p, 128)
     assert r["prefill_tile_heads"] == 3 * 2 + 3 * 1
     assert _close(r["fixed_us"], 2 * p["pre_item_us"] + p["pre_tile_us"] * (6 + 3))
+
+
+def pin_tile_time_scales_with_head_dim(oc):
+    """pre_tile_dfrac = 5/8 of a tile's D = 128 time scales with D: one
+    prefill item of 3 key tiles x 2 heads costs pre_item + 6 x 0.875 = 8.75 us
+    at D = 128 and pre_item + 6 x 0.875 x (3/8 + 5/8 x 1/2) = 3.5 + 3.609375 us
+    at D = 64; a parameter set without the term prices D = 64 as D = 128."""
+    items = [_item(1, 0, 2, 0, 0, 384, nrows=128)]
+    tables, lens = {0: list(range(24))}, {0: 384}
+    p = dict(PARAMS, pre_tile_dfrac=0.625)
+    assert _close(oc.estimate(items, [0], tables, lens, 1, p, 128)["fixed_us"], 8.75)
+    assert _close(oc.estimate(items, [0], tables, lens, 1, p, 64)["fixed_us"], 7.109375)
+    assert _close(oc.estimate(items, [0], tables, lens, 1, PARAMS, 64)["fixed_us"], 8.75)
+    assert _close(oc.tile_us(p, 64), 0.6015625) and _close(oc.tile_us(p, 128), 0.875)
+    # all of a tile's time proportional to D halves it at D = 64; none of it, no change
+    assert _close(oc.tile_us(dict(p, pre_tile_dfrac=1.0), 64), 0.4375)
+    assert _close(oc.tile_us(dict(p, pre_tile_dfrac=0.0), 64), 0.875)
 
 
 def pin_queue_order(oc):
@@ -204,7 +222,7 @@ def pin_chunk_batch(oc):
 
 
 COST_PINS = [pin_one_cta_mixed_items, pin_split_prefill_pays_its_merge, pin_row_pair_prefill_counts_two_tiles,
-             pin_queue_order, pin_shared_bandwidth,
+             pin_tile_time_scales_with_head_dim, pin_queue_order, pin_shared_bandwidth,
              pin_equal_items_in_rounds, pin_tma_boxes, pin_recompute_flops, pin_chunk_candidates,
              pin_chunk_closed_form_optimum, pin_chunk_budget, pin_chunk_ties_to_the_larger, pin_chunk_batch]
 

@@ -50,6 +50,22 @@ def test_library_matches_oracle(wl_fn):
         assert lib[k] == pytest.approx(ref[k], rel=1e-9), k
 
 
+@pytest.mark.parametrize("dfrac", [0.0, 0.4, 1.0])
+@pytest.mark.parametrize("d", [64, 128])
+def test_library_matches_oracle_head_dim_term(d, dfrac):
+    """Prefill tiles priced at the plan's head dim (pre_tile_dfrac): library =
+    oracle on a mixed decode + prefill + odd-G work list at D = 64 and 128."""
+    wl = W.custom([700, 260, 90], [[4, 30, 10], [5, 12], [6]], [[(0, 300), (650, 701)], [(258, 261)], [(87, 91)]],
+                  hq=6, hkv=2, d=d, seed=12)
+    lib, ref, _ = _both(wl, dict(PARAMS, pre_tile_dfrac=dfrac))
+    assert lib["prefill_tile_heads"] == ref["prefill_tile_heads"] > 0
+    for k in ("fixed_us", "makespan_us", "time_us"):
+        assert lib[k] == pytest.approx(ref[k], rel=1e-9), k
+    if d == 128 or dfrac == 0.0:  # the term changes nothing there
+        base, _, _ = _both(wl, PARAMS)
+        assert lib["time_us"] == pytest.approx(base["time_us"], rel=1e-12)
+
+
 @pytest.mark.parametrize("num_sms", [1, 7, 1500])
 def test_library_matches_oracle_other_grids(num_sms):
     lib, ref, _ = _both(W.small_config(3), num_sms=num_sms)
@@ -215,20 +231,25 @@ def test_bad_cost_params_are_rejected():
             msa.msa_plan_estimate(plan, dict(FITTED, dec_gbs=-1.0))
         with pytest.raises(msa.MsaError):
             msa.msa_plan_estimate(plan, dict(FITTED, pre_tile_us=float("nan")))
+        for bad in (-0.1, 1.5, float("nan")):
+            with pytest.raises(msa.MsaError):
+                msa.msa_plan_estimate(plan, dict(FITTED, pre_tile_dfrac=bad))
     finally:
         msa.msa_plan_destroy(plan)
 
 
 def test_fit_recovers_known_constants():
     """costfit.fit on launch times generated by the model itself from known
-    constants (several workloads x split plans) finds constants that predict
-    those times to 1e-3; the ones the plans constrain well come back to 2 %."""
+    constants (several workloads x split plans, one of them prefill at head
+    dim 64) finds constants that predict those times to 1e-3; the ones the
+    plans constrain well come back to 2 %."""
     from kv_cache_segment_gb300 import costfit
     truth = dict(launch_us=20.0, dec_item_us=3.0, dec_gbs=7000.0, dec_cta_gbs=55.0, pre_item_us=5.0,
-                 pre_tile_us=0.9, box_us=0.01, dec_merge_us=1.5, pre_merge_us=40.0)
+                 pre_tile_us=0.9, box_us=0.01, dec_merge_us=1.5, pre_merge_us=40.0, pre_tile_dfrac=0.6)
     plans = []
     for wl in (W.small_config(2), W.small_config(3), W.small_config(5), W.config(2),
-               W.batched_decode(seed=9, num_seqs=64, len_range=(512, 4096), pool_tokens=1 << 20)):
+               W.batched_decode(seed=9, num_seqs=64, len_range=(512, 4096), pool_tokens=1 << 20),
+               W.hole_recompute(seed=9, num_seqs=4, cached_blocks=128, evict_blocks=32, d=64)):
         dims = msa.make_dims(wl.num_q_heads, wl.num_kv_heads, wl.head_dim, 16, wl.scale)
         for ds, ps in ((1.0, 1.0), (3.0, 4.0), (8.0, 8.0)):
             for sms in (152, 40):
@@ -239,8 +260,12 @@ def test_fit_recovers_known_constants():
         got = costfit.fit(records)
         err = costfit.errors(records, got)
         assert err["max_abs_rel_err"] < 1e-3, err
-        for k in ("launch_us", "pre_tile_us", "dec_gbs"):
+        for k in ("launch_us", "pre_tile_us", "dec_gbs", "pre_tile_dfrac"):
             assert got[k] == pytest.approx(truth[k], rel=0.02), (k, got[k])
+        # without a prefill at another head dim the share is held at 0
+        at128 = [r for r, p in zip(records, plans) if msa.msa_plan_estimate(p, dict(truth, pre_tile_dfrac=0.0))
+                 ["time_us"] == r[1]]
+        assert len(at128) < len(records) and costfit.fit(at128)["pre_tile_dfrac"] == 0.0
     finally:
         for p in plans:
             msa.msa_plan_destroy(p)

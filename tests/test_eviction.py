@@ -3,6 +3,7 @@ restatement in oracle/eviction.py and closed forms."""
 import numpy as np
 import pytest
 
+import oracle.costmodel as OC
 import oracle.eviction as OE
 from kv_cache_segment_gb300 import msa
 
@@ -16,7 +17,12 @@ def _dims(hq=32, hkv=8, d=128):
 
 @pytest.mark.parametrize("seed", range(24))
 def test_library_matches_oracle(seed):
+    """Random lengths, probabilities, weights and modes; every third case at
+    head dim 64 with part of a tile's time proportional to D, where the
+    costs take the latency model's tile time at that head dim."""
     rng = np.random.default_rng(seed)
+    d = 64 if seed % 3 == 1 else 128
+    params = dict(PARAMS, pre_tile_dfrac=0.55) if seed % 6 == 1 else PARAMS
     L = int(rng.integers(1, 5000))
     nb = -(-L // 16)
     hit = rng.random(nb).astype(np.float32)
@@ -26,8 +32,8 @@ def test_library_matches_oracle(seed):
     n = int(rng.integers(0, nb + 1))
     expected, prefix = seed % 3 == 2, seed % 4 >= 2
     mode = (msa.MSA_EVICT_EXPECTED_COST if expected else 0) | (msa.MSA_EVICT_PREFIX_COST if prefix else 0)
-    ev, cost = msa.msa_select_evictions(_dims(), L, hit, alpha, beta, PARAMS, n, mode=mode)
-    want, want_cost = OE.select_evictions(L, 32, hit, alpha, beta, PARAMS["pre_tile_us"], n, expected_cost=expected,
+    ev, cost = msa.msa_select_evictions(_dims(d=d), L, hit, alpha, beta, params, n, mode=mode)
+    want, want_cost = OE.select_evictions(L, 32, hit, alpha, beta, OC.tile_us(params, d), n, expected_cost=expected,
                                           prefix=prefix)
     assert ev.tolist() == want
     # the suffix sums may add in another order: equal to the last few ulps
@@ -115,3 +121,20 @@ def test_unknown_mode_is_rejected():
     with pytest.raises(msa.MsaError) as e:
         msa.msa_select_evictions(_dims(), 160, np.zeros(10, np.float32), 1.0, 1.0, PARAMS, 2, mode=4)
     assert e.value.status == msa.MSA_ERR_INVALID_ARG
+
+
+def test_block_cost_scales_with_the_head_dim_term():
+    """With pre_tile_dfrac = 0.5 a block's cost at D = 64 is 3/4 of its cost
+    at D = 128; without the term the two are equal; a share outside [0, 1] is
+    rejected."""
+    L = 10 * 16
+    hit = np.full(10, 0.5, np.float32)
+    p = dict(PARAMS, pre_tile_dfrac=0.5)
+    _, c128 = msa.msa_select_evictions(_dims(d=128), L, hit, 1.0, 1.0, p, 2)
+    _, c64 = msa.msa_select_evictions(_dims(d=64), L, hit, 1.0, 1.0, p, 2)
+    _, c64_flat = msa.msa_select_evictions(_dims(d=64), L, hit, 1.0, 1.0, PARAMS, 2)
+    assert np.allclose(c64, 0.75 * c128, rtol=1e-15, atol=0)
+    assert np.array_equal(c64_flat, c128)
+    for bad in (-0.5, 2.0):
+        with pytest.raises(msa.MsaError):
+            msa.msa_select_evictions(_dims(d=64), L, hit, 1.0, 1.0, dict(PARAMS, pre_tile_dfrac=bad), 2)

@@ -29,7 +29,15 @@ def test_eviction_oracle_pin(pin):
 
 # (module, name, text in the module, replacement)
 MUTATIONS = [
-    ("costmodel", "prefill_qtiles_dropped", 'params["pre_tile_us"] * tiles * qtiles', 'params["pre_tile_us"] * tiles'),
+    ("costmodel", "prefill_qtiles_dropped", "tile_us(params, head_dim) * tiles * qtiles",
+     "tile_us(params, head_dim) * tiles"),
+    ("costmodel", "tile_head_dim_ratio_inverted", "dfrac * head_dim / 128.0", "dfrac * 128.0 / head_dim"),
+    ("costmodel", "tile_fixed_share_dropped", "((1.0 - dfrac) + dfrac * head_dim / 128.0)",
+     "(dfrac * head_dim / 128.0)"),
+    ("costmodel", "tile_shares_swapped", "((1.0 - dfrac) + dfrac * head_dim / 128.0)",
+     "(dfrac + (1.0 - dfrac) * head_dim / 128.0)"),
+    ("costmodel", "tile_head_dim_ignored", "tile_us(params, head_dim) * tiles * qtiles",
+     'params["pre_tile_us"] * tiles * qtiles'),
     ("costmodel", "qtiles_ignore_rows", "qtiles = -(-nrows // TILE) * heads", "qtiles = heads"),
     ("costmodel", "stream_k_only", "tile_bytes = 2.0 * TILE * head_dim * 2.0", "tile_bytes = TILE * head_dim * 2.0"),
     ("costmodel", "bandwidth_not_shared", 'params["dec_gbs"] / n_stream', 'params["dec_gbs"]'),
