@@ -1501,11 +1501,10 @@ __device__ void compute(const AttnParams& p, uint8_t* smem, Ctl* ctl, int warp, 
         if (DEC || it.kind == kDecode) {
             // decode items run on warpgroup 0; warpgroup 1 only keeps count
             if (wg == 0) {
-                // half tiles (at most 8 live rows) in the decode-only kernel;
-                // the kernel with prefill items has no registers to spare for
-                // a second copy of the decode loop
-                if (DEC && g.nrows * p.G <= 8)
-                    ok = decode_item<D, DEC, DEC>(p, smem, ctl, ii, it, g, kv_cnt, cs, mg, cw, lane);
+                // half tiles for groups of at most 8 live rows (the bf16
+                // residual of P rides in rows 8..15 of the same MMAs)
+                if (g.nrows * p.G <= 8)
+                    ok = decode_item<D, DEC, true>(p, smem, ctl, ii, it, g, kv_cnt, cs, mg, cw, lane);
                 else
                     ok = decode_item<D, DEC, false>(p, smem, ctl, ii, it, g, kv_cnt, cs, mg, cw, lane);
             }
