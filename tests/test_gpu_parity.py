@@ -824,14 +824,11 @@ def test_chosen_prefill_chunk_step_matches_oracle(budget):
     compare(out, lse, ro, rl, f"chosen chunk {choice['chunk']}")
 
 
-@pytest.mark.parametrize("name", ["decode", "holes", "mixed", "long", "holes_d64"])
+@pytest.mark.parametrize("name", ["decode", "holes", "mixed", "long", "holes_d64", "mixed_d64"])
 def test_latency_model_predicts_measured_launches(name):
     """The shipped latency-model constants predict the measured launch time
     (back to back, as costfit measures and the bench times) of medium
-    workloads it was not fitted on within 10 %, prefill at head dims 128 and
-    64.  Mixed launches at head dim 64 are left out: their decode and prefill
-    items cost more together than apart, which the model does not price
-    (it predicts them 9-15 % short)."""
+    workloads it was not fitted on within 10 %, at head dims 128 and 64."""
     from kv_cache_segment_gb300 import costfit
     params = costfit.load_params()
     if params is None:
@@ -841,7 +838,8 @@ def test_latency_model_predicts_measured_launches(name):
           "holes": lambda: W.hole_recompute(seed=4002, num_seqs=6, cached_blocks=448, evict_blocks=96),
           "mixed": lambda: W.mixed_batch(seed=4003, num_decode=48, num_prefill=2, chunk=1536),
           "long": lambda: W.long_context(seed=4004, num_seqs=1, length=40960, n_runs=24, chunk=1024),
-          "holes_d64": lambda: W.hole_recompute(seed=4005, num_seqs=6, cached_blocks=448, evict_blocks=96, d=64)}[name]()
+          "holes_d64": lambda: W.hole_recompute(seed=4005, num_seqs=6, cached_blocks=448, evict_blocks=96, d=64),
+          "mixed_d64": lambda: W.mixed_batch(seed=4006, num_decode=48, num_prefill=2, chunk=1536, d=64)}[name]()
     us, sess = costfit.measure(wl, torch.device("cuda"), reps=9, splits=((0.0, 0.0),))[0]
     try:
         pred = msa.msa_plan_estimate(sess.plan, params)["time_us"]
